@@ -1,0 +1,335 @@
+"""Seeded synthetic inputs for the quantized lightning indexer (QLI).
+
+This module draws random tensors and lays them out in the paged index-K cache
+format. It holds none of the indexer's arithmetic (no visibility rule, no
+scoring, no selection): the CUDA path's tests and bench and the CPU oracle both
+consume what it produces, and each computes the indexer on its own.
+
+Layout facts used here come from the vllm-ascend developer guide
+"DeepSeek V4.1 QLI V2 与候选集成", section "数据流" (data flow):
+  * ratio-2 caches use a 64-row page view with a 131072-byte block stride,
+    ratio-1 caches a 128-row view with a 147712-byte stride;
+  * inside each page the INT8 index-K rows and their FP16 per-token scales are
+    packed after the KV rows.
+The KV row size (1024 B) is the reading that makes the ratio-1 stride exact:
+147712 = 128 * (1024 + 128 + 2). The blog "DeepSeek V4.1-Flash 登陆昇腾 ·
+需求故事（PR 16925）", section 四 (get_layer_tuples), states that the index K
+and its FP16 scale sit after the KV in the same page.
+
+Value distributions (INT8 uniform in [-127, 127], FP16 head weights N(0, 0.1),
+FP16 Q/K scales U(0.005, 0.02), shuffled page table with 10% spare pages) are
+the ones the decode workloads are specified with.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+D = 128                      # index head dimension
+KV_ROW_BYTES = 1024          # KV bytes per row that precede the index K in a page
+BLOCK = 8                    # compressed positions per candidate block
+GEOMETRY = {2: (64, 131072), 1: (128, 147712)}   # ratio -> (rows per page, page stride)
+CAND_MODES = {"none": 1, "source": 2, "consumer": 3}
+
+
+def page_offsets(rows_per_page: int) -> tuple:
+    """Byte offsets of the index-K rows and of the FP16 scales inside a page."""
+    k_off = rows_per_page * KV_ROW_BYTES
+    s_off = k_off + rows_per_page * D
+    return k_off, s_off
+
+
+def _fp16_bits(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x.astype(np.float16).view(np.uint16))
+
+
+def _rng(seed: int, stream: int) -> np.random.Generator:
+    # one independent stream per tensor, so a size change in one tensor does
+    # not reshuffle the others
+    return np.random.default_rng([int(seed), int(stream)])
+
+
+@dataclass
+class Case:
+    """One batch of indexer inputs, in host memory (numpy)."""
+    name: str
+    seed: int
+    N: int
+    ratio: int
+    rows_per_page: int
+    page_stride: int
+    k_offset: int
+    scale_offset: int
+    num_pages: int
+    q: np.ndarray                 # int8 [T, N, D]
+    cu_seqlens_q: np.ndarray      # int32 [B+1]
+    raw_lens: np.ndarray          # int64 [B] raw (uncompressed) context lengths
+    k_lens: np.ndarray            # int32 [B] compressed lengths
+    residual: Optional[np.ndarray]  # int32 [B] raw length mod ratio; None for ratio 1
+    k_rows: np.ndarray            # int8 [sum(k_lens), D], request-major, logical order
+    k_row_start: np.ndarray       # int64 [B+1] offsets of each request in k_rows
+    k_scale: np.ndarray           # uint16 [sum(k_lens)] FP16 bits
+    block_table: np.ndarray       # int32 [B, bt_stride]
+    head_weights: np.ndarray      # uint16 [T, N] FP16 bits
+    q_scale: np.ndarray           # uint16 [T, N] FP16 bits
+    topk: int
+    cand_mode: str
+    cand_blocks: int
+    cand_in: Optional[np.ndarray]  # int32 [T, 1, C] (consumer only)
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def T(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def B(self) -> int:
+        return int(self.k_lens.shape[0])
+
+    @property
+    def bt_stride(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def cand_mode_id(self) -> int:
+        return CAND_MODES[self.cand_mode]
+
+    def request_pages(self, b: int) -> int:
+        R = self.rows_per_page
+        return (int(self.k_lens[b]) + R - 1) // R
+
+    # -- page packing ---------------------------------------------------
+    def pack_pages_numpy(self, page_stride: Optional[int] = None,
+                         k_offset: Optional[int] = None,
+                         scale_offset: Optional[int] = None,
+                         filler: bool = True) -> np.ndarray:
+        """Paged cache as uint8 [num_pages, page_stride] in host memory.
+
+        With no arguments the case's own geometry is used. Passing a compact
+        geometry (for example stride R*130, k_offset 0, scale_offset R*128)
+        gives the same cache contents in less host memory.
+        """
+        stride = self.page_stride if page_stride is None else int(page_stride)
+        k_off = self.k_offset if k_offset is None else int(k_offset)
+        s_off = self.scale_offset if scale_offset is None else int(scale_offset)
+        R = self.rows_per_page
+        if filler:
+            pages = _rng(self.seed, 99).integers(0, 256, size=(self.num_pages, stride),
+                                                 dtype=np.uint8)
+        else:
+            pages = np.zeros((self.num_pages, stride), dtype=np.uint8)
+        for b in range(self.B):
+            L = int(self.k_lens[b])
+            rows = self.k_rows[self.k_row_start[b]:self.k_row_start[b] + L]
+            scl = self.k_scale[self.k_row_start[b]:self.k_row_start[b] + L]
+            for p in range(self.request_pages(b)):
+                pid = int(self.block_table[b, p])
+                n = min(R, L - p * R)
+                kb = rows[p * R:p * R + n].view(np.uint8).reshape(-1)
+                pages[pid, k_off:k_off + kb.size] = kb
+                sb = scl[p * R:p * R + n].view(np.uint8)
+                pages[pid, s_off:s_off + sb.size] = sb
+        return pages
+
+    def pack_pages_torch(self, device, filler: bool = True):
+        """Paged cache as a torch uint8 tensor [num_pages, page_stride] on `device`.
+
+        Filler bytes (the KV and alias parts of each page, never read by the
+        indexer) are drawn on the device from a seeded torch generator.
+        """
+        import torch
+        R, stride = self.rows_per_page, self.page_stride
+        pages = torch.empty((self.num_pages, stride), dtype=torch.uint8, device=device)
+        if filler:
+            g = torch.Generator(device=device)
+            g.manual_seed(int(self.seed) * 1000003 + 17)
+            pages.random_(0, 256, generator=g)
+        else:
+            pages.zero_()
+        krows = torch.from_numpy(self.k_rows.view(np.uint8)).to(device)
+        kscl = torch.from_numpy(self.k_scale.view(np.uint8).reshape(-1, 2)).to(device)
+        bt = torch.from_numpy(self.block_table.astype(np.int64)).to(device)
+        ko, so = self.k_offset, self.scale_offset
+        for b in range(self.B):
+            L = int(self.k_lens[b])
+            if L == 0:
+                continue
+            base = int(self.k_row_start[b])
+            full = L // R
+            if full:
+                ids = bt[b, :full]
+                src = krows[base:base + full * R].reshape(full, R * D)
+                pages[ids, ko:ko + R * D] = src
+                ssrc = kscl[base:base + full * R].reshape(full, R * 2)
+                pages[ids, so:so + R * 2] = ssrc
+            tail = L - full * R
+            if tail:
+                pid = int(self.block_table[b, full])
+                pages[pid, ko:ko + tail * D] = krows[base + full * R:base + L].reshape(-1)
+                pages[pid, so:so + tail * 2] = kscl[base + full * R:base + L].reshape(-1)
+        return pages
+
+    def k_rows_of(self, b: int) -> np.ndarray:
+        return self.k_rows[self.k_row_start[b]:self.k_row_start[b + 1]]
+
+    def k_scale_of(self, b: int) -> np.ndarray:
+        return self.k_scale[self.k_row_start[b]:self.k_row_start[b + 1]]
+
+
+def make_case(seed: int, raw_lens: Sequence[int], q_lens: Sequence[int], N: int,
+              ratio: int, topk: int, cand_mode: str = "none", cand_blocks: int = 0,
+              rows_per_page: Optional[int] = None, page_stride: Optional[int] = None,
+              spare: float = 0.10, bt_stride: Optional[int] = None,
+              cand_policy: str = "valid", cand_count: Optional[tuple] = None,
+              name: str = "case") -> Case:
+    """Build one batch.
+
+    raw_lens are raw context lengths S_b (the query tokens are the last q_len
+    raw positions of each request); k_lens = S_b // ratio and the residual is
+    S_b mod ratio (absent for ratio 1).
+
+    cand_policy (consumer mode only):
+      "valid": per token, distinct block IDs in [0, ceil(k_len/8)) that always
+               include the last one, shuffled, -1 padded; the valid count is
+               drawn from cand_count (default U[3C/4, C]).
+      "messy": as "valid" but with duplicates, IDs past the end, -1 holes in
+               the middle and sometimes without the last block.
+    """
+    if cand_mode not in CAND_MODES:
+        raise ValueError(cand_mode)
+    raw_lens = np.asarray(raw_lens, dtype=np.int64)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    B = raw_lens.size
+    assert q_lens.size == B
+    R_def, stride_def = GEOMETRY[ratio]
+    R = R_def if rows_per_page is None else int(rows_per_page)
+    stride = stride_def if page_stride is None else int(page_stride)
+    k_off, s_off = page_offsets(R)
+    if s_off + 2 * R > stride:
+        # a non-default row count: keep the packing order, grow the page
+        stride = ((s_off + 2 * R + 15) // 16) * 16
+    k_lens = (raw_lens // ratio).astype(np.int32)
+    residual = None if ratio == 1 else (raw_lens % ratio).astype(np.int32)
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    T = int(cu[-1])
+
+    q = _rng(seed, 1).integers(-127, 128, size=(T, N, D), dtype=np.int8)
+    total = int(k_lens.sum())
+    k_rows = _rng(seed, 2).integers(-127, 128, size=(total, D), dtype=np.int8)
+    k_scale = _fp16_bits(_rng(seed, 3).uniform(0.005, 0.02, size=total))
+    head_w = _fp16_bits(_rng(seed, 4).normal(0.0, 0.1, size=(T, N)))
+    q_scale = _fp16_bits(_rng(seed, 5).uniform(0.005, 0.02, size=(T, N)))
+    starts = np.zeros(B + 1, dtype=np.int64)
+    starts[1:] = np.cumsum(k_lens.astype(np.int64))
+
+    pages_per_req = (k_lens.astype(np.int64) + R - 1) // R
+    needed = int(pages_per_req.sum())
+    num_pages = max(1, int(np.ceil(needed * (1.0 + spare))))
+    perm = _rng(seed, 6).permutation(num_pages).astype(np.int32)
+    width = max(1, int(pages_per_req.max()) if B else 1)
+    if bt_stride is not None:
+        assert bt_stride >= width
+        width = int(bt_stride)
+    bt = np.zeros((B, width), dtype=np.int32)
+    cur = 0
+    for b in range(B):
+        n = int(pages_per_req[b])
+        bt[b, :n] = perm[cur:cur + n]
+        # unused slots hold a real page ID so that no entry is out of range
+        bt[b, n:] = perm[0]
+        cur += n
+
+    cand_in = None
+    if cand_mode in ("source", "consumer"):
+        if cand_blocks <= 0:
+            raise ValueError("candidate modes need cand_blocks")
+    if cand_mode == "consumer":
+        cand_in = _make_candidates(seed, cu, k_lens, cand_blocks, cand_policy, cand_count)
+
+    return Case(name=name, seed=int(seed), N=int(N), ratio=int(ratio), rows_per_page=R,
+                page_stride=stride, k_offset=k_off, scale_offset=s_off, num_pages=num_pages,
+                q=q, cu_seqlens_q=cu, raw_lens=raw_lens, k_lens=k_lens, residual=residual,
+                k_rows=k_rows, k_row_start=starts, k_scale=k_scale, block_table=bt,
+                head_weights=head_w, q_scale=q_scale, topk=int(topk), cand_mode=cand_mode,
+                cand_blocks=int(cand_blocks), cand_in=cand_in)
+
+
+def _make_candidates(seed, cu, k_lens, C, policy, count_range):
+    rng = _rng(seed, 7)
+    T = int(cu[-1])
+    out = np.full((T, 1, C), -1, dtype=np.int32)
+    for b in range(k_lens.size):
+        nblk = (int(k_lens[b]) + BLOCK - 1) // BLOCK
+        for t in range(int(cu[b]), int(cu[b + 1])):
+            if nblk == 0:
+                if policy == "messy":
+                    out[t, 0, :3] = [0, 5, 1 << 20]
+                continue
+            lo, hi = count_range if count_range else ((3 * C) // 4, C)
+            cnt = int(rng.integers(lo, hi, endpoint=True))
+            cnt = max(1, min(cnt, C, nblk))
+            others = rng.choice(nblk - 1, size=cnt - 1, replace=False) if cnt > 1 else []
+            ids = np.concatenate([np.asarray(others, dtype=np.int64), [nblk - 1]])
+            rng.shuffle(ids)
+            row = np.full(C, -1, dtype=np.int64)
+            row[:cnt] = ids
+            if policy == "messy":
+                # duplicates, IDs past the end, -1 holes, sometimes no last block
+                k = max(1, C // 16)
+                pos = rng.choice(C, size=k, replace=False)
+                src = rng.integers(0, max(1, cnt), size=k)
+                row[pos[: k // 2]] = row[src[: k // 2]]
+                row[pos[k // 2:]] = -1
+                if C > cnt:
+                    row[cnt] = nblk + int(rng.integers(0, 100))
+                if rng.random() < 0.3:
+                    row[row == nblk - 1] = -1
+            out[t, 0, :] = row
+    return out
+
+
+# -- the five workloads ------------------------------------------------------
+
+CONFIG_NAMES = {
+    1: "decode-b1-r2-ctx2048-n64-topk512-none",
+    2: "decode-b64-r1-ctxU8K..32K-n64-topk2048-none",
+    3: "prefill-t4096-2x2048-r2-ctx64K-n64-source2048-topk2048",
+    4: "consumer-decode-b32-r2-ctxU32K..128K-n32-cand1024-topk2048",
+    5: "longctx-decode-8x1M+4x4K-r2-n64-source2048-topk2048",
+}
+
+
+def config(idx: int, seed: Optional[int] = None) -> Case:
+    """The five workloads the indexer is measured on (seeds 0..4 by default)."""
+    s = idx - 1 if seed is None else int(seed)
+    if idx == 1:
+        return make_case(s, [2048], [1], N=64, ratio=2, topk=512, cand_mode="none",
+                         name=CONFIG_NAMES[1])
+    if idx == 2:
+        raw = _rng(s, 0).integers(8192, 32768, size=64, endpoint=True)
+        return make_case(s, raw, [1] * 64, N=64, ratio=1, topk=2048, cand_mode="none",
+                         name=CONFIG_NAMES[2])
+    if idx == 3:
+        return make_case(s, [65536, 65536], [2048, 2048], N=64, ratio=2, topk=2048,
+                         cand_mode="source", cand_blocks=2048, name=CONFIG_NAMES[3])
+    if idx == 4:
+        raw = _rng(s, 0).integers(32768, 131072, size=32, endpoint=True)
+        return make_case(s, raw, [1] * 32, N=32, ratio=2, topk=2048, cand_mode="consumer",
+                         cand_blocks=1024, cand_count=(768, 1024), name=CONFIG_NAMES[4])
+    if idx == 5:
+        raw = []
+        for b in range(12):
+            raw.append(4096 if b % 3 == 2 else 1 << 20)
+        return make_case(s, raw, [1] * 12, N=64, ratio=2, topk=2048, cand_mode="source",
+                         cand_blocks=2048, name=CONFIG_NAMES[5])
+    raise ValueError(idx)
+
+
+def workload_pairs_upper(case: Case) -> int:
+    """Sum over requests of q_len * k_len: an upper bound on scored pairs that
+    needs no knowledge of the causal rule (used only to size samples)."""
+    q_lens = np.diff(case.cu_seqlens_q).astype(np.int64)
+    return int((q_lens * case.k_lens.astype(np.int64)).sum())
