@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Throughput bench of the quantized lightning indexer on one or more GB300s.
+
+A step is one full indexer call (plan, score, select) over one batch of the
+chosen workload, with every input resident in HBM. The metric is scored
+(query, position) pairs per second. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Multi-GPU (torchrun, one process per GPU): independent replicas, no data
+exchange; the per-rank times are reduced with a max and the pairs summed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_indexer_qli_gb300 import synth  # noqa: E402
+
+METRIC = "QLI scored (query,position) pairs/s; % of HBM (decode) / INT8 (prefill) roof"
+UNIT = "pairs/s"
+L2_BYTES = 129 * 1024 * 1024
+ROTATE_SETS = {1: 1, 2: 3, 3: 1, 4: 8, 5: 1}   # input sets cycled so a step never hits L2
+SCORE_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_score.cu")
+
+
+# ---------------------------------------------------------------- accounting
+
+def visible(case, t, b):
+    """Visible compressed positions of token t (bench accounting only)."""
+    c0, c1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+    lk = int(case.k_lens[b])
+    res = 0 if case.residual is None else int(case.residual[b])
+    seen = lk * case.ratio + res - (c1 - c0) + (t - c0) + 1
+    return 0 if seen <= 0 else min(lk, seen // case.ratio)
+
+
+def pairs_of(case) -> int:
+    """Scored pairs of one step: sum over tokens of the eligible positions."""
+    total = 0
+    for b in range(case.B):
+        for t in range(int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])):
+            V = visible(case, t, b)
+            if case.cand_mode == "consumer":
+                nb = (V + 7) // 8
+                ids = np.unique(case.cand_in[t, 0])
+                ids = ids[(ids >= 0) & (ids < nb)]
+                total += int(np.minimum(8, V - 8 * ids).sum())
+            else:
+                total += V
+    return total
+
+
+def score_algorithmic_bytes(case, pairs: int) -> int:
+    """Bytes the score kernel must move per launch: 130 B per pair (INT8 K row
+    + FP16 K scale), each query's N*128 INT8 Q bytes and 4N bytes of FP16
+    weights and scales, and one 4-byte block-table entry per page touched."""
+    pages = sum(case.request_pages(b) for b in range(case.B))
+    return 130 * pairs + case.T * case.N * (128 + 4) + 4 * pages
+
+
+def step_bytes_in(case) -> int:
+    n = case.q.nbytes + case.cu_seqlens_q.nbytes + case.k_lens.nbytes + case.block_table.nbytes
+    n += case.head_weights.nbytes + case.q_scale.nbytes
+    n += 0 if case.residual is None else case.residual.nbytes
+    n += 0 if case.cand_in is None else case.cand_in.nbytes
+    return int(n)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """Per-launch DRAM traffic of the score kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_decode_b64_r1.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
+    h = re.search(r"score_source_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(SCORE_SRC, "rb").read()).hexdigest()
+    return int(m.group(1)) if h.group(1) == cur else None
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    import torch
+    torch.cuda.synchronize()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_rate(case, budget_s: float, rows_per_chunk: int):
+    """Times the oracle, as it stands, on successive row chunks of the
+    workload until `budget_s` of work is done; returns (pairs/s, rows, cores)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    prep = oracle.prepare(case)
+    order = np.random.default_rng(12345).permutation(case.T)
+    done_pairs, done_rows, spent = 0, 0, 0.0
+    i = 0
+    while spent < budget_s and i < case.T:
+        rows = order[i:i + rows_per_chunk]
+        i += rows.size
+        t0 = time.perf_counter()
+        out = oracle.run(prep, rows=rows, nthreads=cores)
+        spent += time.perf_counter() - t0
+        done_rows += rows.size
+        if case.cand_mode == "consumer":
+            sub = 0
+            for r, t in enumerate(rows):
+                V = int(out["visible"][r])
+                nb = (V + 7) // 8
+                ids = np.unique(case.cand_in[t, 0])
+                ids = ids[(ids >= 0) & (ids < nb)]
+                sub += int(np.minimum(8, V - 8 * ids).sum())
+            done_pairs += sub
+        else:
+            done_pairs += int(out["visible"].sum())
+    return done_pairs / spent, done_rows, cores, spent
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on the host cores."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case = synth.config(args.config)
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    prep = oracle.prepare(case)
+    per_step = max(1, min(case.T, args.ref_rows))
+    order = np.random.default_rng(777).permutation(case.T)
+
+    def step(k):
+        lo = (k * per_step) % case.T
+        rows = np.take(order, np.arange(lo, lo + per_step), mode="wrap")
+        out = oracle.run(prep, rows=rows, nthreads=cores)
+        return int(out["visible"].sum()) if case.cand_mode != "consumer" else None
+
+    for k in range(args.warmup):
+        step(k)
+    pairs = 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        p = step(args.warmup + k)
+        pairs += p if p is not None else 0
+    dt = time.perf_counter() - t0
+    if case.cand_mode == "consumer":
+        pairs = int(round(pairs_of(case) * per_step / case.T)) * args.steps
+    value = pairs / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic",
+        "config": {"workload": synth.CONFIG_NAMES[args.config],
+                   "reference": "CPU oracle (plain C, OpenMP over positions), no GPU"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d query rows per step of the workload, cycled" % per_step},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_ours(args):
+    import torch
+
+    from sparse_attention_indexer_qli_gb300 import qli
+
+    world, rank, local = dist_setup()
+    qli.lib()
+    idx = args.config
+    nsets = args.sets or ROTATE_SETS[idx]
+    base_seed = idx - 1
+    sets = []
+    for s in range(nsets):
+        case = synth.config(idx, seed=base_seed + 1000 * s + 100 * rank)
+        kw = synth.upload(case, "cuda")
+        call = qli.Call(**kw)
+        sets.append((case, call, pairs_of(case)))
+    ws_bytes = max(c.workspace_bytes() for _, c, _ in sets)
+    workspace = torch.empty(max(256, ws_bytes), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches_per_step = sets[0][1].launches(0)
+
+    def step(k, ev=None):
+        case, call, _ = sets[k % nsets]
+        if ev is None:
+            call.run(workspace, stream)
+            return
+        ev[0].record(stream)
+        call.run_stage(qli.STAGE_PLAN, workspace, stream)
+        ev[1].record(stream)
+        call.run_stage(qli.STAGE_SCORE, workspace, stream)
+        ev[2].record(stream)
+        call.run_stage(qli.STAGE_SELECT, workspace, stream)
+
+    for k in range(args.warmup):
+        step(k)
+    # timed region: K steps, score-stage events recorded on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for k in range(args.steps):
+            step(args.warmup + k, evs[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(stop)
+    ms_max = reduce_max(ms, world)
+    my_pairs = sum(sets[(args.warmup + k) % nsets][2] for k in range(args.steps))
+    all_pairs = reduce_sum(my_pairs, world)
+    value = all_pairs / (ms_max / 1e3)
+    score_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    score_ms_avg = sum(score_ms) / len(score_ms)
+    alg = sum(score_algorithmic_bytes(sets[(args.warmup + k) % nsets][0],
+                                      sets[(args.warmup + k) % nsets][2])
+              for k in range(args.steps)) / args.steps
+    peak, peak_kind = peaks()
+    achieved = alg / (score_ms_avg / 1e3) / 1e9
+    traffic = profiled_traffic()
+
+    # e2e: the public call from pinned host buffers, copies inside the timed region
+    e2e = run_e2e(args, sets, workspace, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, cores, spent = oracle_rate(sets[0][0], args.cpu_seconds, args.cpu_rows)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%d of %d query rows of the workload (%.1f s of oracle time)"
+                         % (rows, sets[0][0].T, spent)}
+    if rank != 0:
+        return
+    case0 = sets[0][0]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {
+            "workload": synth.CONFIG_NAMES[idx], "global_batch": case0.B * world,
+            "query_tokens": case0.T, "heads": case0.N, "ratio": case0.ratio,
+            "topk": case0.topk, "cand_mode": case0.cand_mode,
+            "pairs_per_step": my_pairs / args.steps,
+            "l2": "inputs rotate over %d independent sets, %.0f MB of index K each (L2 129 MB)"
+                  % (nsets, 128 * sets[0][2] / 1e6),
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "score_tile_kernel", "peak_source": peak_kind,
+                     "kernel_ms": score_ms_avg, "algorithmic_bytes": alg},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
+def run_e2e(args, sets, workspace, stream, world):
+    import torch
+
+    from sparse_attention_indexer_qli_gb300 import qli
+    nsets = len(sets)
+    host, dev, calls = [], [], []
+    for case, call, _ in sets:
+        names = ["q", "cu_seqlens_q", "k_lens", "residual", "block_table", "head_weights",
+                 "q_scale", "cand_in"]
+        kw = {}
+        h = {}
+        for n, t in zip(names, call.keep[:3] + call.keep[3:4] + call.keep[5:9]):
+            if t is None:
+                kw[n] = None
+                continue
+            h[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+            kw[n] = torch.empty_like(t)
+        host.append(h)
+        dev.append(kw)
+        c = qli.Call(kw["q"], kw["cu_seqlens_q"], kw["k_lens"], kw["residual"], call.keep[4],
+                     kw["block_table"], kw["head_weights"], kw["q_scale"], ratio=case.ratio,
+                     rows_per_page=case.rows_per_page, page_stride=case.page_stride,
+                     k_offset=case.k_offset, scale_offset=case.scale_offset, topk=case.topk,
+                     cand_mode=case.cand_mode, cand_blocks=case.cand_blocks,
+                     cand_in=kw["cand_in"])
+        calls.append(c)
+    out_h = [torch.empty(c.indices.shape, dtype=torch.int32, pin_memory=True) for c in calls]
+    cand_h = [None if c.cand is None else torch.empty(c.cand.shape, dtype=torch.int32,
+                                                      pin_memory=True) for c in calls]
+
+    def step(k):
+        i = k % nsets
+        for n, h in host[i].items():
+            dev[i][n].copy_(h, non_blocking=True)
+        calls[i].run(workspace, stream)
+        out_h[i].copy_(calls[i].indices, non_blocking=True)
+        if cand_h[i] is not None:
+            cand_h[i].copy_(calls[i].cand, non_blocking=True)
+
+    for k in range(args.warmup):
+        step(k)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + k)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(t0.elapsed_time(t1), world)
+    pairs = reduce_sum(sum(sets[(args.warmup + k) % nsets][2] for k in range(args.steps)), world)
+    h2d = sum(step_bytes_in(sets[(args.warmup + k) % nsets][0]) for k in range(args.steps))
+    d2h = sum(out_h[(args.warmup + k) % nsets].numel() * 4 +
+              (0 if cand_h[(args.warmup + k) % nsets] is None
+               else cand_h[(args.warmup + k) % nsets].numel() * 4) for k in range(args.steps))
+    return {"value": pairs / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d // args.steps, "d2h_bytes_per_step": d2h // args.steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = default)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-rows", type=int, default=4)
+    ap.add_argument("--ref-rows", type=int, default=4, help="oracle rows per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * qli.h — C ABI of the GB300 quantized lightning indexer (QLI).
+ *
+ * The indexer scores every causally visible compressed position of a paged
+ * INT8 index-K cache against per-head INT8 queries and returns, per query
+ * token, the chronologically ordered position TopK and, in source mode, the
+ * 8-position candidate block IDs. It is the operator the vllm-ascend
+ * developer guide "DeepSeek V4.1 QLI V2 与候选集成" documents:
+ *   section "数据流" (data flow)      — inputs, page geometry, metadata,
+ *                                        the three candidate modes, outputs;
+ *   section "当前 A3 契约" (contract)  — dtypes, ranges and the numeric golden;
+ *   section "构建与回归覆盖"           — candidate size T * N_k * blocks.
+ *
+ * Conventions
+ *  - Every pointer inside qli_args is a DEVICE pointer (memory of the current
+ *    CUDA device, sm_103a) unless stated otherwise. The library never
+ *    allocates, frees or synchronises on the run path; the caller owns every
+ *    buffer, including the workspace, and keeps it alive until the work
+ *    queued on `stream` has finished.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Validation runs on the host before anything is queued; a non-OK status
+ *    means nothing was launched. Values that live on the device (lengths,
+ *    block-table entries) are checked by the first kernel: out-of-range values
+ *    are clamped so that no access leaves its buffer, and a bit is set in the
+ *    workspace's error word (qli_read_device_error).
+ *  - No state is kept between calls. Candidates produced by a source call
+ *    reach a later consumer call only through the caller's buffer.
+ *  - Every FP16 value is IEEE binary16 passed as its 16-bit pattern.
+ */
+#ifndef QLI_H
+#define QLI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QLI_ABI_VERSION 1
+
+typedef enum qli_status {
+    QLI_OK = 0,
+    QLI_ERR_INVALID_ARG = 1,          /* NULL pointer, bad size or extent */
+    QLI_ERR_UNSUPPORTED = 2,          /* layout, dtype, quant/mask mode, N, D, ratio,
+                                         block size or page geometry outside the contract */
+    QLI_ERR_CONSUMER_WITHOUT_SOURCE = 3, /* consumer mode with no candidate input */
+    QLI_ERR_RESIDUAL_WITH_RATIO1 = 4, /* a residual tensor was given with ratio 1 */
+    QLI_ERR_WORKSPACE_TOO_SMALL = 5,
+    QLI_ERR_ALIGNMENT = 6,            /* pointer, stride or offset not 16-byte aligned */
+    QLI_ERR_CUDA = 7,                 /* a CUDA runtime call failed */
+    QLI_ERR_DEVICE = 8                /* current device is not an sm_103 GPU */
+} qli_status;
+
+/* Candidate modes. The guide numbers them 1/2/3 ("候选模式 1/2/3") without
+ * naming them in the surviving text; this library reads 1 = none (position
+ * TopK only), 2 = source (also emits candidate blocks), 3 = consumer (TopK
+ * restricted to given candidate blocks). */
+enum { QLI_CAND_NONE = 1, QLI_CAND_SOURCE = 2, QLI_CAND_CONSUMER = 3 };
+/* Layouts, quantisation and mask modes the contract compiles. */
+enum { QLI_LAYOUT_TND = 1, QLI_LAYOUT_PA_BBND = 2 };
+enum { QLI_QUANT_INT8 = 2 };          /* quant mode 2: INT8 Q/K, FP16 weights/scales */
+enum { QLI_MASK_CAUSAL = 3 };         /* causal mask mode 3 */
+/* Stages of one call, for timing them separately (qli_run_stage). */
+enum { QLI_STAGE_PLAN = 1, QLI_STAGE_SCORE = 2, QLI_STAGE_SELECT = 3 };
+/* Bits of the device error word. */
+enum {
+    QLI_DEVERR_SEQLENS = 1u << 0,     /* cu_seqlens_q not 0..T non-decreasing */
+    QLI_DEVERR_KLEN = 1u << 1,        /* k_lens outside [0, bt_stride*rows_per_page] */
+    QLI_DEVERR_RESIDUAL = 1u << 2,    /* residual outside [0, ratio) */
+    QLI_DEVERR_PAGE = 1u << 3,        /* block-table entry outside [0, num_pages) */
+    QLI_DEVERR_TIMEOUT = 1u << 4      /* an on-chip wait gave up (never expected) */
+};
+
+typedef struct qli_args {
+    /* Queries, TND: element (t, h, d) at q[t*q_stride_t + h*q_stride_h + d],
+     * INT8, strides in bytes, each a multiple of 16 with q_stride_h >= D. */
+    const int8_t *q;
+    int64_t q_stride_t, q_stride_h;
+    int32_t T;                        /* query tokens (all requests)            */
+    int32_t N;                        /* index heads: 32 or 64                  */
+    int32_t D;                        /* head dim: 128                          */
+    /* Metadata ("数据流"): raw query boundaries, compressed K lengths, raw
+     * length mod ratio. Device int32 arrays. */
+    const int32_t *cu_seqlens_q;      /* [B+1], 0 = cu[0] <= ... <= cu[B] = T   */
+    int32_t B;                        /* requests                               */
+    const int32_t *k_lens;            /* [B] compressed positions per request   */
+    const int32_t *residual;          /* [B] raw length mod ratio; must be NULL
+                                         when ratio == 1, NULL means 0 otherwise */
+    /* PA_BBND paged index K: page p starts at cache + p*page_stride; row r of
+     * the page holds position (slot*rows_per_page + r) of the request whose
+     * block table lists p at `slot`; its 128 INT8 values sit at
+     * k_offset + r*128 and its FP16 scale at scale_offset + r*2 inside the page. */
+    const uint8_t *cache;
+    int64_t page_stride;              /* bytes; 131072 (ratio 2) / 147712 (ratio 1) */
+    int32_t rows_per_page;            /* 64 or 128                              */
+    int64_t k_offset, scale_offset;   /* bytes inside a page                    */
+    int64_t num_pages;                /* pages in the pool (bounds checks)       */
+    const int32_t *block_table;       /* [B, bt_stride] page IDs                 */
+    int32_t bt_stride;                /* >= pages of the longest request        */
+    /* FP16 head weights and per-head Q scales, [T, N] contiguous. */
+    const uint16_t *head_weights;
+    const uint16_t *q_scale;
+    int32_t ratio;                    /* compression ratio: 1 or 2              */
+    int32_t mask_mode;                /* QLI_MASK_CAUSAL                        */
+    int32_t quant_mode;               /* QLI_QUANT_INT8                         */
+    int32_t layout_q;                 /* QLI_LAYOUT_TND                         */
+    int32_t layout_k;                 /* QLI_LAYOUT_PA_BBND                     */
+    int32_t topk;                     /* K in [1, 2048]                         */
+    int32_t cand_mode;                /* QLI_CAND_*                             */
+    int32_t cand_blocks;              /* C in [64, 2048], multiple of 64 (source/consumer) */
+    int32_t block_size;               /* positions per candidate block: 8      */
+    const int32_t *cand_in;           /* consumer: [T, 1, C] block IDs, -1 pads  */
+    int64_t cand_in_numel;            /* must equal T * 1 * C in consumer mode  */
+    int32_t *cand_out;                /* source: [T, 1, C] block IDs, -1 padded  */
+    int64_t cand_out_numel;           /* must equal T * 1 * C in source mode    */
+    int32_t *indices_out;             /* [T, 1, K] positions, ascending, -1 at the end */
+    int64_t indices_numel;            /* must equal T * K                       */
+} qli_args;
+
+/* Checks `a` against the contract ("当前 A3 契约", "数据流", "构建与回归覆盖")
+ * on the host. Touches no device memory. */
+qli_status qli_validate(const qli_args *a);
+
+/* Bytes of device workspace qli_run needs for these arguments (an upper bound
+ * derived from T, B, N, bt_stride*rows_per_page and C; no device reads). */
+qli_status qli_workspace_size(const qli_args *a, size_t *bytes);
+
+/* Queues the whole indexer on `stream`: planning, scoring, selection. Writes
+ * indices_out and, in source mode, cand_out. `workspace` must be 256-byte
+ * aligned device memory of at least qli_workspace_size bytes; its contents on
+ * entry do not matter. Asynchronous: returns once the kernels are queued. */
+qli_status qli_run(const qli_args *a, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Queues one stage (QLI_STAGE_*) of qli_run, for timing. Running PLAN, SCORE
+ * and SELECT in that order on one stream equals qli_run. */
+qli_status qli_run_stage(const qli_args *a, void *workspace, size_t workspace_bytes,
+                         int32_t stage, void *stream);
+
+/* Kernel launches one call of the given stage queues (0 = all stages). */
+qli_status qli_launch_count(const qli_args *a, int32_t stage, int32_t *launches);
+
+/* Where the FP32 scores sit in the workspace after the SCORE stage: row t
+ * starts at byte `offset` + t*row_stride*4. In none/source mode entry j of
+ * row t is the score of position j (valid for j < V(t)); in consumer mode
+ * entry s is the score of the s-th position of the token's sorted candidate
+ * blocks. For tests; the values are not part of the operator's outputs. */
+qli_status qli_scores_layout(const qli_args *a, size_t *offset, int64_t *row_stride);
+
+/* Copies the device error word (QLI_DEVERR_* bits of the last call that used
+ * this workspace) to *host_word and waits for `stream`. Synchronous. */
+qli_status qli_read_device_error(const void *workspace, uint32_t *host_word, void *stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char *qli_status_string(qli_status s);
+
+/* QLI_ABI_VERSION of the loaded library, and sizeof(qli_args) it was built with. */
+int32_t qli_abi_version(void);
+int64_t qli_args_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLI_H */

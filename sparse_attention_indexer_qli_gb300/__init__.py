@@ -6,13 +6,6 @@ sm_103a CUDA kernels); :mod:`.qli` is its thin Python binding and
 native; the first call into :mod:`.qli` does, and fails loudly when the
 library or a CUDA device is missing.
 """
-from . import synth  # noqa: F401
+from . import qli, synth  # noqa: F401
 
-__all__ = ["synth", "qli"]
-
-
-def __getattr__(name):
-    if name == "qli":
-        from . import qli
-        return qli
-    raise AttributeError(name)
+__all__ = ["qli", "synth"]

@@ -1,0 +1,90 @@
+// Internal declarations shared by the library's translation units: the
+// by-value argument block every kernel receives, the workspace layout and the
+// stage launchers. Not part of the public ABI (include/qli.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "qli.h"
+
+namespace qli {
+
+constexpr int kHeadDim = 128;      // D
+constexpr int kTile = 128;         // positions per score tile (MMA M)
+constexpr int kBlock = 8;          // positions per candidate block
+constexpr int kMaxMmaN = 256;      // token-heads per tile (MMA N)
+constexpr int kMaxTopK = 2048;
+constexpr int kMaxCand = 2048;
+
+// Everything a kernel needs, passed by value (a few hundred bytes).
+struct DevArgs {
+  // inputs
+  const int8_t* q;
+  int64_t q_st, q_sh;
+  int32_t T, N, B;
+  const int32_t* cu;
+  const int32_t* k_lens;
+  const int32_t* residual;
+  const uint8_t* cache;
+  int64_t page_stride;
+  int32_t R;
+  int64_t k_off, s_off, num_pages;
+  const int32_t* bt;
+  int32_t bt_stride;
+  const uint16_t* w;
+  const uint16_t* qs;
+  int32_t ratio, topk, mode, C;
+  const int32_t* cand_in;
+  int32_t* cand_out;
+  int32_t* idx_out;
+  // workspace views
+  uint32_t* err;       // device error word (QLI_DEVERR_*)
+  int32_t* tok_V;      // [T] visible compressed positions V(t)
+  int32_t* tok_b;      // [T] request of token t, -1 if none
+  int32_t* req_lk;     // [B] sanitised compressed length
+  int32_t* req_res;    // [B] sanitised residual
+  int32_t* req_q0;     // [B] sanitised first token
+  int32_t* req_q1;     // [B] sanitised end token
+  int32_t* req_g0;     // [B] first token group of the request
+  int32_t* grp_t0;     // [Gmax] first token of a group
+  int32_t* grp_cnt;    // [Gmax] tokens in the group (0 = unused)
+  int32_t* cand_list;  // [T, C] consumer: sorted distinct usable block IDs
+  int32_t* cand_cnt;   // [T] consumer: how many
+  int32_t* unit_start; // [T+1] stream path: first score tile of token t
+  uint32_t* counter;   // stream path: CTAs done in cand_prep (reset by plan)
+  float* scores;       // [T, Lrow]
+  float* bscores;      // [T, Brow] source: block maxima
+  int64_t Lrow, Brow;
+  int32_t Gmax, G;     // token groups (upper bound), tokens per group
+  int64_t cap;         // bt_stride * R: most positions a request can hold
+  int32_t stream_path; // 1: one token per tile, persistent streaming kernel
+  int32_t num_sms;     // SMs of the device (stream path grid)
+};
+
+struct WsLayout {
+  size_t err, counter, tok_V, tok_b, req_lk, req_res, req_q0, req_q1, req_g0;
+  size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, scores, bscores, total;
+  int64_t Lrow, Brow;
+  int32_t Gmax, G;
+  int32_t stream_path;
+};
+
+// The streaming (decode) kernel takes one token per tile; the group kernel
+// shares a tile between up to 256/N tokens of one request (prefill).
+bool use_stream_path(const qli_args& a);
+
+WsLayout workspace_layout(const qli_args& a);
+DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L);
+
+// Stage launchers (one .cu file each). Return the first CUDA error.
+cudaError_t launch_plan(const DevArgs& d, cudaStream_t s);
+cudaError_t launch_score(const DevArgs& d, cudaStream_t s);
+cudaError_t launch_select(const DevArgs& d, cudaStream_t s);
+int plan_launches(const DevArgs& d);
+int score_launches(const DevArgs& d);
+int select_launches(const DevArgs& d);
+
+}  // namespace qli

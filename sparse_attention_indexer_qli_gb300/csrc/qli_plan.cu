@@ -1,0 +1,232 @@
+// Planning stage: turns the device-side metadata into per-token and
+// per-group work descriptions, and (consumer mode) the sorted set of usable
+// candidate blocks per token.
+//
+// The metadata follows the guide "DeepSeek V4.1 QLI V2 与候选集成", section
+// 数据流: raw query boundaries (cu_seqlens_q), compressed K lengths and the raw
+// length mod ratio (absent for ratio 1). Causal mask mode 3 is read as: the
+// queries of a request are the last q_len of its S = k_len*ratio + residual
+// raw tokens, and compressed position j (raw span [j*r, j*r + r - 1]) is
+// visible to the query at raw position pos once pos >= j*r + r - 1, i.e.
+// V = floor((pos + 1) / r) positions.
+#include <climits>
+
+#include "qli_internal.h"
+#include "qli_ptx.cuh"
+
+namespace qli {
+namespace {
+
+__device__ __forceinline__ int32_t visible_count(int32_t lk, int32_t res, int32_t ratio,
+                                                 int32_t q_len, int32_t i) {
+  const int64_t S = static_cast<int64_t>(lk) * ratio + res;
+  const int64_t seen = S - q_len + i + 1;   // raw tokens at or before the query
+  if (seen <= 0) return 0;
+  const int64_t v = seen / ratio;
+  return static_cast<int32_t>(v < lk ? v : lk);
+}
+
+// Exclusive prefix sum of f(0..n-1) into out[0..n], by one CTA of NT threads.
+template <int NT, class F>
+__device__ void cta_scan_store(int32_t n, F f, int32_t* out) {
+  __shared__ int32_t warp_tot[NT / 32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int32_t base = 0; base < n; base += NT) {
+    const int32_t i = base + tid;
+    const int32_t v = i < n ? f(i) : 0;
+    int32_t incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t x = lane < NT / 32 ? warp_tot[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane < NT / 32) warp_tot[lane] = x;
+    }
+    __syncthreads();
+    const int32_t excl = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+    if (i < n) out[i] = excl;
+    __syncthreads();
+    if (tid == NT - 1) carry = excl + v;
+    __syncthreads();
+  }
+  if (tid == 0) out[n] = carry;
+}
+
+// One CTA. Sanitises the metadata (clamping it so no later kernel can leave
+// its buffers, and flagging what was clamped), then writes V(t), the request
+// of every token and the token groups that share one score tile.
+__global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
+  const int tid = threadIdx.x;
+  for (int t = tid; t < a.T; t += blockDim.x) {
+    a.tok_V[t] = 0;
+    a.tok_b[t] = -1;
+  }
+  for (int g = tid; g < a.Gmax; g += blockDim.x) a.grp_cnt[g] = 0;
+  __syncthreads();
+
+  if (tid == 0) {
+    uint32_t e = 0;
+    int32_t prev = 0, groups = 0;
+    if (a.B > 0 && a.cu[0] != 0) e |= QLI_DEVERR_SEQLENS;
+    for (int b = 0; b < a.B; ++b) {
+      const int32_t c0 = a.cu[b], c1 = a.cu[b + 1];
+      const int32_t q0 = min(max(c0, prev), a.T);
+      const int32_t q1 = min(max(c1, q0), a.T);
+      if (c0 != q0 || c1 != q1) e |= QLI_DEVERR_SEQLENS;
+      prev = q1;
+      int32_t lk = a.k_lens[b];
+      if (lk < 0 || lk > a.cap) {
+        e |= QLI_DEVERR_KLEN;
+        lk = lk < 0 ? 0 : static_cast<int32_t>(a.cap);
+      }
+      int32_t res = a.residual ? a.residual[b] : 0;
+      if (res < 0 || res >= a.ratio) {
+        e |= QLI_DEVERR_RESIDUAL;
+        res = 0;
+      }
+      a.req_q0[b] = q0;
+      a.req_q1[b] = q1;
+      a.req_lk[b] = lk;
+      a.req_res[b] = res;
+      a.req_g0[b] = groups;
+      groups += (q1 - q0 + a.G - 1) / a.G;
+    }
+    if (prev != a.T) e |= QLI_DEVERR_SEQLENS;
+    *a.err = e;   // first writer of this call: resets the word
+    *a.counter = 0u;
+  }
+  __syncthreads();
+
+  // one warp per request, lanes over its tokens and groups
+  const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  for (int b = warp; b < a.B; b += nwarps) {
+    const int32_t q0 = a.req_q0[b], q1 = a.req_q1[b], lk = a.req_lk[b], res = a.req_res[b];
+    const int32_t qlen = q1 - q0;
+    for (int i = lane; i < qlen; i += 32) {
+      a.tok_V[q0 + i] = visible_count(lk, res, a.ratio, qlen, i);
+      a.tok_b[q0 + i] = b;
+    }
+    const int32_t ng = (qlen + a.G - 1) / a.G;
+    for (int gi = lane; gi < ng; gi += 32) {
+      const int32_t g = a.req_g0[b] + gi;
+      if (g < a.Gmax) {
+        a.grp_t0[g] = q0 + gi * a.G;
+        a.grp_cnt[g] = min(a.G, qlen - gi * a.G);
+      }
+    }
+  }
+  // stream path, dense modes: token t owns ceil(V(t)/128) score tiles
+  if (a.stream_path && a.mode != QLI_CAND_CONSUMER) {
+    __syncthreads();
+    cta_scan_store<1024>(a.T, [&](int32_t t) { return (a.tok_V[t] + kTile - 1) / kTile; },
+                         a.unit_start);
+  }
+}
+
+// Consumer mode, one CTA per token: keep the candidate IDs that name a block
+// with at least one visible position (0 <= id < ceil(V/8)), sort them
+// ascending and drop duplicates. The guide gives candidates as a padded list
+// of block IDs; they are used as a set.
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads) cand_prep_kernel(DevArgs a, int32_t pow2) {
+  __shared__ int32_t keys[kMaxCand];
+  __shared__ int32_t warp_sum[kPrepThreads / 32];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int32_t V = a.tok_V[t];
+  const int32_t nb = (V + kBlock - 1) / kBlock;
+  const int32_t* row = a.cand_in + static_cast<int64_t>(t) * a.C;
+  for (int k = tid; k < pow2; k += kPrepThreads) {
+    int32_t v = k < a.C ? row[k] : INT_MAX;
+    if (v < 0 || v >= nb) v = INT_MAX;
+    keys[k] = v;
+  }
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int size = 2; size <= pow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int k = tid; k < pow2; k += kPrepThreads) {
+        const int partner = k ^ stride;
+        if (partner > k) {
+          const bool up = (k & size) == 0;
+          const int32_t x = keys[k], y = keys[partner];
+          if ((x > y) == up) {
+            keys[k] = y;
+            keys[partner] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // keep first occurrences of real IDs; each thread owns a contiguous run
+  const int per = pow2 / kPrepThreads > 0 ? pow2 / kPrepThreads : 1;
+  const int lo = tid * per;
+  int cnt = 0;
+  for (int k = lo; k < lo + per && k < pow2; ++k)
+    cnt += (keys[k] != INT_MAX && (k == 0 || keys[k] != keys[k - 1])) ? 1 : 0;
+  // block exclusive scan of cnt
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < kPrepThreads / 32; ++w) {
+    if (w < warp) base += warp_sum[w];
+    total += warp_sum[w];
+  }
+  int pos = base + incl - cnt;
+  int32_t* out = a.cand_list + static_cast<int64_t>(t) * a.C;
+  for (int k = lo; k < lo + per && k < pow2; ++k)
+    if (keys[k] != INT_MAX && (k == 0 || keys[k] != keys[k - 1])) out[pos++] = keys[k];
+  if (tid == 0) a.cand_cnt[t] = total;
+
+  // the last CTA to finish turns the counts into the stream path's tile
+  // prefix: token t owns ceil(count/16) tiles of 128 candidate positions
+  __shared__ bool s_last;
+  __threadfence();
+  if (tid == 0) s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (s_last && a.stream_path) {
+    __threadfence();
+    cta_scan_store<kPrepThreads>(
+        a.T, [&](int32_t i) { return (__ldcg(&a.cand_cnt[i]) + kTile / kBlock - 1) / (kTile / kBlock); },
+        a.unit_start);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const DevArgs& d, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (d.mode == QLI_CAND_CONSUMER && d.T > 0) {
+    int32_t pow2 = 1;
+    while (pow2 < d.C) pow2 <<= 1;
+    if (pow2 < kPrepThreads) pow2 = kPrepThreads;
+    cand_prep_kernel<<<d.T, kPrepThreads, 0, s>>>(d, pow2);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+int plan_launches(const DevArgs& d) {
+  return 1 + ((d.mode == QLI_CAND_CONSUMER && d.T > 0) ? 1 : 0);
+}
+
+}  // namespace qli

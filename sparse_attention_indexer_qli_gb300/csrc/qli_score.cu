@@ -1,0 +1,612 @@
+// Scoring stage: paged index-K gather, the Q.K contraction on the tcgen05
+// tensor cores, and the fused golden epilogue.
+//
+// Numeric golden (guide "DeepSeek V4.1 QLI V2 与候选集成", section 当前 A3 契约):
+// INT32 QK / 1024 -> FP16, FP16 ReLU, times FP16(weight * q_scale), FP32
+// reduction over the heads, then times the per-token K scale.
+//
+// sm_103a has no INT8 tensor-core MMA (tcgen05 kind::i8 is not available on
+// this target), so the INT8 operands are widened to FP16 and contracted with
+// kind::f16 into FP32. This is exact: every INT8 value is an FP16 integer,
+// every product is an integer below 2^15, and every partial sum of the 128
+// terms is an integer of magnitude <= 128*128*128 = 2^21 < 2^24. The queries
+// are pre-multiplied by 2^-10 (exact in FP16 for |q| <= 128), so the FP32
+// accumulator holds exactly s/1024, the value the golden rounds to FP16.
+//
+// Orientation: A (M = 128) = the K rows of a tile of 128 positions, B (N) =
+// the queries' heads (up to 256/N tokens of one request share a tile), so
+// TMEM lane i holds every head's dot for position i and the epilogue thread
+// of lane i sums its heads sequentially in FP32 — the order the golden's
+// reduction is read with.
+//
+// Page addressing (section 数据流, PA_BBND): position j of a request lives in
+// page block_table[b][j / R], row j % R; its 128 INT8 values at
+// k_offset + row*128 and its FP16 scale at scale_offset + row*2 in that page.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "qli_internal.h"
+#include "qli_ptx.cuh"
+
+namespace qli {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kSmemA = kTile * kHeadDim * 2;        // 32 KB
+constexpr int kSmemB = kMaxMmaN * kHeadDim * 2;     // 64 KB
+constexpr int kSmemWq = kMaxMmaN * 2;
+constexpr int kSmemBytes = 1024 + kSmemA + kSmemB + kSmemWq + 64;
+
+// Byte offset of 16-byte chunk c (8 FP16 values, c in 0..15) of row n in a
+// K-major tile with the 128-byte swizzle: two 64-element K halves of
+// rows*128 bytes each; rows grouped by 8 (1024 B); the chunk index XORed with
+// the row within its group.
+__device__ __forceinline__ uint32_t sw128_off(uint32_t rows, uint32_t n, uint32_t c) {
+  return (c >> 3) * (rows * 128u) + (n >> 3) * 1024u + (n & 7u) * 128u +
+         (((c & 7u) ^ (n & 7u)) << 4);
+}
+
+// 8 INT8 values -> 8 FP16 values (exact): (x + 128) placed in the mantissa
+// of 1024.0h gives 1024 + x + 128, then 1152 is subtracted.
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 v) {
+  const uint32_t u0 = v.x ^ 0x80808080u, u1 = v.y ^ 0x80808080u;
+  uint32_t h[4];
+  h[0] = __byte_perm(u0, 0x64646464u, 0x5140);
+  h[1] = __byte_perm(u0, 0x64646464u, 0x7362);
+  h[2] = __byte_perm(u1, 0x64646464u, 0x5140);
+  h[3] = __byte_perm(u1, 0x64646464u, 0x7362);
+  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
+  uint4 r;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __half2 x = __hsub2(*reinterpret_cast<__half2*>(&h[k]), bias);
+    o[k] = *reinterpret_cast<uint32_t*>(&x);
+  }
+  return r;
+}
+
+// Same, times 2^-10 (exact: |x| <= 128).
+__device__ __forceinline__ uint4 i8x8_to_f16x8_div1024(uint2 v) {
+  uint4 r = i8x8_to_f16x8(v);
+  const __half2 s = __floats2half2_rn(1.0f / 1024.0f, 1.0f / 1024.0f);
+  uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __half2 x = __hmul2(*reinterpret_cast<__half2*>(&o[k]), s);
+    o[k] = *reinterpret_cast<uint32_t*>(&x);
+  }
+  return r;
+}
+
+// One CTA scores one tile of 128 positions against one token group.
+//   grid.x = tile, grid.y = token group (none/source) or token (consumer).
+__global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kSmemA;
+  __half* s_wq = reinterpret_cast<__half*>(sB + kSmemB);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kSmemB + kSmemWq);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tile = blockIdx.x, g = blockIdx.y;
+  const bool consumer = a.mode == QLI_CAND_CONSUMER;
+
+  int32_t t0, cnt, ncand = 0, vmax;
+  if (consumer) {
+    t0 = g;
+    cnt = 1;
+    ncand = a.cand_cnt[t0];
+    vmax = a.tok_V[t0];
+    if (tile * (kTile / kBlock) >= ncand) return;
+  } else {
+    cnt = a.grp_cnt[g];
+    if (cnt == 0) return;
+    t0 = a.grp_t0[g];
+    vmax = a.tok_V[t0 + cnt - 1];   // V grows with the token index
+    if (tile * kTile >= vmax) return;
+  }
+  const int32_t b = a.tok_b[t0];
+  if (b < 0) return;
+  const int n_mma = cnt * a.N;
+
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+
+  // B operand: the group's query heads, times 2^-10, and wq = fp16(w * qs)
+  for (int idx = tid; idx < n_mma * 16; idx += kThreads) {
+    const int n = idx >> 4, c = idx & 15;
+    const int gi = n / a.N, h = n % a.N;
+    const int8_t* src = a.q + static_cast<int64_t>(t0 + gi) * a.q_st +
+                        static_cast<int64_t>(h) * a.q_sh + c * 8;
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    *reinterpret_cast<uint4*>(sB + sw128_off(n_mma, n, c)) = i8x8_to_f16x8_div1024(v);
+  }
+  for (int n = tid; n < n_mma; n += kThreads) {
+    const int gi = n / a.N, h = n % a.N;
+    const int64_t o = static_cast<int64_t>(t0 + gi) * a.N + h;
+    s_wq[n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
+  }
+
+  // A operand: row `tid` of the tile is one position
+  const int i = tid;
+  int32_t pos, slot = 0;
+  bool row_ok;
+  if (consumer) {
+    slot = tile * kTile + i;
+    row_ok = slot < ncand * kBlock;
+    const int32_t blk = row_ok ? a.cand_list[static_cast<int64_t>(t0) * a.C + slot / kBlock] : 0;
+    pos = blk * kBlock + (slot & (kBlock - 1));
+    row_ok = row_ok && pos < vmax;
+  } else {
+    pos = tile * kTile + i;
+    row_ok = pos < vmax;
+  }
+  uint4 kv[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) kv[c] = make_uint4(0, 0, 0, 0);
+  __half ks = __ushort_as_half(0);
+  if (row_ok) {
+    const int32_t page = a.bt[static_cast<int64_t>(b) * a.bt_stride + pos / a.R];
+    if (page < 0 || page >= a.num_pages) {
+      atomicOr(a.err, QLI_DEVERR_PAGE);
+      row_ok = false;
+    } else {
+      const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
+      const int r = pos % a.R;
+      const uint4* kr = reinterpret_cast<const uint4*>(pg + a.k_off + r * kHeadDim);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) kv[c] = __ldg(kr + c);
+      ks = __ushort_as_half(*reinterpret_cast<const uint16_t*>(pg + a.s_off + r * 2));
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    *reinterpret_cast<uint4*>(sA + sw128_off(kTile, i, 2 * c)) =
+        i8x8_to_f16x8(make_uint2(kv[c].x, kv[c].y));
+    *reinterpret_cast<uint4*>(sA + sw128_off(kTile, i, 2 * c + 1)) =
+        i8x8_to_f16x8(make_uint2(kv[c].z, kv[c].w));
+  }
+
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (tid == 0) {
+    const uint32_t idesc = idesc_f16_m128(static_cast<uint32_t>(n_mma));
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+#pragma unroll
+    for (int s = 0; s < kHeadDim / 16; ++s) {
+      const uint32_t kb = s >> 2, koff = (s & 3) * 32;
+      mma_f16_ss(tmem, sdesc_k_sw128(a0 + kb * (kTile * 128) + koff),
+                 sdesc_k_sw128(b0 + kb * (n_mma * 128) + koff), idesc, s > 0 ? 1u : 0u);
+    }
+    mma_commit(bar);
+  }
+  __syncwarp();
+  const bool done = mbar_wait_bounded(bar, 0);
+  tc_fence_after();
+  if (!done) {
+    if (tid == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+  } else {
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int gi = 0; gi < cnt; ++gi) {
+      const int32_t t = t0 + gi;
+      const int32_t V = a.tok_V[t];
+      float acc = 0.0f;
+      for (int hc = 0; hc < a.N; hc += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(gi * a.N + hc), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc = head_term_acc(acc, __uint_as_float(r[k]), s_wq[gi * a.N + hc + k]);
+      }
+      const float score = __fmul_rn(acc, __half2float(ks));
+      const bool elig = row_ok && pos < V;
+      float* srow = a.scores + static_cast<int64_t>(t) * a.Lrow;
+      if (elig) srow[consumer ? slot : pos] = score;
+      if (a.mode == QLI_CAND_SOURCE) {
+        // max over the 8 positions of the block (8 consecutive lanes)
+        float m = elig ? score : -INFINITY;
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        if ((i & (kBlock - 1)) == 0 && pos < V)
+          a.bscores[static_cast<int64_t>(t) * a.Brow + pos / kBlock] = m;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Streaming kernel: one token per tile (decode batches and consumer mode).
+//
+// Persistent, one CTA per SM, each CTA owns a contiguous range of the
+// (token, tile) list, so the token's queries stay in shared memory across
+// its tiles. Warp roles:
+//   warp 0      producer: TMA bulk copies of the tile's INT8 K rows and FP16
+//               scales into a 4-stage shared-memory ring (whole pages for
+//               dense tiles; 1 KB + 16 B per 8-position block in consumer mode)
+//   warp 1      MMA: 8 x tcgen05.mma (A from TMEM, B = the token's queries
+//               from shared memory), committed to the stage's barrier
+//   warps 2-5   converters: row = position; INT8 -> FP16 in registers, stored
+//               to TMEM as the MMA's A operand; queries -> FP16 * 2^-10 in
+//               128-byte-swizzled shared memory when the token changes
+//   warps 6-9   epilogue: the golden chain per position, score store, block max
+// TMEM: 4 stages x (64 A columns + 64 accumulator columns).
+namespace stream {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per stage
+constexpr int kSBytes = kTile * 2;                   // 256 B of FP16 scales per stage
+constexpr int kBBytes = 64 * kHeadDim * 2;           // 16 KB: up to 64 heads, FP16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kStageCols = 128;                 // A: 64 columns, D: 64 columns
+
+struct Smem {
+  uint8_t k[kStages][kKBytes];                       // 1024-aligned (offset 0)
+  uint8_t b[kStages][kBBytes];                       // 1024-aligned
+  uint8_t sc[kStages][kSBytes];
+  __half wq[kStages][64];
+  float ks[kStages][kTile];
+  uint64_t full[kStages], empty[kStages], afull[kStages], dfull[kStages], tempty[kStages];
+  uint32_t tmem_base;
+};
+constexpr int kSmemBytes = static_cast<int>(sizeof(Smem)) + 1024;
+
+// Walks the CTA's units in order: (token, tile within the token).
+struct Cursor {
+  int32_t t, tile, end_t;
+  __device__ void init(const DevArgs& a, int32_t u) {
+    int32_t lo = 0, hi = a.T - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (a.unit_start[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    t = lo;
+    tile = u - a.unit_start[t];
+    end_t = a.unit_start[t + 1];
+  }
+  __device__ void next(const DevArgs& a, int32_t u_next) {
+    ++tile;
+    if (u_next >= end_t) {
+      do { ++t; } while (t + 1 <= a.T && a.unit_start[t + 1] <= u_next);
+      tile = 0;
+      end_t = (t < a.T) ? a.unit_start[t + 1] : u_next;
+    }
+  }
+};
+
+__device__ __forceinline__ void cvt_row16(const uint4 v, uint32_t* out8) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t u = w[k] ^ 0x80808080u;
+    uint32_t lo = __byte_perm(u, 0x64646464u, 0x5140);
+    uint32_t hi = __byte_perm(u, 0x64646464u, 0x7362);
+    __half2 x = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+    __half2 y = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+    out8[2 * k] = *reinterpret_cast<uint32_t*>(&x);
+    out8[2 * k + 1] = *reinterpret_cast<uint32_t*>(&y);
+  }
+}
+
+// tm_page: box of R rows x 128 B (a whole page's index K); tm_blk: box of
+// 8 rows x 128 B (one candidate block). Both use the 128-byte swizzle, so
+// row r's 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(
+    const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_blk,
+    DevArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t U = a.unit_start[a.T];
+  const int32_t u0 = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
+  const int32_t u1 = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
+  if (u0 >= u1) return;
+  const int32_t nk = u1 - u0;
+  const bool consumer = a.mode == QLI_CAND_CONSUMER;
+
+  if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
+  if (tid == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 4);
+      mbar_init(&S.afull[s], 4);
+      mbar_init(&S.dfull[s], 1);
+      mbar_init(&S.tempty[s], 4);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------- producer
+    Cursor c;
+    c.init(a, u0);
+    int issued = 0;
+    for (int k = 0; k < nk && ok; ++k) {
+      const int s = k % kStages;
+      const uint32_t ph = (k / kStages) & 1;
+      if (lane == 0) ok = mbar_wait_bounded(&S.empty[s], ph ^ 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int32_t t = c.t, b = a.tok_b[t];
+      const int64_t bt_row = static_cast<int64_t>(b) * a.bt_stride;
+      if (!consumer) {
+        const int32_t V = a.tok_V[t];
+        const int32_t j0 = c.tile * kTile;
+        const int npages = (a.R == kTile) ? 1 : ((j0 + a.R < V) ? 2 : 1);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&S.full[s], npages * (a.R * kHeadDim + a.R * 2));
+          for (int p = 0; p < npages; ++p) {
+            int32_t page = a.bt[bt_row + j0 / a.R + p];
+            if (page < 0 || page >= a.num_pages) {
+              atomicOr(a.err, QLI_DEVERR_PAGE);
+              page = 0;
+            }
+            const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
+            tma_load_3d(&S.k[s][p * a.R * kHeadDim], &tm_page, 0, 0, page, &S.full[s]);
+            bulk_g2s(&S.sc[s][p * a.R * 2], pg + a.s_off, a.R * 2, &S.full[s]);
+          }
+        }
+      } else {
+        const int32_t nc = a.cand_cnt[t];
+        const int32_t first = c.tile * (kTile / kBlock);
+        const int32_t nblk = min(kTile / kBlock, nc - first);
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[s], nblk * (kBlock * kHeadDim + kBlock * 2));
+        __syncwarp();
+        if (lane < nblk) {
+          const int32_t blk = a.cand_list[static_cast<int64_t>(t) * a.C + first + lane];
+          const int32_t pos0 = blk * kBlock;
+          int32_t page = a.bt[bt_row + pos0 / a.R];
+          if (page < 0 || page >= a.num_pages) {
+            atomicOr(a.err, QLI_DEVERR_PAGE);
+            page = 0;
+          }
+          const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
+          const int32_t row = pos0 % a.R;
+          tma_load_3d(&S.k[s][lane * kBlock * kHeadDim], &tm_blk, 0, row, page, &S.full[s]);
+          bulk_g2s(&S.sc[s][lane * kBlock * 2], pg + a.s_off + row * 2, kBlock * 2, &S.full[s]);
+        }
+      }
+      __syncwarp();
+      ++issued;
+      c.next(a, u0 + k + 1);
+    }
+    // never leave a copy in flight: wait for the last stages issued
+    if (lane == 0) {
+      for (int k = max(0, issued - kStages); k < issued; ++k)
+        (void)mbar_wait_bounded(&S.full[k % kStages], (k / kStages) & 1);
+    }
+    if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_m128(static_cast<uint32_t>(a.N));
+      int k = 0;
+      for (; k < nk; ++k) {
+        const int s = k % kStages;
+        const uint32_t ph = (k / kStages) & 1;
+        if (!mbar_wait_bounded(&S.afull[s], ph)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_col = tmem + s * kStageCols;
+        const uint32_t d_col = a_col + 64;
+        const uint32_t b0 = smem_u32(&S.b[s][0]);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint32_t kb = kk >> 2, koff = (kk & 3) * 32;
+          mma_f16_ts(d_col, a_col + kk * 8, sdesc_k_sw128(b0 + kb * (a.N * 128) + koff), idesc,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&S.dfull[s]);
+      }
+      if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) % kStages], ((k - 1) / kStages) & 1);
+      if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+    }
+  } else if (warp < 6) {
+    // ---------------- converters: row = TMEM lane
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int ctid = tid - 64;   // 0..127
+    int32_t btok[kStages];
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) btok[s] = -1;
+    Cursor c;
+    c.init(a, u0);
+    for (int k = 0; k < nk; ++k) {
+      const int s = k % kStages;
+      const uint32_t ph = (k / kStages) & 1;
+      bool w1 = mbar_wait_bounded(&S.full[s], ph);
+      bool w2 = w1 && mbar_wait_bounded(&S.tempty[s], ph ^ 1);
+      if (!(w1 && w2)) { ok = false; break; }
+      tc_fence_after();
+      const int32_t t = c.t;
+      if (btok[s] != t) {
+        // queries of token t: FP16 * 2^-10, K-major, 128-byte swizzle
+        for (int idx = ctid; idx < a.N * 16; idx += 128) {
+          const int n = idx >> 4, ch = idx & 15;
+          const int8_t* src = a.q + static_cast<int64_t>(t) * a.q_st +
+                              static_cast<int64_t>(n) * a.q_sh + ch * 8;
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          *reinterpret_cast<uint4*>(&S.b[s][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v);
+        }
+        for (int n = ctid; n < a.N; n += 128) {
+          const int64_t o = static_cast<int64_t>(t) * a.N + n;
+          S.wq[s][n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
+        }
+        btok[s] = t;
+      }
+      // this thread's K row, stored 128-byte swizzled by the TMA: logical
+      // chunk ch (K elements 16ch..16ch+15) sits at chunk ch ^ (row & 7); a
+      // quarter-warp (8 consecutive rows) reads 8 distinct bank groups
+      uint32_t regs[64];
+      const uint8_t* src = &S.k[s][row * kHeadDim];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
+        cvt_row16(v, &regs[8 * ch]);
+      }
+      S.ks[s][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[s][row * 2]));
+      tmem_st_32x32b_x64(tmem + lane_addr + s * kStageCols, regs);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.empty[s]);
+        mbar_arrive(&S.afull[s]);
+      }
+      c.next(a, u0 + k + 1);
+    }
+    if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+  } else {
+    // ---------------- epilogue: row = TMEM lane
+    const int row = 32 * (warp & 3) + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    Cursor c;
+    c.init(a, u0);
+    for (int k = 0; k < nk; ++k) {
+      const int s = k % kStages;
+      const uint32_t ph = (k / kStages) & 1;
+      bool w1 = mbar_wait_bounded(&S.afull[s], ph);
+      bool w2 = w1 && mbar_wait_bounded(&S.dfull[s], ph);
+      if (!(w1 && w2)) { ok = false; break; }
+      tc_fence_after();
+      const int32_t t = c.t;
+      const uint32_t d_col = tmem + lane_addr + s * kStageCols + 64;
+      float acc = 0.0f;
+      for (int hc = 0; hc < a.N; hc += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(d_col + hc, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk)
+          acc = head_term_acc(acc, __uint_as_float(r[kk]), S.wq[s][hc + kk]);
+      }
+      const float score = __fmul_rn(acc, S.ks[s][row]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tempty[s]);
+
+      const int32_t V = a.tok_V[t];
+      float* srow = a.scores + static_cast<int64_t>(t) * a.Lrow;
+      if (!consumer) {
+        const int32_t pos = c.tile * kTile + row;
+        const bool elig = pos < V;
+        if (elig) srow[pos] = score;
+        if (a.mode == QLI_CAND_SOURCE) {
+          float m = elig ? score : -INFINITY;
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          if ((row & (kBlock - 1)) == 0 && pos < V)
+            a.bscores[static_cast<int64_t>(t) * a.Brow + pos / kBlock] = m;
+        }
+      } else {
+        const int32_t slot = c.tile * kTile + row;
+        if (slot < a.cand_cnt[t] * kBlock) {
+          const int32_t pos =
+              a.cand_list[static_cast<int64_t>(t) * a.C + slot / kBlock] * kBlock + (row & 7);
+          if (pos < V) srow[slot] = score;
+        }
+      }
+      c.next(a, u0 + k + 1);
+    }
+    if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace stream
+
+// Tensor map over the index-K rows of the page pool: x = the 128 bytes of a
+// row, y = row within the page (R rows, 128 B apart), z = page (page_stride
+// apart); the box is 128 B x box_rows x 1 page, 128-byte swizzle.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool encode_k_map(const DevArgs& d, int box_rows, CUtensorMap* m) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(d.R),
+                              static_cast<cuuint64_t>(d.num_pages)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                 static_cast<cuuint64_t>(d.page_stride)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  void* base = const_cast<uint8_t*>(d.cache + d.k_off);
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
+  if (d.T == 0) return cudaSuccess;
+  if (d.stream_path) {
+    CUtensorMap tm_page, tm_blk;
+    if (!encode_k_map(d, d.R, &tm_page) || !encode_k_map(d, kBlock, &tm_blk))
+      return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(stream::stream_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         stream::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    stream::stream_kernel<<<d.num_sms, stream::kThreads, stream::kSmemBytes, s>>>(tm_page, tm_blk, d);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(score_tile_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid;
+  if (d.mode == QLI_CAND_CONSUMER) {
+    grid = dim3(static_cast<unsigned>(d.C * kBlock / kTile), static_cast<unsigned>(d.T));
+  } else {
+    grid = dim3(static_cast<unsigned>((d.cap + kTile - 1) / kTile), static_cast<unsigned>(d.Gmax));
+  }
+  score_tile_kernel<<<grid, kThreads, kSmemBytes, s>>>(d);
+  return cudaGetLastError();
+}
+
+int score_launches(const DevArgs& d) { return d.T > 0 ? 1 : 0; }
+
+}  // namespace qli

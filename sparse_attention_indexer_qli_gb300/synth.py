@@ -333,3 +333,28 @@ def workload_pairs_upper(case: Case) -> int:
     needs no knowledge of the causal rule (used only to size samples)."""
     q_lens = np.diff(case.cu_seqlens_q).astype(np.int64)
     return int((q_lens * case.k_lens.astype(np.int64)).sum())
+
+
+def upload(case: Case, device="cuda", filler: bool = True, cache=None) -> dict:
+    """Device tensors and call parameters for `case`, as keyword arguments of
+    the binding's `Call`. The paged cache is packed on the device unless
+    `cache` (an already packed device tensor) is given."""
+    import torch
+
+    def t(a, dtype=None):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            x = x.view(dtype)
+        return x.to(device)
+
+    return dict(
+        q=t(case.q), cu_seqlens_q=t(case.cu_seqlens_q), k_lens=t(case.k_lens),
+        residual=None if case.residual is None else t(case.residual),
+        cache=case.pack_pages_torch(device, filler) if cache is None else cache,
+        block_table=t(case.block_table),
+        head_weights=t(case.head_weights, torch.float16), q_scale=t(case.q_scale, torch.float16),
+        ratio=case.ratio, rows_per_page=case.rows_per_page, page_stride=case.page_stride,
+        k_offset=case.k_offset, scale_offset=case.scale_offset, topk=case.topk,
+        cand_mode=case.cand_mode, cand_blocks=case.cand_blocks,
+        cand_in=None if case.cand_in is None else t(case.cand_in),
+    )
