@@ -48,7 +48,9 @@ class OracleError(RuntimeError):
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # ORACLE_LIB points the wrapper at another build of qli_oracle.c (the
+        # mutation tests use it to check that the pins catch planted mistakes)
+        path = os.environ.get("ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         L.oracle_qli.restype = ctypes.c_int
         L.oracle_qli.argtypes = [ctypes.POINTER(_In), ctypes.c_void_p, ctypes.c_int32,
