@@ -24,7 +24,7 @@ NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I", INCLUDE, "-I", CSRC]
-UNITS = ["qli_api.cpp", "qli_plan.cu", "qli_score.cu", "qli_select.cu"]
+UNITS = ["qli_api.cpp", "qli_plan.cu", "qli_score.cu", "qli_prefill.cu", "qli_select.cu"]
 HEADERS = ["qli_internal.h", "qli_ptx.cuh"]
 
 
@@ -39,10 +39,10 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def _compile(unit: str, verbose: bool) -> str:
+def _compile(unit: str, verbose: bool, out_dir: str = OUT_DIR, defines=()) -> str:
     src = os.path.join(CSRC, unit)
-    obj = os.path.join(OUT_DIR, unit + ".o")
-    cmd = [NVCC] + ARCH + COMMON + ["-c", src, "-o", obj]
+    obj = os.path.join(out_dir, unit + ".o")
+    cmd = [NVCC] + ARCH + COMMON + ["-D" + d for d in defines] + ["-c", src, "-o", obj]
     if unit.endswith(".cu") and verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,25 +53,29 @@ def _compile(unit: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
-    stamp_path = os.path.join(OUT_DIR, "stamp")
-    stamp = _stamp()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_path):
+def build(force: bool = False, verbose: bool = False, out_dir: str = OUT_DIR,
+          defines=()) -> str:
+    """Builds the library into out_dir (default: the package's _build/).
+    `defines` are extra preprocessor symbols for diagnostic variants."""
+    lib = os.path.join(out_dir, "libqli_gb300.so")
+    os.makedirs(out_dir, exist_ok=True)
+    stamp_path = os.path.join(out_dir, "stamp")
+    stamp = _stamp() + ":" + ",".join(defines)
+    if not force and os.path.exists(lib) and os.path.exists(stamp_path):
         with open(stamp_path) as f:
             if f.read() == stamp:
-                return LIB
+                return lib
     with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
-        objs = list(ex.map(lambda u: _compile(u, verbose), UNITS))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+        objs = list(ex.map(lambda u: _compile(u, verbose, out_dir, defines), UNITS))
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [NVCC] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

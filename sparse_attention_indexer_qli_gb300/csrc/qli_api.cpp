@@ -91,7 +91,12 @@ qli_status check_device() {
 // every consumer call take the streaming kernel; prefill-shaped calls take
 // the group kernel, which shares each K tile between up to 256/N tokens.
 bool use_stream_path(const qli_args& a) {
+#ifdef QLI_TILE_KERNEL_ONLY
+  (void)a;
+  return false;
+#else
   return a.cand_mode == QLI_CAND_CONSUMER || static_cast<int64_t>(a.T) <= 2 * static_cast<int64_t>(a.B);
+#endif
 }
 
 WsLayout workspace_layout(const qli_args& a) {
@@ -128,6 +133,9 @@ WsLayout workspace_layout(const qli_args& a) {
   const bool cons = a.cand_mode == QLI_CAND_CONSUMER;
   L.cand_list = take(cons ? 4 * T * C : 0);
   L.cand_cnt = take(cons ? 4 * T : 0);
+  const size_t kstride = round_up(static_cast<size_t>(cap), kTile);
+  L.kf16 = take(L.stream_path ? 0 : 2 * kHeadDim * static_cast<size_t>(B) * kstride);
+  L.ks32 = take(L.stream_path ? 0 : 4 * static_cast<size_t>(B) * kstride);
   L.scores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Lrow));
   L.bscores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Brow));
   L.total = off;
@@ -176,6 +184,14 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.unit_start = reinterpret_cast<int32_t*>(w + L.unit_start);
   d.counter = reinterpret_cast<uint32_t*>(w + L.counter);
   d.stream_path = L.stream_path;
+#ifdef QLI_TILE_KERNEL_ONLY
+  d.use_prefill_kernel = 0;   // diagnostic build: one CTA per (tile, group)
+#else
+  d.use_prefill_kernel = 1;
+#endif
+  d.kf16 = reinterpret_cast<__half*>(w + L.kf16);
+  d.ks32 = reinterpret_cast<float*>(w + L.ks32);
+  d.kstride = static_cast<int64_t>(round_up(static_cast<size_t>(d.bt_stride) * a.rows_per_page, kTile));
   d.cand_list = reinterpret_cast<int32_t*>(w + L.cand_list);
   d.cand_cnt = reinterpret_cast<int32_t*>(w + L.cand_cnt);
   d.scores = reinterpret_cast<float*>(w + L.scores);

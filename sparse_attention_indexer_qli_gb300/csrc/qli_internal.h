@@ -6,6 +6,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "qli.h"
@@ -18,6 +19,7 @@ constexpr int kBlock = 8;          // positions per candidate block
 constexpr int kMaxMmaN = 256;      // token-heads per tile (MMA N)
 constexpr int kMaxTopK = 2048;
 constexpr int kMaxCand = 2048;
+constexpr int kPrefillUnitTiles = 64;   // position tiles per prefill work unit
 
 // Everything a kernel needs, passed by value (a few hundred bytes).
 struct DevArgs {
@@ -55,18 +57,22 @@ struct DevArgs {
   int32_t* cand_cnt;   // [T] consumer: how many
   int32_t* unit_start; // [T+1] stream path: first score tile of token t
   uint32_t* counter;   // stream path: CTAs done in cand_prep (reset by plan)
+  __half* kf16;        // group path: [B, kstride, 128] widened K
+  float* ks32;         // group path: [B, kstride] K scales as FP32
+  int64_t kstride;     // group path: rows per request (cap rounded up to 128)
   float* scores;       // [T, Lrow]
   float* bscores;      // [T, Brow] source: block maxima
   int64_t Lrow, Brow;
   int32_t Gmax, G;     // token groups (upper bound), tokens per group
   int64_t cap;         // bt_stride * R: most positions a request can hold
   int32_t stream_path; // 1: one token per tile, persistent streaming kernel
-  int32_t num_sms;     // SMs of the device (stream path grid)
+  int32_t num_sms;     // SMs of the device (persistent grids)
+  int32_t use_prefill_kernel;  // group path: persistent prefill kernel (else one CTA per tile)
 };
 
 struct WsLayout {
   size_t err, counter, tok_V, tok_b, req_lk, req_res, req_q0, req_q1, req_g0;
-  size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, scores, bscores, total;
+  size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, kf16, ks32, scores, bscores, total;
   int64_t Lrow, Brow;
   int32_t Gmax, G;
   int32_t stream_path;
@@ -83,6 +89,8 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L);
 cudaError_t launch_plan(const DevArgs& d, cudaStream_t s);
 cudaError_t launch_score(const DevArgs& d, cudaStream_t s);
 cudaError_t launch_select(const DevArgs& d, cudaStream_t s);
+cudaError_t launch_prefill(const DevArgs& d, cudaStream_t s);
+int prefill_launches(const DevArgs& d);
 int plan_launches(const DevArgs& d);
 int score_launches(const DevArgs& d);
 int select_launches(const DevArgs& d);

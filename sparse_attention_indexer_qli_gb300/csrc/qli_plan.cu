@@ -125,11 +125,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
       }
     }
   }
-  // stream path, dense modes: token t owns ceil(V(t)/128) score tiles
+  __syncthreads();
   if (a.stream_path && a.mode != QLI_CAND_CONSUMER) {
-    __syncthreads();
+    // stream path, dense modes: token t owns ceil(V(t)/128) score tiles
     cta_scan_store<1024>(a.T, [&](int32_t t) { return (a.tok_V[t] + kTile - 1) / kTile; },
                          a.unit_start);
+  } else if (!a.stream_path) {
+    // group path: group g owns ceil(tiles/64) units of up to 64 tiles, where
+    // its last (most advanced) token sees ceil(V/128) tiles
+    cta_scan_store<1024>(
+        a.Gmax,
+        [&](int32_t g) {
+          const int32_t c = a.grp_cnt[g];
+          if (c == 0) return 0;
+          const int32_t tiles = (a.tok_V[a.grp_t0[g] + c - 1] + kTile - 1) / kTile;
+          return (tiles + kPrefillUnitTiles - 1) / kPrefillUnitTiles;
+        },
+        a.unit_start);
   }
 }
 

@@ -1,0 +1,354 @@
+// Scoring stage for prefill-shaped calls (many query tokens per request).
+//
+// Here the contraction dominates (each K row meets thousands of query
+// tokens), so the kernel is built around the tensor core:
+//  * kconv_kernel widens each request's paged INT8 index K once into a dense
+//    FP16 [cap, 128] array and its FP16 scales into FP32, in the workspace
+//    (a few MB per request: L2-resident while the main kernel runs);
+//  * prefill_kernel is persistent, one CTA per SM. A unit is one token group
+//    (up to 4 tokens of one request, MMA N = tokens*64 <= 256) and a range of
+//    up to 64 position tiles. The group's queries stay in shared memory
+//    (FP16 * 2^-10, 128-byte swizzle) for the whole unit; K tiles stream in
+//    by TMA (128-byte swizzle) through a 4-stage ring; the 128 x N FP32
+//    accumulator is double-buffered across all 512 TMEM columns.
+// Warp roles: warp 0 producer, warp 1 MMA issuer, warps 2-9 epilogue (two
+// warps per TMEM lane quarter, each summing the heads of half the group's
+// tokens).
+//
+// Numerics are those of the streaming kernel (see qli_score.cu): exact
+// FP16 products of INT8 values, exact FP32 sums, the accumulator holding
+// s/1024, then the golden chain of the guide "DeepSeek V4.1 QLI V2 与候选集成"
+// (section 当前 A3 契约) per head in ascending order.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "qli_internal.h"
+#include "qli_ptx.cuh"
+
+namespace qli {
+namespace {
+
+constexpr int kUnitTiles = kPrefillUnitTiles;
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kABytes = kTile * kHeadDim * 2;     // 32 KB FP16 tile (two 16 KB K halves)
+constexpr int kBBytes = kMaxMmaN * kHeadDim * 2;  // 64 KB: 4 tokens x 64 heads
+constexpr uint32_t kTmemCols = 512;
+
+struct Smem {
+  uint8_t a[kStages][kABytes];   // 1024-aligned
+  uint8_t b[kBBytes];            // 1024-aligned
+  __half wq[kMaxMmaN];
+  uint64_t full[kStages], empty[kStages], dfull[2], dempty[2], bfull, bempty;
+  uint32_t tmem_base;
+};
+constexpr int kSmemBytes = static_cast<int>(sizeof(Smem)) + 1024;
+
+__device__ __forceinline__ uint32_t sw128(uint32_t rows, uint32_t n, uint32_t c) {
+  return (c >> 3) * (rows * 128u) + (n >> 3) * 1024u + (n & 7u) * 128u +
+         (((c & 7u) ^ (n & 7u)) << 4);
+}
+
+// 8 INT8 -> 8 FP16 (exact), optionally times 2^-10 (exact for |x| <= 128).
+__device__ __forceinline__ uint4 widen8(uint2 v, bool div1024) {
+  const uint32_t u0 = v.x ^ 0x80808080u, u1 = v.y ^ 0x80808080u;
+  uint32_t h[4] = {__byte_perm(u0, 0x64646464u, 0x5140), __byte_perm(u0, 0x64646464u, 0x7362),
+                   __byte_perm(u1, 0x64646464u, 0x5140), __byte_perm(u1, 0x64646464u, 0x7362)};
+  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
+  const __half2 sc = __floats2half2_rn(1.0f / 1024.0f, 1.0f / 1024.0f);
+  uint4 r;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __half2 x = __hsub2(*reinterpret_cast<__half2*>(&h[k]), bias);
+    if (div1024) x = __hmul2(x, sc);
+    o[k] = *reinterpret_cast<uint32_t*>(&x);
+  }
+  return r;
+}
+
+// ---- K widening: one thread per 8 INT8 values, 16 threads per row ---------
+constexpr int kConvThreads = 256;
+
+__global__ void __launch_bounds__(kConvThreads) kconv_kernel(DevArgs a) {
+  const int b = blockIdx.y;
+  const int lk = a.req_lk[b];
+  const int row = blockIdx.x * (kConvThreads / 16) + threadIdx.x / 16;
+  const int ch = threadIdx.x % 16;
+  const int padded = (lk + kTile - 1) / kTile * kTile;
+  if (row >= padded) return;
+  uint4* dst = reinterpret_cast<uint4*>(a.kf16 + (static_cast<int64_t>(b) * a.kstride + row) * kHeadDim) + ch;
+  if (row >= lk) {   // zero tail of the last tile
+    *dst = make_uint4(0, 0, 0, 0);
+    if (ch == 0) a.ks32[static_cast<int64_t>(b) * a.kstride + row] = 0.0f;
+    return;
+  }
+  int32_t page = a.bt[static_cast<int64_t>(b) * a.bt_stride + row / a.R];
+  if (page < 0 || page >= a.num_pages) {
+    if (ch == 0) atomicOr(a.err, QLI_DEVERR_PAGE);
+    page = 0;
+  }
+  const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
+  const int r = row % a.R;
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(pg + a.k_off + r * kHeadDim) + ch);
+  *dst = widen8(v, false);
+  if (ch == 0)
+    a.ks32[static_cast<int64_t>(b) * a.kstride + row] =
+        __half2float(*reinterpret_cast<const __half*>(pg + a.s_off + r * 2));
+}
+
+// ---- unit walk -----------------------------------------------------------
+struct Unit {
+  int32_t g, t0, cnt, b, tile0, ntiles;
+};
+
+__device__ __forceinline__ Unit unit_at(const DevArgs& a, int32_t u) {
+  int32_t lo = 0, hi = a.Gmax - 1;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (a.unit_start[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  Unit x;
+  x.g = lo;
+  x.t0 = a.grp_t0[lo];
+  x.cnt = a.grp_cnt[lo];
+  x.b = a.tok_b[x.t0];
+  const int32_t vmax = a.tok_V[x.t0 + x.cnt - 1];
+  const int32_t tiles = (vmax + kTile - 1) / kTile;
+  x.tile0 = (u - a.unit_start[lo]) * kUnitTiles;
+  x.ntiles = min(kUnitTiles, tiles - x.tile0);
+  return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
+    const __grid_constant__ CUtensorMap tm_k, DevArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t U = a.unit_start[a.Gmax];
+  if (static_cast<int32_t>(blockIdx.x) >= U) return;
+
+  if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
+  if (tid == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.dfull[s], 1);
+      mbar_init(&S.dempty[s], 8);
+    }
+    mbar_init(&S.bfull, 8);
+    mbar_init(&S.bempty, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------- producer: FP16 K tiles by TMA
+    int k = 0;
+    for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x) {
+      const Unit x = unit_at(a, u);
+      for (int i = 0; i < x.ntiles && ok; ++i, ++k) {
+        const int s = k % kStages;
+        const uint32_t ph = (k / kStages) & 1;
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&S.empty[s], ph ^ 1);
+          if (ok) {
+            mbar_arrive_expect_tx(&S.full[s], kABytes);
+            const int32_t y = x.b * static_cast<int32_t>(a.kstride) + (x.tile0 + i) * kTile;
+            tma_load_3d(&S.a[s][0], &tm_k, 0, y, 0, &S.full[s]);
+            tma_load_3d(&S.a[s][kABytes / 2], &tm_k, 64, y, 0, &S.full[s]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+    }
+    if (lane == 0) {
+      for (int j = max(0, k - kStages); j < k; ++j)
+        (void)mbar_wait_bounded(&S.full[j % kStages], (j / kStages) & 1);
+      if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      int k = 0, n = 0;
+      const uint32_t b0 = smem_u32(&S.b[0]);
+      for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
+        const Unit x = unit_at(a, u);
+        const uint32_t nmma = static_cast<uint32_t>(x.cnt * a.N);
+        const uint32_t idesc = idesc_f16_m128(nmma);
+        if (!mbar_wait_bounded(&S.bfull, n & 1)) { ok = false; break; }
+        for (int i = 0; i < x.ntiles; ++i, ++k) {
+          const int s = k % kStages, ds = k & 1;
+          if (!mbar_wait_bounded(&S.full[s], (k / kStages) & 1) ||
+              !mbar_wait_bounded(&S.dempty[ds], ((k >> 1) & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(&S.a[s][0]);
+          const uint32_t d = tmem + ds * 256;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+            const uint32_t kb = kk >> 2, koff = (kk & 3) * 32;
+            mma_f16_ss(d, sdesc_k_sw128(a0 + kb * (kABytes / 2) + koff),
+                       sdesc_k_sw128(b0 + kb * (nmma * 128) + koff), idesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&S.empty[s]);
+          mma_commit(&S.dfull[ds]);
+        }
+        mma_commit(&S.bempty);   // the unit's queries are no longer read
+      }
+      if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) & 1], ((k - 1) >> 1) & 1);
+      if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+    }
+  } else {
+    // ---------------- epilogue (and query staging), 8 warps
+    const int e = warp - 2;                 // 0..7
+    const int quarter = warp & 3;
+    const int half = e >> 2;                // tokens 2*half, 2*half+1
+    const int row = 32 * quarter + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
+    const int etid = tid - 64;              // 0..255
+    int k = 0, n = 0;
+    for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
+      const Unit x = unit_at(a, u);
+      // before overwriting the queries and weights: every epilogue warp is
+      // done with the previous unit's last tile, and its MMAs are complete
+      if (k > 0 && !mbar_wait_bounded(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait_bounded(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
+      const int nrows = x.cnt * a.N;
+      for (int idx = etid; idx < nrows * 16; idx += 256) {
+        const int nn = idx >> 4, ch = idx & 15;
+        const int gi = nn / a.N, h = nn % a.N;
+        const int8_t* src = a.q + static_cast<int64_t>(x.t0 + gi) * a.q_st +
+                            static_cast<int64_t>(h) * a.q_sh + ch * 8;
+        *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) =
+            widen8(*reinterpret_cast<const uint2*>(src), true);
+      }
+      for (int nn = etid; nn < nrows; nn += 256) {
+        const int64_t o = static_cast<int64_t>(x.t0) * a.N + nn;   // tokens are consecutive
+        S.wq[nn] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.bfull);
+      // every warp's staging is complete (and visible) once bfull flips
+      if (!mbar_wait_bounded(&S.bfull, n & 1)) { ok = false; break; }
+
+      // this warp sums the heads of tokens half*G/2 .. half*G/2 + G/2 - 1
+      const int per = a.G / 2;             // 2 (N = 64) or 4 (N = 32)
+      int32_t Vt[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int gi = half * per + j;
+        Vt[j] = (j < per && gi < x.cnt) ? a.tok_V[x.t0 + gi] : 0;
+      }
+      for (int i = 0; i < x.ntiles; ++i, ++k) {
+        const int ds = k & 1;
+        if (!mbar_wait_bounded(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const int32_t pos = (x.tile0 + i) * kTile + row;
+        const float ks = a.ks32[static_cast<int64_t>(x.b) * a.kstride + pos];
+        float score[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int gi = half * per + j;
+          float acc = 0.0f;
+          if (j < per && gi < x.cnt) {     // uniform across the warp
+            const uint32_t col = tmem + lane_addr + ds * 256 + gi * a.N;
+            for (int hc = 0; hc < a.N; hc += 32) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(col + hc, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int kk = 0; kk < 32; ++kk)
+                acc = head_term_acc(acc, __uint_as_float(r[kk]), S.wq[gi * a.N + hc + kk]);
+            }
+          }
+          score[j] = __fmul_rn(acc, ks);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.dempty[ds]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int gi = half * per + j;
+          if (j >= per || gi >= x.cnt) continue;     // uniform across the warp
+          const int32_t t = x.t0 + gi;
+          const bool elig = pos < Vt[j];
+          if (elig) a.scores[static_cast<int64_t>(t) * a.Lrow + pos] = score[j];
+          if (a.mode == QLI_CAND_SOURCE) {
+            float m = elig ? score[j] : -INFINITY;
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            if ((row & (kBlock - 1)) == 0 && elig)
+              a.bscores[static_cast<int64_t>(t) * a.Brow + pos / kBlock] = m;
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Tensor map over the widened K of every request: x = 128 FP16 of a row, y =
+// row (B * cap rows of 256 B); box = 64 FP16 (128 B) x 128 rows, 128-byte
+// swizzle (the layout the MMA's smem descriptor reads).
+bool encode_kf16_map(const DevArgs& d, CUtensorMap* m) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim),
+                              static_cast<cuuint64_t>(d.B) * static_cast<cuuint64_t>(d.kstride), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
+                                 static_cast<cuuint64_t>(kHeadDim * 2) * dims[1]};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, d.kf16, dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const DevArgs& d, cudaStream_t s) {
+  if (d.T == 0 || d.B == 0) return cudaSuccess;
+  const int rows_per_cta = kConvThreads / 16;
+  dim3 cgrid(static_cast<unsigned>((d.kstride + rows_per_cta - 1) / rows_per_cta),
+             static_cast<unsigned>(d.B));
+  kconv_kernel<<<cgrid, kConvThreads, 0, s>>>(d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm;
+  if (!encode_kf16_map(d, &tm)) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<<<d.num_sms, kThreads, kSmemBytes, s>>>(tm, d);
+  return cudaGetLastError();
+}
+
+int prefill_launches(const DevArgs& d) { return (d.T > 0 && d.B > 0) ? 2 : 0; }
+
+}  // namespace qli

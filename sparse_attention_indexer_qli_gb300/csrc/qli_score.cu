@@ -594,6 +594,7 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
     stream::stream_kernel<<<d.num_sms, stream::kThreads, stream::kSmemBytes, s>>>(tm_page, tm_blk, d);
     return cudaGetLastError();
   }
+  if (d.use_prefill_kernel) return launch_prefill(d, s);
   cudaError_t e = cudaFuncSetAttribute(score_tile_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -607,6 +608,9 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int score_launches(const DevArgs& d) { return d.T > 0 ? 1 : 0; }
+int score_launches(const DevArgs& d) {
+  if (d.T == 0) return 0;
+  return (!d.stream_path && d.use_prefill_kernel) ? prefill_launches(d) : 1;
+}
 
 }  // namespace qli

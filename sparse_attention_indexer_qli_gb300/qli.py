@@ -65,7 +65,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    # QLI_LIB selects another build of the same library (diagnostic variants)
+    p = path or os.environ.get("QLI_LIB") or LIB_PATH
     if not os.path.exists(p):
         raise ImportError("libqli_gb300.so not built (run __graft_entry__.build() or "
                           "python -m sparse_attention_indexer_qli_gb300.build)")
