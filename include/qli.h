@@ -151,6 +151,26 @@ qli_status qli_scores_layout(const qli_args *a, size_t *offset, int64_t *row_str
  * this workspace) to *host_word and waits for `stream`. Synchronous. */
 qli_status qli_read_device_error(const void *workspace, uint32_t *host_word, void *stream);
 
+/* Bytes of the fixed device scratch array qli_run_static uses. */
+#define QLI_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* Same result as qli_run, for callers that cannot allocate device memory at
+ * call time (for example a serving engine whose device memory is all handed
+ * to its KV-cache pool at start-up, or a C program with no device allocator).
+ * The pages describe no counterpart of this entry point; it is a property of
+ * this library only.
+ * Instead of a caller workspace it uses one array of QLI_STATIC_SCRATCH_BYTES
+ * compiled into the library, held on every GPU that loads the library until
+ * the process exits. Nothing is allocated or freed. The array's device
+ * address is looked up on the first call made on each device, with that
+ * device current; make that first call before any stream capture begins.
+ * Calls whose workspace need (qli_workspace_size) exceeds the array return
+ * QLI_ERR_WORKSPACE_TOO_SMALL without launching anything. All calls share the
+ * array and it keeps the previous call's contents (none of them has to start
+ * at zero); calls that overlap on the GPU race on it, so issue them in order
+ * on one stream. Inputs, outputs, stream and errors are as for qli_run. */
+qli_status qli_run_static(const qli_args *a, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *qli_status_string(qli_status s);
 

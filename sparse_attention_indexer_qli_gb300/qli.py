@@ -55,7 +55,7 @@ class Args(ctypes.Structure):
 
 EXPORTS = ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage", "qli_launch_count",
            "qli_scores_layout", "qli_read_device_error", "qli_status_string", "qli_abi_version",
-           "qli_args_size"]
+           "qli_args_size", "qli_run_static"]
 
 _lib = None
 
@@ -79,6 +79,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.qli_launch_count.argtypes = [P, c_int32, ctypes.POINTER(c_int32)]
     L.qli_scores_layout.argtypes = [P, ctypes.POINTER(c_size_t), ctypes.POINTER(c_int64)]
     L.qli_read_device_error.argtypes = [c_void_p, ctypes.POINTER(c_uint32), c_void_p]
+    L.qli_run_static.argtypes = [P, c_void_p]
+    L.qli_run_static.restype = c_int32
     L.qli_status_string.argtypes = [c_int32]
     L.qli_status_string.restype = ctypes.c_char_p
     L.qli_abi_version.restype = c_int32
@@ -183,6 +185,12 @@ class Call:
     def run(self, workspace, stream=None):
         _check(lib().qli_run(ctypes.byref(self.args), _ptr(workspace), workspace.numel(),
                              _stream(stream)), "qli_run")
+        return self.indices, self.cand
+
+    def run_static(self, stream=None):
+        """qli_run_static: the same call on the library's fixed scratch array
+        (for callers that cannot allocate a workspace)."""
+        _check(lib().qli_run_static(ctypes.byref(self.args), _stream(stream)), "qli_run_static")
         return self.indices, self.cand
 
     def run_stage(self, stage: int, workspace, stream=None):
