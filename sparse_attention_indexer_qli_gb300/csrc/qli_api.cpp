@@ -12,6 +12,7 @@
 //    size exactly 8;
 //  section 构建与回归覆盖 — the TND candidate tensor holds T * N_k * blocks
 //    elements (T already spans every request; no extra factor of B).
+#include <atomic>
 #include <cstring>
 
 #include "qli_internal.h"
@@ -75,17 +76,40 @@ qli_status validate(const qli_args* a) {
   return QLI_OK;
 }
 
-qli_status check_device() {
+// Per device ordinal below 64: 0 = not yet queried, -1 = not an sm_103
+// device, otherwise its SM count. Device properties never change within a
+// process, so they are queried once.
+std::atomic<int> g_device_sms[64];
+
+qli_status device_sms(int* sms) {
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QLI_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return QLI_ERR_CUDA;
-  if (major != 10 || minor != 3) return QLI_ERR_DEVICE;
+  int known = (dev >= 0 && dev < 64) ? g_device_sms[dev].load(std::memory_order_relaxed) : 0;
+  if (known == 0) {
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&known, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QLI_ERR_CUDA;
+    if (major != 10 || minor != 3) known = -1;
+    if (dev >= 0 && dev < 64) g_device_sms[dev].store(known, std::memory_order_relaxed);
+  }
+  if (known < 0) return QLI_ERR_DEVICE;
+  *sms = known;
   return QLI_OK;
 }
 
 }  // namespace
+
+cudaError_t ensure_smem_limit(const void* func, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_relaxed);
+  return e;
+}
 
 // Decode-shaped calls (at most two query tokens per request on average) and
 // every consumer call take the streaming kernel; prefill-shaped calls take
@@ -126,7 +150,7 @@ WsLayout workspace_layout(const qli_args& a) {
   L.req_res = take(4 * B);
   L.req_q0 = take(4 * B);
   L.req_q1 = take(4 * B);
-  L.req_g0 = take(4 * B);
+  L.req_g0 = take(4 * (B + 1));
   L.grp_t0 = take(4 * static_cast<size_t>(L.Gmax));
   L.grp_cnt = take(4 * static_cast<size_t>(L.Gmax));
   L.unit_start = take(4 * static_cast<size_t>(T + 1));
@@ -136,6 +160,16 @@ WsLayout workspace_layout(const qli_args& a) {
   const size_t kstride = round_up(static_cast<size_t>(cap), kTile);
   L.kf16 = take(L.stream_path ? 0 : 2 * kHeadDim * static_cast<size_t>(B) * kstride);
   L.ks32 = take(L.stream_path ? 0 : 4 * static_cast<size_t>(B) * kstride);
+  // long-row selection scratch, only when a row can exceed shared memory
+  const int64_t longest = L.Lrow > L.Brow ? L.Lrow : L.Brow;
+  L.lchunks = longest > kSmemKeys ? static_cast<int32_t>((longest + kLongChunk - 1) / kLongChunk) : 0;
+  const size_t rows2 = 2 * static_cast<size_t>(T);
+  L.lext = take(L.lchunks ? 16 * rows2 : 0);            // 4 words per row
+  L.lhist = take(L.lchunks ? 4 * 4096 * rows2 : 0);
+  L.lcount = take(L.lchunks ? 4 * rows2 * L.lchunks : 0);
+  L.long_bytes = L.lchunks ? (off - L.lext) : 0;          // zeroed before the passes
+  L.lkey = take(L.lchunks ? 4 * rows2 * L.lchunks * kLongChunkCap : 0);
+  L.lid = take(L.lchunks ? 4 * rows2 * L.lchunks * kLongChunkCap : 0);
   L.scores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Lrow));
   L.bscores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Brow));
   L.total = off;
@@ -189,6 +223,13 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
 #else
   d.use_prefill_kernel = 1;
 #endif
+  d.lext = reinterpret_cast<uint32_t*>(w + L.lext);
+  d.lhist = reinterpret_cast<uint32_t*>(w + L.lhist);
+  d.lcount = reinterpret_cast<int32_t*>(w + L.lcount);
+  d.lkey = reinterpret_cast<uint32_t*>(w + L.lkey);
+  d.lid = reinterpret_cast<int32_t*>(w + L.lid);
+  d.lchunks = L.lchunks;
+  d.long_zero_bytes = L.long_bytes;
   d.kf16 = reinterpret_cast<__half*>(w + L.kf16);
   d.ks32 = reinterpret_cast<float*>(w + L.ks32);
   d.kstride = static_cast<int64_t>(round_up(static_cast<size_t>(d.bt_stride) * a.rows_per_page, kTile));
@@ -215,13 +256,9 @@ qli_status run_stages(const qli_args* a, void* ws, size_t bytes, int32_t stage, 
   if (ws == nullptr || bytes < L.total) return QLI_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(ws, kAlign)) return QLI_ERR_ALIGNMENT;
   if (L.Gmax > 65535) return QLI_ERR_UNSUPPORTED;
-  st = check_device();
-  if (st != QLI_OK) return st;
   DevArgs d = make_dev_args(*a, ws, L);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return QLI_ERR_CUDA;
+  st = device_sms(&d.num_sms);
+  if (st != QLI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (stage == 0 || stage == QLI_STAGE_PLAN) e = launch_plan(d, s);

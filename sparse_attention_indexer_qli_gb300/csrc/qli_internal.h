@@ -3,6 +3,7 @@
 // stage launchers. Not part of the public ABI (include/qli.h is).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -20,6 +21,10 @@ constexpr int kMaxMmaN = 256;      // token-heads per tile (MMA N)
 constexpr int kMaxTopK = 2048;
 constexpr int kMaxCand = 2048;
 constexpr int kPrefillUnitTiles = 64;   // position tiles per prefill work unit
+constexpr int kSmemKeys = 48 * 1024;    // keys one selection CTA holds in shared memory
+constexpr int kLongChunk = 16384;       // row entries per CTA in the long-row passes
+constexpr int kLongChunkCap = 2048;     // candidates kept per chunk
+constexpr int kLongCandCap = 16384;     // candidates kept per long row
 
 // Everything a kernel needs, passed by value (a few hundred bytes).
 struct DevArgs {
@@ -50,7 +55,7 @@ struct DevArgs {
   int32_t* req_res;    // [B] sanitised residual
   int32_t* req_q0;     // [B] sanitised first token
   int32_t* req_q1;     // [B] sanitised end token
-  int32_t* req_g0;     // [B] first token group of the request
+  int32_t* req_g0;     // [B+1] first token group of the request (prefix)
   int32_t* grp_t0;     // [Gmax] first token of a group
   int32_t* grp_cnt;    // [Gmax] tokens in the group (0 = unused)
   int32_t* cand_list;  // [T, C] consumer: sorted distinct usable block IDs
@@ -60,6 +65,15 @@ struct DevArgs {
   __half* kf16;        // group path: [B, kstride, 128] widened K
   float* ks32;         // group path: [B, kstride] K scales as FP32
   int64_t kstride;     // group path: rows per request (cap rounded up to 128)
+  // long rows (longer than the keys one CTA holds in shared memory): row
+  // r = 2t (positions) or 2t+1 (source blocks)
+  uint32_t* lext;      // [2T, 4] max key, max complemented key, eligible count, unused
+  uint32_t* lhist;     // [2T, 4096] digit histogram below the row's common prefix
+  int32_t* lcount;     // [2T, lchunks] candidates found per chunk
+  uint32_t* lkey;      // [2T, lchunks, kLongChunkCap] candidate keys, position order
+  int32_t* lid;        // [2T, lchunks, kLongChunkCap] candidate ids
+  int32_t lchunks;     // chunks per long row (0: no row is long)
+  size_t long_zero_bytes;  // bytes from lext that start each call at zero
   float* scores;       // [T, Lrow]
   float* bscores;      // [T, Brow] source: block maxima
   int64_t Lrow, Brow;
@@ -73,6 +87,8 @@ struct DevArgs {
 struct WsLayout {
   size_t err, counter, tok_V, tok_b, req_lk, req_res, req_q0, req_q1, req_g0;
   size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, kf16, ks32, scores, bscores, total;
+  size_t lext, lhist, lcount, lkey, lid, long_bytes;   // long-row selection (zeroed region: lext..lcount)
+  int32_t lchunks;
   int64_t Lrow, Brow;
   int32_t Gmax, G;
   int32_t stream_path;
@@ -81,6 +97,10 @@ struct WsLayout {
 // The streaming (decode) kernel takes one token per tile; the group kernel
 // shares a tile between up to 256/N tokens of one request (prefill).
 bool use_stream_path(const qli_args& a);
+
+// Raises `func`'s dynamic shared-memory limit to `bytes` once per device
+// (`done` holds one bit per device ordinal below 64; others always set it).
+cudaError_t ensure_smem_limit(const void* func, int bytes, std::atomic<uint64_t>& done);
 
 WsLayout workspace_layout(const qli_args& a);
 DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L);

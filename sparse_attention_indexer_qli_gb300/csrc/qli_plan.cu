@@ -67,6 +67,8 @@ __device__ void cta_scan_store(int32_t n, F f, int32_t* out) {
 // of every token and the token groups that share one score tile.
 __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   const int tid = threadIdx.x;
+  __shared__ uint32_t s_err;
+  if (tid == 0) s_err = 0u;
   for (int t = tid; t < a.T; t += blockDim.x) {
     a.tok_V[t] = 0;
     a.tok_b[t] = -1;
@@ -74,35 +76,37 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   for (int g = tid; g < a.Gmax; g += blockDim.x) a.grp_cnt[g] = 0;
   __syncthreads();
 
-  if (tid == 0) {
-    uint32_t e = 0;
-    int32_t prev = 0, groups = 0;
-    if (a.B > 0 && a.cu[0] != 0) e |= QLI_DEVERR_SEQLENS;
-    for (int b = 0; b < a.B; ++b) {
-      const int32_t c0 = a.cu[b], c1 = a.cu[b + 1];
-      const int32_t q0 = min(max(c0, prev), a.T);
-      const int32_t q1 = min(max(c1, q0), a.T);
-      if (c0 != q0 || c1 != q1) e |= QLI_DEVERR_SEQLENS;
-      prev = q1;
-      int32_t lk = a.k_lens[b];
-      if (lk < 0 || lk > a.cap) {
-        e |= QLI_DEVERR_KLEN;
-        lk = lk < 0 ? 0 : static_cast<int32_t>(a.cap);
-      }
-      int32_t res = a.residual ? a.residual[b] : 0;
-      if (res < 0 || res >= a.ratio) {
-        e |= QLI_DEVERR_RESIDUAL;
-        res = 0;
-      }
-      a.req_q0[b] = q0;
-      a.req_q1[b] = q1;
-      a.req_lk[b] = lk;
-      a.req_res[b] = res;
-      a.req_g0[b] = groups;
-      groups += (q1 - q0 + a.G - 1) / a.G;
+  // every request on its own: clamp the query range into [0, T], the
+  // compressed length into [0, cap] and the residual into [0, ratio)
+  uint32_t e = 0u;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int32_t c0 = a.cu[b], c1 = a.cu[b + 1];
+    const int32_t q0 = min(max(c0, 0), a.T);
+    const int32_t q1 = min(max(c1, q0), a.T);
+    if (c0 != q0 || c1 != q1 || (b == 0 && c0 != 0) || (b == a.B - 1 && c1 != a.T))
+      e |= QLI_DEVERR_SEQLENS;
+    int32_t lk = a.k_lens[b];
+    if (lk < 0 || lk > a.cap) {
+      e |= QLI_DEVERR_KLEN;
+      lk = lk < 0 ? 0 : static_cast<int32_t>(a.cap);
     }
-    if (prev != a.T) e |= QLI_DEVERR_SEQLENS;
-    *a.err = e;   // first writer of this call: resets the word
+    int32_t res = a.residual ? a.residual[b] : 0;
+    if (res < 0 || res >= a.ratio) {
+      e |= QLI_DEVERR_RESIDUAL;
+      res = 0;
+    }
+    a.req_q0[b] = q0;
+    a.req_q1[b] = q1;
+    a.req_lk[b] = lk;
+    a.req_res[b] = res;
+  }
+  if (e) atomicOr(&s_err, e);
+  __syncthreads();
+  // first token group of every request (groups never span two requests)
+  cta_scan_store<1024>(a.B, [&](int32_t b) { return (a.req_q1[b] - a.req_q0[b] + a.G - 1) / a.G; },
+                       a.req_g0);
+  if (tid == 0) {
+    *a.err = s_err;   // first writer of this call: resets the word
     *a.counter = 0u;
   }
   __syncthreads();

@@ -11,9 +11,9 @@
 //    (FP16 * 2^-10, 128-byte swizzle) for the whole unit; K tiles stream in
 //    by TMA (128-byte swizzle) through a 4-stage ring; the 128 x N FP32
 //    accumulator is double-buffered across all 512 TMEM columns.
-// Warp roles: warp 0 producer, warp 1 MMA issuer, warps 2-9 epilogue (two
-// warps per TMEM lane quarter, each summing the heads of half the group's
-// tokens).
+// Warp roles: warp 0 producer, warp 1 MMA issuer, warps 2-17 epilogue (four
+// warps per TMEM lane quarter, each summing the heads of one token, or of two
+// tokens when N = 32).
 //
 // Numerics are those of the streaming kernel (see qli_score.cu): exact
 // FP16 products of INT8 values, exact FP32 sums, the accumulator holding
@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kUnitTiles = kPrefillUnitTiles;
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 576;
 constexpr int kABytes = kTile * kHeadDim * 2;     // 32 KB FP16 tile (two 16 KB K halves)
 constexpr int kBBytes = kMaxMmaN * kHeadDim * 2;  // 64 KB: 4 tokens x 64 heads
 constexpr uint32_t kTmemCols = 512;
@@ -137,9 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.dfull[s], 1);
-      mbar_init(&S.dempty[s], 8);
+      mbar_init(&S.dempty[s], 16);
     }
-    mbar_init(&S.bfull, 8);
+    mbar_init(&S.bfull, 16);
     mbar_init(&S.bempty, 1);
     fence_mbar_init();
   }
@@ -206,13 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else {
-    // ---------------- epilogue (and query staging), 8 warps
-    const int e = warp - 2;                 // 0..7
+    // ---------------- epilogue (and query staging), 16 warps: warp e handles
+    // TMEM lane quarter (warp & 3) and token slot e / 4 of the group; with
+    // N = 64 that is one token (heads 0-31 and 32-63), with N = 32 two tokens
+    // (slot and slot + 4). Both TMEM loads are issued before one wait.
+    const int e = warp - 2;                 // 0..15
     const int quarter = warp & 3;
-    const int half = e >> 2;                // tokens 2*half, 2*half+1
+    const int slot = e >> 2;                // 0..3
     const int row = 32 * quarter + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
-    const int etid = tid - 64;              // 0..255
+    const int etid = tid - 64;              // 0..511
     int k = 0, n = 0;
     for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
       const Unit x = unit_at(a, u);
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       if (k > 0 && !mbar_wait_bounded(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
       if (!mbar_wait_bounded(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
       const int nrows = x.cnt * a.N;
-      for (int idx = etid; idx < nrows * 16; idx += 256) {
+      for (int idx = etid; idx < nrows * 16; idx += 512) {
         const int nn = idx >> 4, ch = idx & 15;
         const int gi = nn / a.N, h = nn % a.N;
         const int8_t* src = a.q + static_cast<int64_t>(x.t0 + gi) * a.q_st +
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) =
             widen8(*reinterpret_cast<const uint2*>(src), true);
       }
-      for (int nn = etid; nn < nrows; nn += 256) {
+      for (int nn = etid; nn < nrows; nn += 512) {
         const int64_t o = static_cast<int64_t>(x.t0) * a.N + nn;   // tokens are consecutive
         S.wq[nn] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
       }
@@ -239,50 +242,60 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       // every warp's staging is complete (and visible) once bfull flips
       if (!mbar_wait_bounded(&S.bfull, n & 1)) { ok = false; break; }
 
-      // this warp sums the heads of tokens half*G/2 .. half*G/2 + G/2 - 1
-      const int per = a.G / 2;             // 2 (N = 64) or 4 (N = 32)
-      int32_t Vt[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int gi = half * per + j;
-        Vt[j] = (j < per && gi < x.cnt) ? a.tok_V[x.t0 + gi] : 0;
-      }
+      // the (up to two) tokens this warp sums, and the TMEM columns of each
+      // 32-column half it loads
+      const bool wide = a.N == 64;
+      const int g0 = slot, g1 = wide ? slot : slot + 4;
+      const bool has0 = g0 < x.cnt, has1 = wide ? has0 : g1 < x.cnt;
+      const int32_t V0 = has0 ? a.tok_V[x.t0 + g0] : 0;
+      const int32_t V1 = has1 ? a.tok_V[x.t0 + g1] : 0;
+      const uint32_t c0 = static_cast<uint32_t>(g0 * a.N);
+      const uint32_t c1 = wide ? c0 + 32 : static_cast<uint32_t>(g1 * a.N);
+      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[0]);
       for (int i = 0; i < x.ntiles; ++i, ++k) {
         const int ds = k & 1;
         if (!mbar_wait_bounded(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const int32_t pos = (x.tile0 + i) * kTile + row;
         const float ks = a.ks32[static_cast<int64_t>(x.b) * a.kstride + pos];
-        float score[4];
+        uint32_t r0[32], r1[32];
+        const uint32_t base = tmem + lane_addr + ds * 256;
+        if (has0) tmem_ld_32x32b_x32(base + c0, r0);     // uniform across the warp
+        if (has1) tmem_ld_32x32b_x32(base + c1, r1);
+        tmem_ld_wait();
+        float acc0 = 0.0f, acc1 = 0.0f;
+        if (has0) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int gi = half * per + j;
-          float acc = 0.0f;
-          if (j < per && gi < x.cnt) {     // uniform across the warp
-            const uint32_t col = tmem + lane_addr + ds * 256 + gi * a.N;
-            for (int hc = 0; hc < a.N; hc += 32) {
-              uint32_t r[32];
-              tmem_ld_32x32b_x32(col + hc, r);
-              tmem_ld_wait();
+          for (int kk = 0; kk < 32; kk += 2)
+            acc0 = head_pair_acc(acc0, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]),
+                                 wq2[(c0 + kk) >> 1]);
+        }
+        if (has1) {
+          if (wide) {   // heads 32-63 of the same token continue its chain
 #pragma unroll
-              for (int kk = 0; kk < 32; ++kk)
-                acc = head_term_acc(acc, __uint_as_float(r[kk]), S.wq[gi * a.N + hc + kk]);
-            }
+            for (int kk = 0; kk < 32; kk += 2)
+              acc0 = head_pair_acc(acc0, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
+                                   wq2[(c1 + kk) >> 1]);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 32; kk += 2)
+              acc1 = head_pair_acc(acc1, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
+                                   wq2[(c1 + kk) >> 1]);
           }
-          score[j] = __fmul_rn(acc, ks);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.dempty[ds]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int gi = half * per + j;
-          if (j >= per || gi >= x.cnt) continue;     // uniform across the warp
-          const int32_t t = x.t0 + gi;
-          const bool elig = pos < Vt[j];
-          if (elig) a.scores[static_cast<int64_t>(t) * a.Lrow + pos] = score[j];
+        for (int j = 0; j < 2; ++j) {
+          const bool has = j == 0 ? has0 : (!wide && has1);
+          if (!has) continue;                 // uniform across the warp
+          const int32_t t = x.t0 + (j == 0 ? g0 : g1);
+          const float score = __fmul_rn(j == 0 ? acc0 : acc1, ks);
+          const bool elig = pos < (j == 0 ? V0 : V1);
+          if (elig) a.scores[static_cast<int64_t>(t) * a.Lrow + pos] = score;
           if (a.mode == QLI_CAND_SOURCE) {
-            float m = elig ? score[j] : -INFINITY;
+            float m = elig ? score : -INFINITY;
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
@@ -333,6 +346,8 @@ bool encode_kf16_map(const DevArgs& d, CUtensorMap* m) {
 
 }  // namespace
 
+std::atomic<uint64_t> g_smem_prefill_kernel{0};
+
 cudaError_t launch_prefill(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0 || d.B == 0) return cudaSuccess;
   const int rows_per_cta = kConvThreads / 16;
@@ -343,7 +358,7 @@ cudaError_t launch_prefill(const DevArgs& d, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   CUtensorMap tm;
   if (!encode_kf16_map(d, &tm)) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, g_smem_prefill_kernel);
   if (e != cudaSuccess) return e;
   prefill_kernel<<<d.num_sms, kThreads, kSmemBytes, s>>>(tm, d);
   return cudaGetLastError();

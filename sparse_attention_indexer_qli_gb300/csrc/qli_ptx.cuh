@@ -182,6 +182,20 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 32 consecutive 32-bit columns from registers.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 // 32 lanes x 64 consecutive 32-bit columns from registers: thread i of the
 // warp writes lane (warp's lane quarter base + i), columns col..col+63.
 __device__ __forceinline__ void tmem_st_32x32b_x64(uint32_t taddr, const uint32_t (&r)[64]) {
@@ -221,6 +235,21 @@ __device__ __forceinline__ float head_term_acc(float acc, float s, __half wq) {
   asm("{\n\t.reg .f16 t;\n\tmov.b16 t, %1;\n\tadd.rn.f32.f16 %0, t, %2;\n\t}"
       : "=f"(r)
       : "h"(p), "f"(acc));
+  return r;
+}
+
+// Two heads of the golden chain at once: x = fp16x2(relu(s_hi), relu(s_lo))
+// (one rounding each), p = x * wq2 (IEEE FP16 multiplies), then
+// acc += fp32(p.lo); acc += fp32(p.hi) — head `lo` before head `hi`.
+__device__ __forceinline__ float head_pair_acc(float acc, float s_lo, float s_hi, uint32_t wq2) {
+  uint32_t x, p;
+  asm("cvt.rn.relu.f16x2.f32 %0, %1, %2;" : "=r"(x) : "f"(s_hi), "f"(s_lo));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p) : "r"(x), "r"(wq2));
+  float r;
+  asm("{\n\t.reg .f16 lo, hi;\n\t.reg .f32 t;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.f16 t, lo, %2;\n\tadd.rn.f32.f16 %0, hi, t;\n\t}"
+      : "=f"(r)
+      : "r"(p), "f"(acc));
   return r;
 }
 

@@ -236,20 +236,31 @@ __global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
 // Persistent, one CTA per SM, each CTA owns a contiguous range of the
 // (token, tile) list, so the token's queries stay in shared memory across
 // its tiles. Warp roles:
-//   warp 0      producer: TMA bulk copies of the tile's INT8 K rows and FP16
-//               scales into a 4-stage shared-memory ring (whole pages for
-//               dense tiles; 1 KB + 16 B per 8-position block in consumer mode)
+//   warp 0      producer: TMA copies of the tile's INT8 K rows (128-byte
+//               swizzle) and FP16 scales into an 8-stage shared-memory ring
+//               (whole pages for dense tiles; 1 KB + 16 B per 8-position
+//               block in consumer mode); for dense tiles lane j resolves the
+//               page IDs of tile k0+j once per 32 tiles, so no block-table
+//               load sits between two copies
 //   warp 1      MMA: 8 x tcgen05.mma (A from TMEM, B = the token's queries
 //               from shared memory), committed to the stage's barrier
-//   warps 2-5   converters: row = position; INT8 -> FP16 in registers, stored
-//               to TMEM as the MMA's A operand; queries -> FP16 * 2^-10 in
-//               128-byte-swizzled shared memory when the token changes
-//   warps 6-9   epilogue: the golden chain per position, score store, block max
+//   warps 2-9   converters, two groups of four taking alternate tiles: row =
+//               position; INT8 -> FP16 in registers, stored to TMEM as the
+//               MMA's A operand; queries -> FP16 * 2^-10 in 128-byte-swizzled
+//               shared memory when the token changes
+//   warps 10-17 epilogue, two groups of four taking alternate tiles: the
+//               golden chain per position (a 64-long dependent FP32 add chain,
+//               so two tiles are summed at once), score store, block max
 // TMEM: 4 stages x (64 A columns + 64 accumulator columns).
 namespace stream {
 
-constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kKStages = 8;                          // shared-memory K ring
+constexpr int kStages = 4;                           // TMEM / query stages
+// warp roles: 0 producer, 1 MMA, then two groups of four converter warps,
+// then two groups of four epilogue warps
+constexpr int kConvWarp0 = 2, kEpiWarp0 = kConvWarp0 + 8, kWarpsTotal = kEpiWarp0 + 8;
+constexpr int kThreads = 32 * kWarpsTotal;
+static_assert(kThreads == 576, "stream kernel block size");
 constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per stage
 constexpr int kSBytes = kTile * 2;                   // 256 B of FP16 scales per stage
 constexpr int kBBytes = 64 * kHeadDim * 2;           // 16 KB: up to 64 heads, FP16
@@ -257,12 +268,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStageCols = 128;                 // A: 64 columns, D: 64 columns
 
 struct Smem {
-  uint8_t k[kStages][kKBytes];                       // 1024-aligned (offset 0)
+  uint8_t k[kKStages][kKBytes];                      // 1024-aligned (offset 0)
   uint8_t b[kStages][kBBytes];                       // 1024-aligned
-  uint8_t sc[kStages][kSBytes];
+  uint8_t sc[kKStages][kSBytes];
   __half wq[kStages][64];
   float ks[kStages][kTile];
-  uint64_t full[kStages], empty[kStages], afull[kStages], dfull[kStages], tempty[kStages];
+  uint64_t full[kKStages], empty[kKStages];
+  uint64_t afull[kStages], dfull[kStages], tempty[kStages];
   uint32_t tmem_base;
 };
 constexpr int kSmemBytes = static_cast<int>(sizeof(Smem)) + 1024;
@@ -324,9 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
 
   if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
   if (tid == 32) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 4);
+    }
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.afull[s], 4);
       mbar_init(&S.dfull[s], 1);
       mbar_init(&S.tempty[s], 4);
@@ -344,32 +358,48 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     Cursor c;
     c.init(a, u0);
     int issued = 0;
+    int32_t pg0 = 0, pg1 = -1;     // dense: this lane's look-ahead tile's pages
     for (int k = 0; k < nk && ok; ++k) {
-      const int s = k % kStages;
-      const uint32_t ph = (k / kStages) & 1;
+      const int s = k % kKStages;
+      const uint32_t ph = (k / kKStages) & 1;
+      if (!consumer && (k & 31) == 0) {
+        // lane j resolves tile k+j: request, pages (one or two per tile)
+        if (k + lane < nk) {
+          Cursor m;
+          m.init(a, u0 + k + lane);
+          const int32_t b = a.tok_b[m.t], V = a.tok_V[m.t];
+          const int64_t row = static_cast<int64_t>(b) * a.bt_stride;
+          const int32_t j0 = m.tile * kTile;
+          const bool two = a.R < kTile && j0 + a.R < V;   // 64-row pages: second half visible
+          pg0 = a.bt[row + j0 / a.R];
+          pg1 = two ? a.bt[row + j0 / a.R + 1] : 0;
+          if (pg0 < 0 || pg0 >= a.num_pages || pg1 < 0 || pg1 >= a.num_pages) {
+            atomicOr(a.err, QLI_DEVERR_PAGE);
+            if (pg0 < 0 || pg0 >= a.num_pages) pg0 = 0;
+            if (pg1 < 0 || pg1 >= a.num_pages) pg1 = 0;
+          }
+          if (!two) pg1 = -1;
+        }
+      }
       if (lane == 0) ok = mbar_wait_bounded(&S.empty[s], ph ^ 1);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const int32_t t = c.t, b = a.tok_b[t];
-      const int64_t bt_row = static_cast<int64_t>(b) * a.bt_stride;
       if (!consumer) {
-        const int32_t V = a.tok_V[t];
-        const int32_t j0 = c.tile * kTile;
-        const int npages = (a.R == kTile) ? 1 : ((j0 + a.R < V) ? 2 : 1);
+        const int32_t p0 = __shfl_sync(0xffffffffu, pg0, k & 31);
+        const int32_t p1 = __shfl_sync(0xffffffffu, pg1, k & 31);
         if (lane == 0) {
+          const int npages = p1 >= 0 ? 2 : 1;
           mbar_arrive_expect_tx(&S.full[s], npages * (a.R * kHeadDim + a.R * 2));
           for (int p = 0; p < npages; ++p) {
-            int32_t page = a.bt[bt_row + j0 / a.R + p];
-            if (page < 0 || page >= a.num_pages) {
-              atomicOr(a.err, QLI_DEVERR_PAGE);
-              page = 0;
-            }
+            const int32_t page = p == 0 ? p0 : p1;
             const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
             tma_load_3d(&S.k[s][p * a.R * kHeadDim], &tm_page, 0, 0, page, &S.full[s]);
             bulk_g2s(&S.sc[s][p * a.R * 2], pg + a.s_off, a.R * 2, &S.full[s]);
           }
         }
       } else {
+        const int32_t t = c.t, b = a.tok_b[t];
+        const int64_t bt_row = static_cast<int64_t>(b) * a.bt_stride;
         const int32_t nc = a.cand_cnt[t];
         const int32_t first = c.tile * (kTile / kBlock);
         const int32_t nblk = min(kTile / kBlock, nc - first);
@@ -388,15 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           tma_load_3d(&S.k[s][lane * kBlock * kHeadDim], &tm_blk, 0, row, page, &S.full[s]);
           bulk_g2s(&S.sc[s][lane * kBlock * 2], pg + a.s_off + row * 2, kBlock * 2, &S.full[s]);
         }
+        c.next(a, u0 + k + 1);
       }
       __syncwarp();
       ++issued;
-      c.next(a, u0 + k + 1);
     }
     // never leave a copy in flight: wait for the last stages issued
     if (lane == 0) {
-      for (int k = max(0, issued - kStages); k < issued; ++k)
-        (void)mbar_wait_bounded(&S.full[k % kStages], (k / kStages) & 1);
+      for (int k = max(0, issued - kKStages); k < issued; ++k)
+        (void)mbar_wait_bounded(&S.full[k % kKStages], (k / kKStages) & 1);
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
   } else if (warp == 1) {
@@ -423,25 +453,26 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) % kStages], ((k - 1) / kStages) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
-  } else if (warp < 6) {
-    // ---------------- converters: row = TMEM lane
+  } else if (warp < kEpiWarp0) {
+    // ---------------- converters: row = TMEM lane; group g takes tiles k = g mod 2
+    const int grp = (warp - kConvWarp0) >> 2;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int ctid = tid - 64;   // 0..127
-    int32_t btok[kStages];
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) btok[s] = -1;
+    const int ctid = tid - 32 * kConvWarp0 - 128 * grp;   // 0..127 within the group
+    int32_t btok0 = -1, btok1 = -1;          // token staged in the group's two stages
     Cursor c;
     c.init(a, u0);
-    for (int k = 0; k < nk; ++k) {
-      const int s = k % kStages;
+    if (grp == 1) c.next(a, u0 + 1);
+    for (int k = grp; k < nk; k += 2) {
+      const int s = k % kStages, sk = k % kKStages;
       const uint32_t ph = (k / kStages) & 1;
-      bool w1 = mbar_wait_bounded(&S.full[s], ph);
+      bool w1 = mbar_wait_bounded(&S.full[sk], (k / kKStages) & 1);
       bool w2 = w1 && mbar_wait_bounded(&S.tempty[s], ph ^ 1);
       if (!(w1 && w2)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
-      if (btok[s] != t) {
+      const bool second = (k >> 1) & 1;      // which of the group's two stages
+      if ((second ? btok1 : btok0) != t) {
         // queries of token t: FP16 * 2^-10, K-major, 128-byte swizzle
         for (int idx = ctid; idx < a.N * 16; idx += 128) {
           const int n = idx >> 4, ch = idx & 15;
@@ -454,61 +485,79 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           const int64_t o = static_cast<int64_t>(t) * a.N + n;
           S.wq[s][n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
         }
-        btok[s] = t;
+        if (second) btok1 = t; else btok0 = t;
       }
       // this thread's K row, stored 128-byte swizzled by the TMA: logical
       // chunk ch (K elements 16ch..16ch+15) sits at chunk ch ^ (row & 7); a
-      // quarter-warp (8 consecutive rows) reads 8 distinct bank groups
-      uint32_t regs[64];
-      const uint8_t* src = &S.k[s][row * kHeadDim];
+      // quarter-warp (8 consecutive rows) reads 8 distinct bank groups.
+      // Two halves of 64 K values (32 TMEM columns) each.
+      const uint8_t* src = &S.k[sk][row * kHeadDim];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
-        cvt_row16(v, &regs[8 * ch]);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t regs[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ch = 4 * half + j;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
+          cvt_row16(v, &regs[8 * j]);
+        }
+        tmem_st_32x32b_x32(tmem + lane_addr + s * kStageCols + 32 * half, regs);
       }
-      S.ks[s][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[s][row * 2]));
-      tmem_st_32x32b_x64(tmem + lane_addr + s * kStageCols, regs);
+      S.ks[s][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&S.empty[s]);
+        mbar_arrive(&S.empty[sk]);
         mbar_arrive(&S.afull[s]);
       }
       c.next(a, u0 + k + 1);
+      c.next(a, u0 + k + 2);
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
   } else {
-    // ---------------- epilogue: row = TMEM lane
+    // ---------------- epilogue: row = TMEM lane; group g takes tiles k = g mod 2
+    const int grp = (warp - kEpiWarp0) >> 2;
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     Cursor c;
     c.init(a, u0);
-    for (int k = 0; k < nk; ++k) {
+    if (grp == 1) c.next(a, u0 + 1);
+    int32_t vt = -1, V = 0;          // V of the current token, loaded once per token
+    for (int k = grp; k < nk; k += 2) {
       const int s = k % kStages;
       const uint32_t ph = (k / kStages) & 1;
+      if (c.t != vt) {
+        vt = c.t;
+        V = a.tok_V[vt];
+      }
       bool w1 = mbar_wait_bounded(&S.afull[s], ph);
       bool w2 = w1 && mbar_wait_bounded(&S.dfull[s], ph);
       if (!(w1 && w2)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
       const uint32_t d_col = tmem + lane_addr + s * kStageCols + 64;
+      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[s][0]);
       float acc = 0.0f;
-      for (int hc = 0; hc < a.N; hc += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(d_col + hc, r);
-        tmem_ld_wait();
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(d_col, r0);                  // heads 0-31
+      if (a.N == 64) tmem_ld_32x32b_x32(d_col + 32, r1);   // heads 32-63 (uniform)
+      tmem_ld_wait();
 #pragma unroll
-        for (int kk = 0; kk < 32; ++kk)
-          acc = head_term_acc(acc, __uint_as_float(r[kk]), S.wq[s][hc + kk]);
+      for (int kk = 0; kk < 32; kk += 2)
+        acc = head_pair_acc(acc, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]), wq2[kk >> 1]);
+      if (a.N == 64) {
+#pragma unroll
+        for (int kk = 0; kk < 32; kk += 2)
+          acc = head_pair_acc(acc, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
+                              wq2[(32 + kk) >> 1]);
       }
       const float score = __fmul_rn(acc, S.ks[s][row]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.tempty[s]);
 
-      const int32_t V = a.tok_V[t];
       float* srow = a.scores + static_cast<int64_t>(t) * a.Lrow;
       if (!consumer) {
         const int32_t pos = c.tile * kTile + row;
@@ -531,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         }
       }
       c.next(a, u0 + k + 1);
+      c.next(a, u0 + k + 2);
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
   }
@@ -581,22 +631,23 @@ bool encode_k_map(const DevArgs& d, int box_rows, CUtensorMap* m) {
 
 }  // namespace
 
+std::atomic<uint64_t> g_smem_stream_stream_kernel{0};
+
+std::atomic<uint64_t> g_smem_score_tile_kernel{0};
+
 cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
   if (d.stream_path) {
     CUtensorMap tm_page, tm_blk;
     if (!encode_k_map(d, d.R, &tm_page) || !encode_k_map(d, kBlock, &tm_blk))
       return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(stream::stream_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         stream::kSmemBytes);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream::stream_kernel), stream::kSmemBytes, g_smem_stream_stream_kernel);
     if (e != cudaSuccess) return e;
     stream::stream_kernel<<<d.num_sms, stream::kThreads, stream::kSmemBytes, s>>>(tm_page, tm_blk, d);
     return cudaGetLastError();
   }
   if (d.use_prefill_kernel) return launch_prefill(d, s);
-  cudaError_t e = cudaFuncSetAttribute(score_tile_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_tile_kernel), kSmemBytes, g_smem_score_tile_kernel);
   if (e != cudaSuccess) return e;
   dim3 grid;
   if (d.mode == QLI_CAND_CONSUMER) {

@@ -11,10 +11,11 @@
 //
 // Ranking reading: higher score first, equal scores (with -0 == +0) by the
 // lower position / block ID. The selected entries are found with an exact
-// 4-pass radix select over order-preserving 32-bit keys, then written in
-// position order by one ordered pass, so no sort is needed. Rows that fit
-// are first copied into shared memory as keys, so the passes never go back
-// to L2; longer rows are read from L2 on every pass.
+// radix select over order-preserving 32-bit keys, digit by digit below the
+// bits that every eligible key of the row shares, then written in position
+// order by two warp-segmented sweeps, so no sort is needed. Rows that fit are
+// first copied into shared memory as keys, so the passes never go back to
+// L2; longer rows are read from L2 on every pass.
 #include <cuda_fp16.h>
 
 #include "qli_internal.h"
@@ -24,7 +25,6 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSmemKeys = 48 * 1024;          // keys cached per row (192 KB)
 
 // Order-preserving map of a finite FP32 score to a non-zero uint32 key
 // (larger score -> larger key; -0 and +0 map to the same key). Key 0 is kept
@@ -37,44 +37,17 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 struct Shared {
   uint32_t hist[256];
-  int warp_cnt[kWarps];
+  int warp_a[kWarps], warp_b[kWarps];
+  uint32_t red[kWarps][3];
   uint32_t sel[2];
 };
-
-// Exclusive count of set flags before this thread over the whole CTA, and
-// the CTA total. Every thread must call it.
-__device__ __forceinline__ int cta_excl_count(bool f, Shared& sh, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned m = __ballot_sync(0xffffffffu, f);
-  if (lane == 0) sh.warp_cnt[warp] = __popc(m);
-  __syncthreads();
-  int base = 0;
-  total = 0;
-#pragma unroll 8
-  for (int w = 0; w < kWarps; ++w) {
-    const int c = sh.warp_cnt[w];
-    base += (w < warp) ? c : 0;
-    total += c;
-  }
-  __syncthreads();
-  return base + __popc(m & ((1u << lane) - 1u));
-}
-
-__device__ __forceinline__ int cta_sum(int v, Shared& sh) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) sh.warp_cnt[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int s = 0;
-  for (int w = 0; w < kWarps; ++w) s += sh.warp_cnt[w];
-  __syncthreads();
-  return s;
-}
 
 // A row of the selection: entry s has a key (0 = not eligible) and an id.
 struct Row {
   const float* vals;      // score row
   const int32_t* blocks;  // consumer: sorted candidate blocks (slot -> position)
   const uint32_t* cached; // keys in shared memory, or nullptr
+  const int32_t* ids;     // candidate rows: the id of each cached key, or nullptr
   int32_t len;            // entries in the row
   int32_t V;              // visible positions of the token
   bool consumer;
@@ -90,100 +63,406 @@ struct Row {
     return cached ? cached[s] : key_from_global(s);
   }
   __device__ __forceinline__ int32_t id(int32_t s) const {
+    if (ids) return ids[s];
     return consumer ? blocks[s / kBlock] * kBlock + (s & (kBlock - 1)) : s;
   }
 };
 
-// Histogram add with one shared atomic per distinct bin within the warp
-// (scores concentrate in few bins; plain atomics would serialise).
-__device__ __forceinline__ void hist_add(uint32_t* hist, bool valid, uint32_t bin) {
-  const uint32_t probe = valid ? bin : 0x10000u + (threadIdx.x & 31);
-  const unsigned same = __match_any_sync(0xffffffffu, probe);
-  if (valid && (__ffs(same) - 1) == static_cast<int>(threadIdx.x & 31))
-    atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(same)));
+// Row 2t+which of the selection: which 0 = the token's positions (want K),
+// which 1 = its source candidate blocks 0..nb-2 (want C-1; the last block is
+// pinned separately). len 0 when there is nothing to rank.
+__device__ __forceinline__ Row row_of(const DevArgs& a, int t, int which, int32_t& want) {
+  Row r;
+  r.cached = nullptr;
+  r.ids = nullptr;
+  r.V = a.tok_b[t] >= 0 ? a.tok_V[t] : 0;
+  if (which == 0) {
+    r.consumer = a.mode == QLI_CAND_CONSUMER;
+    r.vals = a.scores + static_cast<int64_t>(t) * a.Lrow;
+    r.blocks = r.consumer ? a.cand_list + static_cast<int64_t>(t) * a.C : nullptr;
+    r.len = r.consumer ? (a.tok_b[t] >= 0 ? a.cand_cnt[t] * kBlock : 0) : r.V;
+    want = a.topk;
+  } else {
+    const int32_t nb = (r.V + kBlock - 1) / kBlock;
+    r.consumer = false;
+    r.vals = a.bscores + static_cast<int64_t>(t) * a.Brow;
+    r.blocks = nullptr;
+    r.len = nb > a.C ? nb - 1 : 0;
+    want = a.C - 1;
+  }
+  return r;
+}
+
+// Adds the warp's live digits to `hist` with one shared atomic per distinct
+// digit: lanes holding the same digit are found by one ballot per digit bit.
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool live, uint32_t digit, int width) {
+  const unsigned live_mask = __ballot_sync(0xffffffffu, live);
+  if (live_mask == 0u) return;
+  unsigned peers = live_mask;
+  for (int b = 0; b < width; ++b) {
+    const bool bit = (digit >> b) & 1u;
+    const unsigned m = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? m : ~m;
+  }
+  const int lane = threadIdx.x & 31;
+  if (live && (__ffs(peers) - 1) == lane) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
 }
 
 // Writes the ids of the `want` best entries of `r` in ascending id order to
 // out[0..), and returns how many were written (min(want, eligible)).
 __device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int local = 0;
-  for (int32_t s = tid; s < r.len; s += kThreads) local += r.key(s) != 0u ? 1 : 0;
-  const int E = cta_sum(local, sh);
+  // eligible count and the extreme eligible keys
+  uint32_t cnt = 0u, kmax = 0u, kmin = 0xffffffffu;
+  for (int32_t s = tid; s < r.len; s += kThreads) {
+    const uint32_t k = r.key(s);
+    if (k != 0u) {
+      ++cnt;
+      kmax = max(kmax, k);
+      kmin = min(kmin, k);
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+  }
+  if (lane == 0) {
+    sh.red[warp][0] = cnt;
+    sh.red[warp][1] = kmax;
+    sh.red[warp][2] = kmin;
+  }
+  __syncthreads();
+  uint32_t E = 0u;
+  kmax = 0u;
+  kmin = 0xffffffffu;
+  for (int w = 0; w < kWarps; ++w) {
+    E += sh.red[w][0];
+    kmax = max(kmax, sh.red[w][1]);
+    kmin = min(kmin, sh.red[w][2]);
+  }
 
-  uint32_t thr = 0u;        // select keys > thr, plus `need_eq` keys == thr
+  uint32_t thr = 0u;        // take keys > thr, plus the first need_eq keys == thr
   int32_t need_eq = 0;
-  if (E > want) {
-    uint32_t prefix = 0u, mask = 0u;
-    int32_t k = want;       // rank (1-based) of the threshold among the remaining
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) sh.hist[tid] = 0u;
-      __syncthreads();
-      const int32_t rounds = (r.len + kThreads - 1) / kThreads;
-      for (int32_t i = 0; i < rounds; ++i) {
-        const int32_t s = i * kThreads + tid;
-        const uint32_t key = s < r.len ? r.key(s) : 0u;
-        const bool v = key != 0u && (key & mask) == prefix;
-        hist_add(sh.hist, v, (key >> shift) & 255u);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // lane l owns bins 255-8l .. 248-8l; find the bin holding rank k
-        uint32_t c[8];
-        uint32_t mine = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          c[j] = sh.hist[255 - 8 * lane - j];
-          mine += c[j];
+  if (E > static_cast<uint32_t>(want)) {
+    const uint32_t diff = kmax ^ kmin;
+    if (diff == 0u) {
+      thr = kmax;           // every eligible key is equal: take the first `want`
+      need_eq = want;
+    } else {
+      // bits above the highest differing bit are common to every eligible key
+      int hi = 31 - __clz(diff);               // highest bit still undecided
+      uint32_t mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
+      uint32_t prefix = kmax & mask;
+      int32_t k = want;     // rank (1-based) of the threshold among the live keys
+      while (hi >= 0) {
+        const int width = hi + 1 < 8 ? hi + 1 : 8;
+        const int shift = hi + 1 - width;
+        if (tid < 256) sh.hist[tid] = 0u;
+        __syncthreads();
+        const int32_t rounds = (r.len + kThreads - 1) / kThreads;
+        for (int32_t i = 0; i < rounds; ++i) {
+          const int32_t s = i * kThreads + tid;
+          const uint32_t key = s < r.len ? r.key(s) : 0u;
+          const bool live = key != 0u && (key & mask) == prefix;
+          hist_add(sh.hist, live, (key >> shift) & ((1u << width) - 1u), width);
         }
-        uint32_t incl = mine;
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        uint32_t above = incl - mine;
-        if (above < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= incl) {
+        __syncthreads();
+        if (warp == 0) {
+          // lane l owns 8 bins from the top; find the bin holding rank k
+          const int nb = 1 << width;
+          uint32_t c[8];
+          uint32_t mine = 0;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            if (above + c[j] >= static_cast<uint32_t>(k)) {
-              sh.sel[0] = 255u - 8u * lane - j;
-              sh.sel[1] = static_cast<uint32_t>(k) - above;
-              break;
+            const int bin = nb - 1 - 8 * lane - j;
+            c[j] = bin >= 0 ? sh.hist[bin] : 0u;
+            mine += c[j];
+          }
+          uint32_t incl = mine;
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          uint32_t above = incl - mine;
+          if (above < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= incl) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (above + c[j] >= static_cast<uint32_t>(k)) {
+                sh.sel[0] = static_cast<uint32_t>(nb - 1 - 8 * lane - j);
+                sh.sel[1] = static_cast<uint32_t>(k) - above;
+                break;
+              }
+              above += c[j];
             }
-            above += c[j];
           }
         }
+        __syncthreads();
+        prefix |= sh.sel[0] << shift;
+        mask |= ((1u << width) - 1u) << shift;
+        k = static_cast<int32_t>(sh.sel[1]);
+        __syncthreads();
+        hi = shift - 1;
       }
-      __syncthreads();
-      prefix |= sh.sel[0] << shift;
-      mask |= 255u << shift;
-      k = static_cast<int32_t>(sh.sel[1]);
-      __syncthreads();
+      thr = prefix;         // the exact key of the want-th best entry
+      need_eq = k;          // how many entries equal to it are taken
     }
-    thr = prefix;           // the exact key of the want-th best entry
-    need_eq = k;            // how many entries equal to it are taken
   }
 
-  // ordered pass: ids with key > thr, and the first need_eq with key == thr
-  int32_t written = 0, eq_seen = 0;
-  for (int32_t base = 0; base < r.len; base += kThreads) {
-    const int32_t s = base + tid;
-    const uint32_t key = s < r.len ? r.key(s) : 0u;
-    const bool sel_gt = key != 0u && key > thr;
-    bool sel = sel_gt;
-    if (need_eq > 0) {
-      const bool eq = key != 0u && key == thr;
-      int eq_total;
-      const int eq_rank = cta_excl_count(eq, sh, eq_total);
-      sel = sel_gt || (eq && eq_seen + eq_rank < need_eq);
-      eq_seen += eq_total;
-    }
-    int sel_total;
-    const int at = cta_excl_count(sel, sh, sel_total);
-    if (sel) out[written + at] = r.id(s);
-    written += sel_total;
+  // ordered output: warp w owns a contiguous segment of the row; a first
+  // sweep counts, one block-level prefix places every warp, a second sweep
+  // writes ids in row (= position) order
+  const int32_t seg = ((r.len + kWarps - 1) / kWarps + 31) & ~31;
+  const int32_t lo = warp * seg, hi = min(r.len, lo + seg);
+  const unsigned below = (1u << lane) - 1u;
+  int gt_cnt = 0, eq_cnt = 0;
+  for (int32_t base = lo; base < hi; base += 32) {
+    const int32_t s = base + lane;
+    const uint32_t key = s < hi ? r.key(s) : 0u;
+    gt_cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && key > thr));
+    eq_cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && key == thr && need_eq > 0));
   }
-  return written;
+  if (lane == 0) {
+    sh.warp_a[warp] = gt_cnt;
+    sh.warp_b[warp] = eq_cnt;
+  }
+  __syncthreads();
+  int gt_before = 0, eq_before = 0, total_gt = 0, total_eq = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    const int a = sh.warp_a[w], b = sh.warp_b[w];
+    if (w < warp) {
+      gt_before += a;
+      eq_before += b;
+    }
+    total_gt += a;
+    total_eq += b;
+  }
+  int taken_before = min(need_eq, eq_before);      // equal keys taken by earlier warps
+  int at = gt_before + taken_before;
+  int eq_seen = eq_before;
+  for (int32_t base = lo; base < hi; base += 32) {
+    const int32_t s = base + lane;
+    const uint32_t key = s < hi ? r.key(s) : 0u;
+    const bool gt = key != 0u && key > thr;
+    const bool eq = key != 0u && key == thr && need_eq > 0;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool take = gt || (eq && eq_seen + __popc(eqm & below) < need_eq);
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) out[at + __popc(tm & below)] = r.id(s);
+    at += __popc(tm);
+    eq_seen += __popc(eqm);
+  }
+  __syncthreads();
+  return total_gt + min(need_eq, total_eq);
+}
+
+// ---------------------------------------------------------------------------
+// Long rows (more entries than one CTA holds in shared memory). Three passes,
+// each spread over many CTAs (grid: chunk of 16384 entries x token x which):
+//   lstat    eligible count, max key and min key of the row;
+//   lhist    histogram of the 12 key bits just below the bits every eligible
+//            key shares (the common prefix of max and min);
+//   lcompact each CTA finds the digit holding the want-th best entry and keeps
+//            its chunk's entries at or above it, in position order, in the
+//            chunk's candidate segment.
+// The select kernel then ranks the (few thousand) candidates exactly in
+// shared memory; segments read in chunk order keep position order, so ties
+// and the ascending output need no sort. A segment or a row that overflows
+// its capacity falls back to ranking the row from L2.
+
+__device__ __forceinline__ bool long_row(const DevArgs& a, int t, int which, Row& r, int32_t& want,
+                                         int32_t& lo, int32_t& hi) {
+  r = row_of(a, t, which, want);
+  if (r.len <= kSmemKeys) return false;
+  lo = blockIdx.x * kLongChunk;
+  hi = min(r.len, lo + kLongChunk);
+  return lo < hi;
+}
+
+__global__ void __launch_bounds__(kThreads) lstat_kernel(DevArgs a) {
+  Row r;
+  int32_t want, lo, hi;
+  const int t = blockIdx.y, which = blockIdx.z;
+  if (!long_row(a, t, which, r, want, lo, hi)) return;
+  uint32_t cnt = 0u, kmax = 0u, nmin = 0u;
+  for (int32_t s = lo + threadIdx.x; s < hi; s += kThreads) {
+    const uint32_t k = r.key(s);
+    if (k != 0u) {
+      ++cnt;
+      kmax = max(kmax, k);
+      nmin = max(nmin, ~k);
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    nmin = max(nmin, __shfl_xor_sync(0xffffffffu, nmin, o));
+  }
+  if ((threadIdx.x & 31) == 0 && cnt) {
+    uint32_t* e = a.lext + 4 * (2 * static_cast<int64_t>(t) + which);
+    atomicMax(&e[0], kmax);
+    atomicMax(&e[1], nmin);
+    atomicAdd(&e[2], cnt);
+  }
+}
+
+// Digit of `key` in the long-row histogram: the (up to) 12 bits below the
+// row's common prefix.
+struct LongDigit {
+  int shift, width;
+  __device__ LongDigit(uint32_t kmax, uint32_t kmin) {
+    const uint32_t diff = kmax ^ kmin;
+    const int hi = diff ? 31 - __clz(diff) : -1;
+    width = hi + 1 < 12 ? hi + 1 : 12;
+    shift = hi + 1 - width;
+  }
+  __device__ __forceinline__ uint32_t of(uint32_t key) const {
+    return width ? (key >> shift) & ((1u << width) - 1u) : 0u;
+  }
+};
+
+__global__ void __launch_bounds__(kThreads) lhist_kernel(DevArgs a) {
+  __shared__ uint32_t hist[4096];
+  Row r;
+  int32_t want, lo, hi;
+  const int t = blockIdx.y, which = blockIdx.z;
+  if (!long_row(a, t, which, r, want, lo, hi)) return;
+  const int64_t row = 2 * static_cast<int64_t>(t) + which;
+  const uint32_t* e = a.lext + 4 * row;
+  const LongDigit dg(e[0], ~e[1]);
+  if (e[2] <= static_cast<uint32_t>(want) || dg.width == 0) return;   // no histogram needed
+  for (int i = threadIdx.x; i < 4096; i += kThreads) hist[i] = 0u;
+  __syncthreads();
+  const int32_t rounds = (hi - lo + kThreads - 1) / kThreads;
+  for (int32_t i = 0; i < rounds; ++i) {
+    const int32_t s = lo + i * kThreads + threadIdx.x;
+    const uint32_t key = s < hi ? r.key(s) : 0u;
+    hist_add(hist, key != 0u, dg.of(key), dg.width);
+  }
+  __syncthreads();
+  uint32_t* g = a.lhist + 4096 * row;
+  for (int i = threadIdx.x; i < 4096; i += kThreads)
+    if (hist[i]) atomicAdd(&g[i], hist[i]);
+}
+
+__global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
+  __shared__ int warp_cnt[kWarps];
+  __shared__ uint32_t s_digit;
+  Row r;
+  int32_t want, lo, hi;
+  const int t = blockIdx.y, which = blockIdx.z;
+  if (!long_row(a, t, which, r, want, lo, hi)) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = 2 * static_cast<int64_t>(t) + which;
+  const uint32_t* e = a.lext + 4 * row;
+  const LongDigit dg(e[0], ~e[1]);
+  // the digit holding the want-th best entry (0: keep every eligible entry)
+  if (tid == 0) s_digit = 0u;
+  __syncthreads();
+  if (e[2] > static_cast<uint32_t>(want) && dg.width > 0) {
+    const uint32_t* g = a.lhist + 4096 * row;
+    const int nb = 1 << dg.width;
+    // thread i owns bins nb-1-4i .. nb-4-4i (top down)
+    uint32_t c[4], mine = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int bin = nb - 1 - 4 * tid - j;
+      c[j] = bin >= 0 ? g[bin] : 0u;
+      mine += c[j];
+    }
+    uint32_t incl = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_cnt[warp] = static_cast<int>(incl);
+    __syncthreads();
+    uint32_t base = 0u;
+    for (int w = 0; w < warp; ++w) base += static_cast<uint32_t>(warp_cnt[w]);
+    uint32_t above = base + incl - mine;
+    const uint32_t k = static_cast<uint32_t>(want);
+    if (above < k && k <= above + mine) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (above + c[j] >= k) {
+          s_digit = static_cast<uint32_t>(nb - 1 - 4 * tid - j);
+          break;
+        }
+        above += c[j];
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t dmin = s_digit;
+  // ordered compaction of the chunk's entries with digit >= dmin
+  const int32_t seg = ((hi - lo + kWarps - 1) / kWarps + 31) & ~31;
+  const int32_t wlo = lo + warp * seg, whi = min(hi, wlo + seg);
+  const unsigned below = (1u << lane) - 1u;
+  int cnt = 0;
+  for (int32_t b = wlo; b < whi; b += 32) {
+    const int32_t s = b + lane;
+    const uint32_t key = s < whi ? r.key(s) : 0u;
+    cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && dg.of(key) >= dmin));
+  }
+  __syncthreads();
+  if (lane == 0) warp_cnt[warp] = cnt;
+  __syncthreads();
+  int at = 0, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    at += w < warp ? warp_cnt[w] : 0;
+    total += warp_cnt[w];
+  }
+  const int64_t segbase = (row * a.lchunks + blockIdx.x) * static_cast<int64_t>(kLongChunkCap);
+  for (int32_t b = wlo; b < whi; b += 32) {
+    const int32_t s = b + lane;
+    const uint32_t key = s < whi ? r.key(s) : 0u;
+    const bool keep = key != 0u && dg.of(key) >= dmin;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    const int dst = at + __popc(m & below);
+    if (keep && dst < kLongChunkCap) {
+      a.lkey[segbase + dst] = key;
+      a.lid[segbase + dst] = r.id(s);
+    }
+    at += __popc(m);
+  }
+  if (tid == 0) a.lcount[row * a.lchunks + blockIdx.x] = total;
+}
+
+// Replaces a long row by its candidates (keys and ids in shared memory, in
+// position order) when every segment fits; returns false to rank from L2.
+__device__ bool load_candidates(const DevArgs& a, int t, int which, Row& r, uint32_t* keys,
+                                int32_t* ids) {
+  __shared__ int s_total, s_over;
+  const int64_t row = 2 * static_cast<int64_t>(t) + which;
+  const int32_t nch = (r.len + kLongChunk - 1) / kLongChunk;
+  if (threadIdx.x == 0) {
+    int tot = 0, over = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int n = a.lcount[row * a.lchunks + c];
+      over |= n > kLongChunkCap;
+      tot += n;
+    }
+    s_total = tot;
+    s_over = over || tot > kLongCandCap;
+  }
+  __syncthreads();
+  if (s_over) return false;
+  int base = 0;
+  for (int c = 0; c < nch; ++c) {
+    const int n = a.lcount[row * a.lchunks + c];
+    const int64_t seg = (row * a.lchunks + c) * static_cast<int64_t>(kLongChunkCap);
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      keys[base + i] = a.lkey[seg + i];
+      ids[base + i] = a.lid[seg + i];
+    }
+    base += n;
+  }
+  __syncthreads();
+  r.cached = keys;
+  r.ids = ids;
+  r.len = s_total;
+  r.consumer = false;
+  return true;
 }
 
 // Copies the row's keys into shared memory (when it fits) and points the
@@ -204,33 +483,24 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
   const int32_t width = blocks ? a.C : a.topk;
   int32_t* out = blocks ? a.cand_out + static_cast<int64_t>(t) * a.C
                         : a.idx_out + static_cast<int64_t>(t) * a.topk;
+  int32_t want;
+  Row r = row_of(a, t, which, want);
   int32_t written = 0;
-  const int32_t V = a.tok_b[t] >= 0 ? a.tok_V[t] : 0;
-
-  Row r;
-  r.V = V;
-  r.cached = nullptr;
-  if (!blocks) {
-    r.consumer = a.mode == QLI_CAND_CONSUMER;
-    r.vals = a.scores + static_cast<int64_t>(t) * a.Lrow;
-    r.blocks = r.consumer ? a.cand_list + static_cast<int64_t>(t) * a.C : nullptr;
-    r.len = r.consumer ? (a.tok_b[t] >= 0 ? a.cand_cnt[t] * kBlock : 0) : V;
-    cache_keys(r, keys, key_cap);
-    written = select_ascending(r, a.topk, out, sh);
+  if (blocks && r.len == 0) {
+    // at most C visible blocks: all of them, in order
+    const int32_t nb = (r.V + kBlock - 1) / kBlock;
+    for (int c = tid; c < nb; c += kThreads) out[c] = c;
+    written = nb;
   } else {
-    const int32_t nb = (V + kBlock - 1) / kBlock;
-    if (nb <= a.C) {
-      for (int c = tid; c < nb; c += kThreads) out[c] = c;
-      written = nb;
+    if (r.len > key_cap) {
+      if (a.lchunks > 0)
+        (void)load_candidates(a, t, which, r, keys, reinterpret_cast<int32_t*>(keys) + kLongCandCap);
     } else {
-      // the best C-1 of blocks 0..nb-2, then the pinned last visible block
-      r.consumer = false;
-      r.vals = a.bscores + static_cast<int64_t>(t) * a.Brow;
-      r.blocks = nullptr;
-      r.len = nb - 1;
       cache_keys(r, keys, key_cap);
-      written = select_ascending(r, a.C - 1, out, sh);
-      if (tid == 0) out[written] = nb - 1;
+    }
+    written = select_ascending(r, want, out, sh);
+    if (blocks) {                      // the pinned last visible block
+      if (tid == 0) out[written] = (r.V + kBlock - 1) / kBlock - 1;
       written += 1;
     }
   }
@@ -241,17 +511,30 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
 
 cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
+  cudaError_t e;
+  if (d.lchunks > 0) {
+    e = cudaMemsetAsync(d.lext, 0, d.long_zero_bytes, s);
+    if (e != cudaSuccess) return e;
+    const dim3 g(static_cast<unsigned>(d.lchunks), static_cast<unsigned>(d.T),
+                 d.mode == QLI_CAND_SOURCE ? 2u : 1u);
+    lstat_kernel<<<g, kThreads, 0, s>>>(d);
+    lhist_kernel<<<g, kThreads, 0, s>>>(d);
+    lcompact_kernel<<<g, kThreads, 0, s>>>(d);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const int64_t longest = d.Lrow > d.Brow ? d.Lrow : d.Brow;
   const int32_t cap = static_cast<int32_t>(longest < kSmemKeys ? longest : kSmemKeys);
-  const int smem = cap * 4;
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem);
+  // candidate rows need room for kLongCandCap keys and ids
+  const int smem = 4 * (d.lchunks > 0 ? (cap > 2 * kLongCandCap ? cap : 2 * kLongCandCap) : cap);
+  static std::atomic<uint64_t> done{0};
+  e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), kSmemKeys * 4, done);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(d.T), d.mode == QLI_CAND_SOURCE ? 2u : 1u);
   select_kernel<<<grid, kThreads, smem, s>>>(d, cap);
   return cudaGetLastError();
 }
 
-int select_launches(const DevArgs& d) { return d.T > 0 ? 1 : 0; }
+int select_launches(const DevArgs& d) { return d.T > 0 ? (d.lchunks > 0 ? 4 : 1) : 0; }
 
 }  // namespace qli

@@ -175,6 +175,36 @@ def test_repeat_calls_reuse_workspace():
     assert torch.equal(a, b) and torch.equal(ca, cb)
 
 
+def test_parity_long_rows():
+    """Rows longer than one CTA's shared memory take the multi-CTA selection
+    (statistics, histogram, compaction, exact ranking of the candidates)."""
+    case = synth.make_case(81, [140000, 30001, 101], [1, 1, 1], N=64, ratio=2, topk=2048,
+                           cand_mode="source", cand_blocks=1024, name="long-rows")
+    check(case)
+
+
+def test_parity_long_rows_all_equal_scores():
+    """Every score of a long row equal: ties everywhere, the candidate buffer
+    overflows and the row is ranked from L2; TopK = the first K positions."""
+    case = synth.make_case(82, [120000, 5000], [1, 1], N=32, ratio=2, topk=1000,
+                           name="long-rows-ties")
+    case.k_rows[:] = 7
+    case.k_scale[:] = np.float16(0.01).view(np.uint16)
+    check(case)
+
+
+def test_parity_long_rows_heavy_ties():
+    """Long rows whose scores take few distinct values: the threshold key is
+    shared by many positions and the lowest positions must win."""
+    case = synth.make_case(83, [130000], [1], N=64, ratio=2, topk=1500, cand_mode="source",
+                           cand_blocks=512, name="long-rows-few-values")
+    rng = np.random.default_rng(5)
+    base = rng.integers(-127, 128, size=(16, 128), dtype=np.int8)
+    case.k_rows[:] = base[rng.integers(0, 16, size=case.k_rows.shape[0])]
+    case.k_scale[:] = np.float16(0.01).view(np.uint16)
+    check(case)
+
+
 @pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
 def test_parity_workloads_full_size(idx):
     """The five workloads at full size; the oracle checks sampled rows (all
