@@ -38,7 +38,7 @@ constexpr uint32_t kTmemCols = 512;
 struct Smem {
   uint8_t a[kStages][kABytes];   // 1024-aligned
   uint8_t b[kBBytes];            // 1024-aligned
-  __half wq[kMaxMmaN];
+  __half wq[2][kMaxMmaN];        // by unit parity: a warp may still sum the previous unit
   uint64_t full[kStages], empty[kStages], dfull[2], dempty[2], bfull, bempty;
   uint32_t tmem_base;
 };
@@ -219,10 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     int k = 0, n = 0;
     for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
       const Unit x = unit_at(a, u);
-      // before overwriting the queries and weights: every epilogue warp is
-      // done with the previous unit's last tile, and its MMAs are complete
-      if (k > 0 && !mbar_wait_bounded(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
-      if (!mbar_wait_bounded(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
+      // before overwriting the queries and this parity's weights: every
+      // epilogue warp has loaded the previous unit's last tile (so it is done
+      // with the unit before that), and the previous unit's MMAs are complete
+      if (k > 0 && !mbar_wait_warp(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait_warp(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
       const int nrows = x.cnt * a.N;
       for (int idx = etid; idx < nrows * 16; idx += 512) {
         const int nn = idx >> 4, ch = idx & 15;
@@ -234,13 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       }
       for (int nn = etid; nn < nrows; nn += 512) {
         const int64_t o = static_cast<int64_t>(x.t0) * a.N + nn;   // tokens are consecutive
-        S.wq[nn] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
+        S.wq[n & 1][nn] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.bfull);
       // every warp's staging is complete (and visible) once bfull flips
-      if (!mbar_wait_bounded(&S.bfull, n & 1)) { ok = false; break; }
+      if (!mbar_wait_warp(&S.bfull, n & 1)) { ok = false; break; }
 
       // the (up to two) tokens this warp sums, and the TMEM columns of each
       // 32-column half it loads
@@ -251,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       const int32_t V1 = has1 ? a.tok_V[x.t0 + g1] : 0;
       const uint32_t c0 = static_cast<uint32_t>(g0 * a.N);
       const uint32_t c1 = wide ? c0 + 32 : static_cast<uint32_t>(g1 * a.N);
-      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[0]);
+      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[n & 1][0]);
       for (int i = 0; i < x.ntiles; ++i, ++k) {
         const int ds = k & 1;
-        if (!mbar_wait_bounded(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const int32_t pos = (x.tile0 + i) * kTile + row;
         const float ks = a.ks32[static_cast<int64_t>(x.b) * a.kstride + pos];
@@ -263,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         if (has0) tmem_ld_32x32b_x32(base + c0, r0);     // uniform across the warp
         if (has1) tmem_ld_32x32b_x32(base + c1, r1);
         tmem_ld_wait();
+        // the accumulator is in registers: hand the TMEM stage back now
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.dempty[ds]);
         float acc0 = 0.0f, acc1 = 0.0f;
         if (has0) {
 #pragma unroll
@@ -283,9 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
                                    wq2[(c1 + kk) >> 1]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.dempty[ds]);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const bool has = j == 0 ? has0 : (!wide && has1);

@@ -267,12 +267,17 @@ constexpr int kBBytes = 64 * kHeadDim * 2;           // 16 KB: up to 64 heads, F
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kStageCols = 128;                 // A: 64 columns, D: 64 columns
 
+// wq and K scales of tile k live in slot k % kSlots: the epilogue releases a
+// TMEM stage as soon as its accumulator is in registers, so the converter of
+// tile k + 4 may already be running while tile k's golden chain is summed.
+constexpr int kSlots = 8;
+
 struct Smem {
   uint8_t k[kKStages][kKBytes];                      // 1024-aligned (offset 0)
   uint8_t b[kStages][kBBytes];                       // 1024-aligned
   uint8_t sc[kKStages][kSBytes];
-  __half wq[kStages][64];
-  float ks[kStages][kTile];
+  __half wq[kSlots][64];
+  float ks[kSlots][kTile];
   uint64_t full[kKStages], empty[kKStages];
   uint64_t afull[kStages], dfull[kStages], tempty[kStages];
   uint32_t tmem_base;
@@ -466,11 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     for (int k = grp; k < nk; k += 2) {
       const int s = k % kStages, sk = k % kKStages;
       const uint32_t ph = (k / kStages) & 1;
-      bool w1 = mbar_wait_bounded(&S.full[sk], (k / kKStages) & 1);
-      bool w2 = w1 && mbar_wait_bounded(&S.tempty[s], ph ^ 1);
+      bool w1 = mbar_wait_warp(&S.full[sk], (k / kKStages) & 1);
+      bool w2 = w1 && mbar_wait_warp(&S.tempty[s], ph ^ 1);
       if (!(w1 && w2)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
+      const int slot = k % kSlots;
       const bool second = (k >> 1) & 1;      // which of the group's two stages
       if ((second ? btok1 : btok0) != t) {
         // queries of token t: FP16 * 2^-10, K-major, 128-byte swizzle
@@ -481,11 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           const uint2 v = *reinterpret_cast<const uint2*>(src);
           *reinterpret_cast<uint4*>(&S.b[s][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v);
         }
-        for (int n = ctid; n < a.N; n += 128) {
-          const int64_t o = static_cast<int64_t>(t) * a.N + n;
-          S.wq[s][n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
-        }
         if (second) btok1 = t; else btok0 = t;
+      }
+      for (int n = ctid; n < a.N; n += 128) {
+        const int64_t o = static_cast<int64_t>(t) * a.N + n;
+        S.wq[slot][n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
       }
       // this thread's K row, stored 128-byte swizzled by the TMA: logical
       // chunk ch (K elements 16ch..16ch+15) sits at chunk ch ^ (row & 7); a
@@ -503,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         }
         tmem_st_32x32b_x32(tmem + lane_addr + s * kStageCols + 32 * half, regs);
       }
-      S.ks[s][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
+      S.ks[slot][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -532,18 +538,23 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         vt = c.t;
         V = a.tok_V[vt];
       }
-      bool w1 = mbar_wait_bounded(&S.afull[s], ph);
-      bool w2 = w1 && mbar_wait_bounded(&S.dfull[s], ph);
+      bool w1 = mbar_wait_warp(&S.afull[s], ph);
+      bool w2 = w1 && mbar_wait_warp(&S.dfull[s], ph);
       if (!(w1 && w2)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
+      const int slot = k % kSlots;
       const uint32_t d_col = tmem + lane_addr + s * kStageCols + 64;
-      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[s][0]);
-      float acc = 0.0f;
       uint32_t r0[32], r1[32];
       tmem_ld_32x32b_x32(d_col, r0);                  // heads 0-31
       if (a.N == 64) tmem_ld_32x32b_x32(d_col + 32, r1);   // heads 32-63 (uniform)
       tmem_ld_wait();
+      // the accumulator is in registers: hand the TMEM stage back now
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.tempty[s]);
+      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[slot][0]);
+      float acc = 0.0f;
 #pragma unroll
       for (int kk = 0; kk < 32; kk += 2)
         acc = head_pair_acc(acc, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]), wq2[kk >> 1]);
@@ -553,10 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           acc = head_pair_acc(acc, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
                               wq2[(32 + kk) >> 1]);
       }
-      const float score = __fmul_rn(acc, S.ks[s][row]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.tempty[s]);
+      const float score = __fmul_rn(acc, S.ks[slot][row]);
 
       float* srow = a.scores + static_cast<int64_t>(t) * a.Lrow;
       if (!consumer) {

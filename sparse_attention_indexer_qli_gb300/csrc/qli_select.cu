@@ -25,6 +25,8 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSampleKeys = 1024;      // sample size of the sample path
+constexpr int kCandCap = 8192;         // candidates the sample path keeps
 
 // Order-preserving map of a finite FP32 score to a non-zero uint32 key
 // (larger score -> larger key; -0 and +0 map to the same key). Key 0 is kept
@@ -48,6 +50,7 @@ struct Row {
   const int32_t* blocks;  // consumer: sorted candidate blocks (slot -> position)
   const uint32_t* cached; // keys in shared memory, or nullptr
   const int32_t* ids;     // candidate rows: the id of each cached key, or nullptr
+  const int32_t* idx;     // sample-path candidates: entry s is row entry idx[s]
   int32_t len;            // entries in the row
   int32_t V;              // visible positions of the token
   bool consumer;
@@ -60,11 +63,13 @@ struct Row {
     return order_key(vals[s]);
   }
   __device__ __forceinline__ uint32_t key(int32_t s) const {
-    return cached ? cached[s] : key_from_global(s);
+    const int32_t j = idx ? idx[s] : s;
+    return cached ? cached[j] : key_from_global(j);
   }
   __device__ __forceinline__ int32_t id(int32_t s) const {
     if (ids) return ids[s];
-    return consumer ? blocks[s / kBlock] * kBlock + (s & (kBlock - 1)) : s;
+    const int32_t j = idx ? idx[s] : s;
+    return consumer ? blocks[j / kBlock] * kBlock + (j & (kBlock - 1)) : j;
   }
 };
 
@@ -75,6 +80,7 @@ __device__ __forceinline__ Row row_of(const DevArgs& a, int t, int which, int32_
   Row r;
   r.cached = nullptr;
   r.ids = nullptr;
+  r.idx = nullptr;
   r.V = a.tok_b[t] >= 0 ? a.tok_V[t] : 0;
   if (which == 0) {
     r.consumer = a.mode == QLI_CAND_CONSUMER;
@@ -108,11 +114,13 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool live, uint32_t dig
   if (live && (__ffs(peers) - 1) == lane) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
 }
 
-// Writes the ids of the `want` best entries of `r` in ascending id order to
-// out[0..), and returns how many were written (min(want, eligible)).
-__device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh) {
+// Eligible count and the extreme eligible keys of a row.
+struct Stats {
+  uint32_t E, kmax, kmin;
+};
+
+__device__ Stats row_stats(const Row& r, Shared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // eligible count and the extreme eligible keys
   uint32_t cnt = 0u, kmax = 0u, kmin = 0xffffffffu;
   for (int32_t s = tid; s < r.len; s += kThreads) {
     const uint32_t k = r.key(s);
@@ -127,91 +135,98 @@ __device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
     kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
   }
+  __syncthreads();
   if (lane == 0) {
     sh.red[warp][0] = cnt;
     sh.red[warp][1] = kmax;
     sh.red[warp][2] = kmin;
   }
   __syncthreads();
-  uint32_t E = 0u;
-  kmax = 0u;
-  kmin = 0xffffffffu;
+  Stats st{0u, 0u, 0xffffffffu};
   for (int w = 0; w < kWarps; ++w) {
-    E += sh.red[w][0];
-    kmax = max(kmax, sh.red[w][1]);
-    kmin = min(kmin, sh.red[w][2]);
+    st.E += sh.red[w][0];
+    st.kmax = max(st.kmax, sh.red[w][1]);
+    st.kmin = min(st.kmin, sh.red[w][2]);
   }
+  return st;
+}
 
-  uint32_t thr = 0u;        // take keys > thr, plus the first need_eq keys == thr
-  int32_t need_eq = 0;
-  if (E > static_cast<uint32_t>(want)) {
-    const uint32_t diff = kmax ^ kmin;
-    if (diff == 0u) {
-      thr = kmax;           // every eligible key is equal: take the first `want`
-      need_eq = want;
-    } else {
-      // bits above the highest differing bit are common to every eligible key
-      int hi = 31 - __clz(diff);               // highest bit still undecided
-      uint32_t mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
-      uint32_t prefix = kmax & mask;
-      int32_t k = want;     // rank (1-based) of the threshold among the live keys
-      while (hi >= 0) {
-        const int width = hi + 1 < 8 ? hi + 1 : 8;
-        const int shift = hi + 1 - width;
-        if (tid < 256) sh.hist[tid] = 0u;
-        __syncthreads();
-        const int32_t rounds = (r.len + kThreads - 1) / kThreads;
-        for (int32_t i = 0; i < rounds; ++i) {
-          const int32_t s = i * kThreads + tid;
-          const uint32_t key = s < r.len ? r.key(s) : 0u;
-          const bool live = key != 0u && (key & mask) == prefix;
-          hist_add(sh.hist, live, (key >> shift) & ((1u << width) - 1u), width);
-        }
-        __syncthreads();
-        if (warp == 0) {
-          // lane l owns 8 bins from the top; find the bin holding rank k
-          const int nb = 1 << width;
-          uint32_t c[8];
-          uint32_t mine = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int bin = nb - 1 - 8 * lane - j;
-            c[j] = bin >= 0 ? sh.hist[bin] : 0u;
-            mine += c[j];
-          }
-          uint32_t incl = mine;
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          uint32_t above = incl - mine;
-          if (above < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= incl) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (above + c[j] >= static_cast<uint32_t>(k)) {
-                sh.sel[0] = static_cast<uint32_t>(nb - 1 - 8 * lane - j);
-                sh.sel[1] = static_cast<uint32_t>(k) - above;
-                break;
-              }
-              above += c[j];
-            }
-          }
-        }
-        __syncthreads();
-        prefix |= sh.sel[0] << shift;
-        mask |= ((1u << width) - 1u) << shift;
-        k = static_cast<int32_t>(sh.sel[1]);
-        __syncthreads();
-        hi = shift - 1;
-      }
-      thr = prefix;         // the exact key of the want-th best entry
-      need_eq = k;          // how many entries equal to it are taken
+// The key of the k-th best eligible entry (k <= E) and how many entries
+// equal to it rank within the best k: take keys > thr plus the first
+// need_eq keys == thr. Exact radix select, 8-bit digits below the bits
+// every eligible key shares.
+__device__ void radix_threshold(const Row& r, int32_t k, const Stats& st, uint32_t& thr,
+                                int32_t& need_eq, Shared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t diff = st.kmax ^ st.kmin;
+  if (diff == 0u) {
+    thr = st.kmax;          // every eligible key is equal: take the first k
+    need_eq = k;
+    return;
+  }
+  int hi = 31 - __clz(diff);               // highest bit still undecided
+  uint32_t mask = hi == 31 ? 0u : ~((2u << hi) - 1u);
+  uint32_t prefix = st.kmax & mask;
+  while (hi >= 0) {
+    const int width = hi + 1 < 8 ? hi + 1 : 8;
+    const int shift = hi + 1 - width;
+    if (tid < 256) sh.hist[tid] = 0u;
+    __syncthreads();
+    const int32_t rounds = (r.len + kThreads - 1) / kThreads;
+    for (int32_t i = 0; i < rounds; ++i) {
+      const int32_t s = i * kThreads + tid;
+      const uint32_t key = s < r.len ? r.key(s) : 0u;
+      const bool live = key != 0u && (key & mask) == prefix;
+      hist_add(sh.hist, live, (key >> shift) & ((1u << width) - 1u), width);
     }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns 8 bins from the top; find the bin holding rank k
+      const int nb = 1 << width;
+      uint32_t c[8];
+      uint32_t mine = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int bin = nb - 1 - 8 * lane - j;
+        c[j] = bin >= 0 ? sh.hist[bin] : 0u;
+        mine += c[j];
+      }
+      uint32_t incl = mine;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t above = incl - mine;
+      if (above < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= incl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (above + c[j] >= static_cast<uint32_t>(k)) {
+            sh.sel[0] = static_cast<uint32_t>(nb - 1 - 8 * lane - j);
+            sh.sel[1] = static_cast<uint32_t>(k) - above;
+            break;
+          }
+          above += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= sh.sel[0] << shift;
+    mask |= ((1u << width) - 1u) << shift;
+    k = static_cast<int32_t>(sh.sel[1]);
+    __syncthreads();
+    hi = shift - 1;
   }
+  thr = prefix;
+  need_eq = k;
+}
 
-  // ordered output: warp w owns a contiguous segment of the row; a first
-  // sweep counts, one block-level prefix places every warp, a second sweep
-  // writes ids in row (= position) order
+// Writes, in row order, the ids of the entries with key > thr and of the
+// first need_eq entries with key == thr; returns how many. Warp w owns a
+// contiguous segment: one sweep counts, one block prefix places the warps,
+// a second sweep writes.
+__device__ int ordered_output(const Row& r, uint32_t thr, int32_t need_eq, int32_t* out,
+                              Shared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t seg = ((r.len + kWarps - 1) / kWarps + 31) & ~31;
   const int32_t lo = warp * seg, hi = min(r.len, lo + seg);
   const unsigned below = (1u << lane) - 1u;
@@ -222,6 +237,7 @@ __device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared
     gt_cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && key > thr));
     eq_cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && key == thr && need_eq > 0));
   }
+  __syncthreads();
   if (lane == 0) {
     sh.warp_a[warp] = gt_cnt;
     sh.warp_b[warp] = eq_cnt;
@@ -229,16 +245,15 @@ __device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared
   __syncthreads();
   int gt_before = 0, eq_before = 0, total_gt = 0, total_eq = 0;
   for (int w = 0; w < kWarps; ++w) {
-    const int a = sh.warp_a[w], b = sh.warp_b[w];
+    const int x = sh.warp_a[w], y = sh.warp_b[w];
     if (w < warp) {
-      gt_before += a;
-      eq_before += b;
+      gt_before += x;
+      eq_before += y;
     }
-    total_gt += a;
-    total_eq += b;
+    total_gt += x;
+    total_eq += y;
   }
-  int taken_before = min(need_eq, eq_before);      // equal keys taken by earlier warps
-  int at = gt_before + taken_before;
+  int at = gt_before + min(need_eq, eq_before);
   int eq_seen = eq_before;
   for (int32_t base = lo; base < hi; base += 32) {
     const int32_t s = base + lane;
@@ -254,6 +269,93 @@ __device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared
   }
   __syncthreads();
   return total_gt + min(need_eq, total_eq);
+}
+
+// Indices s (in row order) of the entries with key >= t_lo, into idx[];
+// returns how many (idx is written only while the count stays <= cap).
+__device__ int compact_at_least(const Row& r, uint32_t t_lo, int32_t* idx, int cap, Shared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t seg = ((r.len + kWarps - 1) / kWarps + 31) & ~31;
+  const int32_t lo = warp * seg, hi = min(r.len, lo + seg);
+  const unsigned below = (1u << lane) - 1u;
+  int cnt = 0;
+  for (int32_t base = lo; base < hi; base += 32) {
+    const int32_t s = base + lane;
+    const uint32_t key = s < hi ? r.key(s) : 0u;
+    cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && key >= t_lo));
+  }
+  __syncthreads();
+  if (lane == 0) sh.warp_a[warp] = cnt;
+  __syncthreads();
+  int at = 0, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    at += w < warp ? sh.warp_a[w] : 0;
+    total += sh.warp_a[w];
+  }
+  if (total <= cap) {
+    for (int32_t base = lo; base < hi; base += 32) {
+      const int32_t s = base + lane;
+      const uint32_t key = s < hi ? r.key(s) : 0u;
+      const bool keep = key != 0u && key >= t_lo;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (keep) idx[at + __popc(m & below)] = s;
+      at += __popc(m);
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// Writes the ids of the `want` best entries of `r` in ascending id order to
+// out[0..), and returns how many were written (min(want, eligible)).
+// `scratch` (shared memory, kSampleKeys + kCandCap words) enables the sample
+// path for long cached rows: a threshold taken a little below the want-th
+// key of an evenly spaced sample keeps a few thousand candidates, compacted
+// in row order, on which the exact selection runs. If the sample misjudges
+// (fewer than `want` or more than kCandCap candidates) the exact selection
+// runs on the whole row; the result is the same either way.
+__device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh,
+                                uint32_t* scratch) {
+  const Stats st = row_stats(r, sh);
+  if (st.E <= static_cast<uint32_t>(want)) return ordered_output(r, 0u, 0, out, sh);
+  if (scratch != nullptr && r.cached != nullptr && r.idx == nullptr && r.ids == nullptr &&
+      r.len >= 4 * want && r.len > 2 * kSampleKeys) {
+    // sample of kSampleKeys evenly spaced keys (one per thread)
+    uint32_t* sample = scratch;
+    int32_t* cand = reinterpret_cast<int32_t*>(scratch + kSampleKeys);
+    for (int i = threadIdx.x; i < kSampleKeys; i += kThreads)
+      sample[i] = r.key(static_cast<int32_t>((static_cast<int64_t>(i) * r.len) / kSampleKeys));
+    __syncthreads();
+    Row sr = r;
+    sr.cached = sample;
+    sr.ids = nullptr;
+    sr.idx = nullptr;
+    sr.len = kSampleKeys;
+    sr.consumer = false;
+    const Stats ss = row_stats(sr, sh);
+    // aim 20% + 16 sample ranks past the expected rank of the want-th key
+    int32_t j = static_cast<int32_t>((static_cast<int64_t>(want) * kSampleKeys * 6) / (5 * r.len)) + 16;
+    if (ss.E > static_cast<uint32_t>(j)) {
+      uint32_t t_lo;
+      int32_t eq_unused;
+      radix_threshold(sr, j, ss, t_lo, eq_unused, sh);
+      const int n = compact_at_least(r, t_lo, cand, kCandCap, sh);
+      if (n >= want && n <= kCandCap) {
+        Row cr = r;
+        cr.idx = cand;
+        cr.len = n;
+        const Stats cs = row_stats(cr, sh);
+        uint32_t thr;
+        int32_t need_eq;
+        radix_threshold(cr, want, cs, thr, need_eq, sh);
+        return ordered_output(cr, thr, need_eq, out, sh);
+      }
+    }
+  }
+  uint32_t thr;
+  int32_t need_eq;
+  radix_threshold(r, want, st, thr, need_eq, sh);
+  return ordered_output(r, thr, need_eq, out, sh);
 }
 
 // ---------------------------------------------------------------------------
@@ -475,8 +577,12 @@ __device__ void cache_keys(Row& r, uint32_t* keys, int32_t cap) {
 }
 
 // grid.x = token, grid.y = 0: position TopK, 1: source candidate blocks.
-__global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key_cap) {
+// Dynamic shared memory: `region` words for the row's keys (or a long row's
+// candidates), then kSampleKeys + kCandCap words for the sample path.
+__global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key_cap,
+                                                          int32_t region) {
   extern __shared__ uint32_t keys[];
+  uint32_t* scratch = keys + region;
   __shared__ Shared sh;
   const int t = blockIdx.x, which = blockIdx.y, tid = threadIdx.x;
   const bool blocks = which == 1;
@@ -498,7 +604,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
     } else {
       cache_keys(r, keys, key_cap);
     }
-    written = select_ascending(r, want, out, sh);
+    written = select_ascending(r, want, out, sh, scratch);
     if (blocks) {                      // the pinned last visible block
       if (tid == 0) out[written] = (r.V + kBlock - 1) / kBlock - 1;
       written += 1;
@@ -526,12 +632,14 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   const int64_t longest = d.Lrow > d.Brow ? d.Lrow : d.Brow;
   const int32_t cap = static_cast<int32_t>(longest < kSmemKeys ? longest : kSmemKeys);
   // candidate rows need room for kLongCandCap keys and ids
-  const int smem = 4 * (d.lchunks > 0 ? (cap > 2 * kLongCandCap ? cap : 2 * kLongCandCap) : cap);
+  const int32_t region = d.lchunks > 0 ? (cap > 2 * kLongCandCap ? cap : 2 * kLongCandCap) : cap;
+  const int smem = 4 * (region + kSampleKeys + kCandCap);
   static std::atomic<uint64_t> done{0};
-  e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), kSmemKeys * 4, done);
+  e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel),
+                        4 * (kSmemKeys + kSampleKeys + kCandCap), done);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(d.T), d.mode == QLI_CAND_SOURCE ? 2u : 1u);
-  select_kernel<<<grid, kThreads, smem, s>>>(d, cap);
+  select_kernel<<<grid, kThreads, smem, s>>>(d, cap, region);
   return cudaGetLastError();
 }
 
