@@ -74,6 +74,9 @@ struct DevArgs {
   int32_t* lid;        // [2T, lchunks, kLongChunkCap] candidate ids
   int32_t lchunks;     // chunks per long row (0: no row is long)
   size_t long_zero_bytes;  // bytes from lext that start each call at zero
+  uint32_t* fhist;     // stream path: [2T, 4096] counts of the top 12 key bits of
+                       // row 2t (positions) and 2t+1 (source blocks), built by the
+                       // score stage; nullptr on the group path
   float* scores;       // [T, Lrow]
   float* bscores;      // [T, Brow] source: block maxima
   int64_t Lrow, Brow;
@@ -88,6 +91,7 @@ struct WsLayout {
   size_t err, counter, tok_V, tok_b, req_lk, req_res, req_q0, req_q1, req_g0;
   size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, kf16, ks32, scores, bscores, total;
   size_t lext, lhist, lcount, lkey, lid, long_bytes;   // long-row selection (zeroed region: lext..lcount)
+  size_t fhist;
   int32_t lchunks;
   int64_t Lrow, Brow;
   int32_t Gmax, G;

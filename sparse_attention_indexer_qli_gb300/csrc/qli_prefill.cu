@@ -120,6 +120,8 @@ __device__ __forceinline__ Unit unit_at(const DevArgs& a, int32_t u) {
   return x;
 }
 
+// 18 warps: the four SM sub-partitions hold 5, 5, 4 and 4 of them in 16K
+// registers each, which caps a thread at 96 registers
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const __grid_constant__ CUtensorMap tm_k, DevArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -225,13 +227,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       if (k > 0 && !mbar_wait_warp(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
       if (!mbar_wait_warp(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
       const int nrows = x.cnt * a.N;
-      for (int idx = etid; idx < nrows * 16; idx += 512) {
-        const int nn = idx >> 4, ch = idx & 15;
-        const int gi = nn / a.N, h = nn % a.N;
-        const int8_t* src = a.q + static_cast<int64_t>(x.t0 + gi) * a.q_st +
-                            static_cast<int64_t>(h) * a.q_sh + ch * 8;
-        *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) =
-            widen8(*reinterpret_cast<const uint2*>(src), true);
+      {
+        // every load first, then the conversions (one global latency, not eight)
+        constexpr int kPer = kMaxMmaN * 16 / 512;
+        uint2 v[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int idx = etid + 512 * i;
+          const int nn = idx >> 4, ch = idx & 15;
+          const int gi = nn / a.N, h = nn % a.N;
+          if (idx < nrows * 16)
+            v[i] = *reinterpret_cast<const uint2*>(a.q + static_cast<int64_t>(x.t0 + gi) * a.q_st +
+                                                   static_cast<int64_t>(h) * a.q_sh + ch * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int idx = etid + 512 * i;
+          const int nn = idx >> 4, ch = idx & 15;
+          if (idx < nrows * 16)
+            *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) = widen8(v[i], true);
+        }
       }
       for (int nn = etid; nn < nrows; nn += 512) {
         const int64_t o = static_cast<int64_t>(x.t0) * a.N + nn;   // tokens are consecutive

@@ -239,6 +239,19 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---- selection keys -------------------------------------------------------
+// Order-preserving map of a finite FP32 score to a non-zero uint32 key
+// (larger score -> larger key; -0 and +0 map to the same key). Key 0 is kept
+// for "not eligible". The score stage histograms the top 12 key bits.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0) u = 0;   // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
+__device__ __forceinline__ uint32_t hist_bin(uint32_t key) { return key >> (32 - kHistBits); }
+
 // ---- the golden chain, one head ----------------------------------------
 // acc += fp32( fp16( relu(fp16(s)) * wq ) ), where s already holds the
 // exact INT32 dot / 1024 in FP32 and wq = fp16(w * q_scale).

@@ -325,6 +325,8 @@ __device__ __forceinline__ void cvt_row16(const uint4 v, uint32_t* out8) {
 // tm_page: box of R rows x 128 B (a whole page's index K); tm_blk: box of
 // 8 rows x 128 B (one candidate block). Both use the 128-byte swizzle, so
 // row r's 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
+// 18 warps: the four SM sub-partitions hold 5, 5, 4 and 4 of them in 16K
+// registers each, which caps a thread at 96 registers
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_blk,
     DevArgs a) {
@@ -471,53 +473,67 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     for (int k = grp; k < nk; k += 2) {
       const int s = k % kStages, sk = k % kKStages;
       const uint32_t ph = (k / kStages) & 1;
-      bool w1 = mbar_wait_warp(&S.full[sk], (k / kKStages) & 1);
-      bool w2 = w1 && mbar_wait_warp(&S.tempty[s], ph ^ 1);
-      if (!(w1 && w2)) { ok = false; break; }
+      // the TMEM stage and its query buffer must be free (tile k-4 drained)
+      if (!mbar_wait_warp(&S.tempty[s], ph ^ 1)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
       const int slot = k % kSlots;
       const bool second = (k >> 1) & 1;      // which of the group's two stages
+      // the token's weights and (on a token change) its queries are staged
+      // before waiting for the K tile, so their global loads overlap the TMA;
+      // every load is issued before the first conversion
+      const int64_t wo = static_cast<int64_t>(t) * a.N + ctid;
+      const bool has_w = ctid < a.N;
+      const uint16_t wb = has_w ? a.w[wo] : 0, qb = has_w ? a.qs[wo] : 0;
       if ((second ? btok1 : btok0) != t) {
         // queries of token t: FP16 * 2^-10, K-major, 128-byte swizzle
-        for (int idx = ctid; idx < a.N * 16; idx += 128) {
+        constexpr int kPer = 64 * 16 / 128;   // chunks per thread at N = 64
+        uint2 v[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int idx = ctid + 128 * i;
           const int n = idx >> 4, ch = idx & 15;
-          const int8_t* src = a.q + static_cast<int64_t>(t) * a.q_st +
-                              static_cast<int64_t>(n) * a.q_sh + ch * 8;
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          *reinterpret_cast<uint4*>(&S.b[s][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v);
+          if (idx < a.N * 16)
+            v[i] = *reinterpret_cast<const uint2*>(a.q + static_cast<int64_t>(t) * a.q_st +
+                                                   static_cast<int64_t>(n) * a.q_sh + ch * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int idx = ctid + 128 * i;
+          const int n = idx >> 4, ch = idx & 15;
+          if (idx < a.N * 16)
+            *reinterpret_cast<uint4*>(&S.b[s][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v[i]);
         }
         if (second) btok1 = t; else btok0 = t;
       }
-      for (int n = ctid; n < a.N; n += 128) {
-        const int64_t o = static_cast<int64_t>(t) * a.N + n;
-        S.wq[slot][n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
-      }
+      if (has_w) S.wq[slot][ctid] = __hmul(__ushort_as_half(wb), __ushort_as_half(qb));
+      if (!mbar_wait_warp(&S.full[sk], (k / kKStages) & 1)) { ok = false; break; }
       // this thread's K row, stored 128-byte swizzled by the TMA: logical
       // chunk ch (K elements 16ch..16ch+15) sits at chunk ch ^ (row & 7); a
       // quarter-warp (8 consecutive rows) reads 8 distinct bank groups.
       // Two halves of 64 K values (32 TMEM columns) each.
+      // The whole row and its scale go to registers first, so the K stage
+      // returns to the producer before any conversion work.
       const uint8_t* src = &S.k[sk][row * kHeadDim];
+      uint4 raw[8];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        raw[ch] = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
+      S.ks[slot][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[sk]);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t regs[32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ch = 4 * half + j;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
-          cvt_row16(v, &regs[8 * j]);
-        }
+        for (int j = 0; j < 4; ++j) cvt_row16(raw[4 * half + j], &regs[8 * j]);
         tmem_st_32x32b_x32(tmem + lane_addr + s * kStageCols + 32 * half, regs);
       }
-      S.ks[slot][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&S.empty[sk]);
-        mbar_arrive(&S.afull[s]);
-      }
+      if (lane == 0) mbar_arrive(&S.afull[s]);
       c.next(a, u0 + k + 1);
       c.next(a, u0 + k + 2);
     }
@@ -566,25 +582,35 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       }
       const float score = __fmul_rn(acc, S.ks[slot][row]);
 
+      // scores, and their selection-key histograms for the select stage
       float* srow = a.scores + static_cast<int64_t>(t) * a.Lrow;
+      uint32_t* hist = a.fhist + 2 * static_cast<int64_t>(t) * kHistBins;
       if (!consumer) {
         const int32_t pos = c.tile * kTile + row;
         const bool elig = pos < V;
-        if (elig) srow[pos] = score;
+        if (elig) {
+          srow[pos] = score;
+          atomicAdd(&hist[hist_bin(order_key(score))], 1u);
+        }
         if (a.mode == QLI_CAND_SOURCE) {
           float m = elig ? score : -INFINITY;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          if ((row & (kBlock - 1)) == 0 && pos < V)
+          if ((row & (kBlock - 1)) == 0 && pos < V) {
             a.bscores[static_cast<int64_t>(t) * a.Brow + pos / kBlock] = m;
+            atomicAdd(&hist[kHistBins + hist_bin(order_key(m))], 1u);
+          }
         }
       } else {
         const int32_t slot = c.tile * kTile + row;
         if (slot < a.cand_cnt[t] * kBlock) {
           const int32_t pos =
               a.cand_list[static_cast<int64_t>(t) * a.C + slot / kBlock] * kBlock + (row & 7);
-          if (pos < V) srow[slot] = score;
+          if (pos < V) {
+            srow[slot] = score;
+            atomicAdd(&hist[hist_bin(order_key(score))], 1u);
+          }
         }
       }
       c.next(a, u0 + k + 1);
@@ -649,7 +675,9 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
     CUtensorMap tm_page, tm_blk;
     if (!encode_k_map(d, d.R, &tm_page) || !encode_k_map(d, kBlock, &tm_blk))
       return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream::stream_kernel), stream::kSmemBytes, g_smem_stream_stream_kernel);
+    cudaError_t e = cudaMemsetAsync(d.fhist, 0, sizeof(uint32_t) * kHistBins * 2 * static_cast<size_t>(d.T), s);
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_limit(reinterpret_cast<const void*>(stream::stream_kernel), stream::kSmemBytes, g_smem_stream_stream_kernel);
     if (e != cudaSuccess) return e;
     stream::stream_kernel<<<d.num_sms, stream::kThreads, stream::kSmemBytes, s>>>(tm_page, tm_blk, d);
     return cudaGetLastError();

@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 
 #include "qli_internal.h"
+#include "qli_ptx.cuh"
 
 namespace qli {
 namespace {
@@ -26,16 +27,8 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSampleKeys = 1024;      // sample size of the sample path
-constexpr int kCandCap = 8192;         // candidates the sample path keeps
-
-// Order-preserving map of a finite FP32 score to a non-zero uint32 key
-// (larger score -> larger key; -0 and +0 map to the same key). Key 0 is kept
-// for "not eligible".
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u << 1) == 0) u = 0;   // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+constexpr int kHeadWords = 4096;       // scratch head: the sample or a row's histogram
+constexpr int kCandCap = 8192;         // candidates the sample / histogram paths keep
 
 struct Shared {
   uint32_t hist[256];
@@ -306,23 +299,77 @@ __device__ int compact_at_least(const Row& r, uint32_t t_lo, int32_t* idx, int c
   return total;
 }
 
+// Threshold from a row's 4096-bin histogram of the top 12 key bits (built by
+// the score stage): copies it to `hs`, drops one count from bin `pinned`
+// (the pinned last block, which the block row does not rank; -1: none), and
+// returns the lowest key of the bin holding the want-th best entry — or 1
+// (every eligible key) when the row has no more than `want` entries. E is
+// the row's eligible count.
+__device__ uint32_t hist_threshold(const uint32_t* g, int32_t pinned, int32_t want, uint32_t* hs,
+                                   Shared& sh, uint32_t& E) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kHistBins; i += kThreads) hs[i] = g[i];
+  __syncthreads();
+  if (tid == 0 && pinned >= 0) hs[pinned] -= 1u;
+  __syncthreads();
+  // thread i owns bins 4095-4i .. 4092-4i (top down)
+  uint32_t c[4], mine = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    c[j] = hs[kHistBins - 1 - 4 * tid - j];
+    mine += c[j];
+  }
+  uint32_t incl = mine;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.warp_a[warp] = static_cast<int>(incl);
+  if (tid == 0) sh.sel[0] = 0u;
+  __syncthreads();
+  uint32_t base = 0u, total = 0u;
+  for (int w = 0; w < kWarps; ++w) {
+    base += w < warp ? static_cast<uint32_t>(sh.warp_a[w]) : 0u;
+    total += static_cast<uint32_t>(sh.warp_a[w]);
+  }
+  E = total;
+  const uint32_t k = static_cast<uint32_t>(want);
+  if (total > k) {
+    uint32_t above = base + incl - mine;
+    if (above < k && k <= above + mine) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (above + c[j] >= k) {
+          sh.sel[0] = static_cast<uint32_t>(kHistBins - 1 - 4 * tid - j);
+          break;
+        }
+        above += c[j];
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t t_lo = total > k ? (sh.sel[0] << (32 - kHistBits)) : 1u;
+  __syncthreads();
+  return t_lo == 0u ? 1u : t_lo;
+}
+
 // Writes the ids of the `want` best entries of `r` in ascending id order to
 // out[0..), and returns how many were written (min(want, eligible)).
-// `scratch` (shared memory, kSampleKeys + kCandCap words) enables the sample
+// `scratch` (shared memory, kHeadWords + kCandCap words) enables the sample
 // path for long cached rows: a threshold taken a little below the want-th
 // key of an evenly spaced sample keeps a few thousand candidates, compacted
 // in row order, on which the exact selection runs. If the sample misjudges
 // (fewer than `want` or more than kCandCap candidates) the exact selection
 // runs on the whole row; the result is the same either way.
 __device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh,
-                                uint32_t* scratch) {
-  const Stats st = row_stats(r, sh);
+                                uint32_t* scratch, const Stats* known = nullptr) {
+  const Stats st = known ? *known : row_stats(r, sh);
   if (st.E <= static_cast<uint32_t>(want)) return ordered_output(r, 0u, 0, out, sh);
   if (scratch != nullptr && r.cached != nullptr && r.idx == nullptr && r.ids == nullptr &&
       r.len >= 4 * want && r.len > 2 * kSampleKeys) {
     // sample of kSampleKeys evenly spaced keys (one per thread)
     uint32_t* sample = scratch;
-    int32_t* cand = reinterpret_cast<int32_t*>(scratch + kSampleKeys);
+    int32_t* cand = reinterpret_cast<int32_t*>(scratch + kHeadWords);
     for (int i = threadIdx.x; i < kSampleKeys; i += kThreads)
       sample[i] = r.key(static_cast<int32_t>((static_cast<int64_t>(i) * r.len) / kSampleKeys));
     __syncthreads();
@@ -418,6 +465,7 @@ struct LongDigit {
     width = hi + 1 < 12 ? hi + 1 : 12;
     shift = hi + 1 - width;
   }
+  __device__ LongDigit() : shift(32 - kHistBits), width(kHistBits) {}  // top 12 bits
   __device__ __forceinline__ uint32_t of(uint32_t key) const {
     return width ? (key >> shift) & ((1u << width) - 1u) : 0u;
   }
@@ -456,20 +504,28 @@ __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
   if (!long_row(a, t, which, r, want, lo, hi)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = 2 * static_cast<int64_t>(t) + which;
+  // digits: the score stage's top-12-bit histogram when there is one, else
+  // the 12 bits below the row's common prefix (lstat / lhist)
+  const bool fused = a.fhist != nullptr;
   const uint32_t* e = a.lext + 4 * row;
-  const LongDigit dg(e[0], ~e[1]);
+  const LongDigit dg = fused ? LongDigit() : LongDigit(e[0], ~e[1]);
+  const uint32_t* g = fused ? a.fhist + row * kHistBins : a.lhist + 4096 * row;
+  int32_t pinned = -1;     // the pinned last block is counted but not ranked
+  if (fused && which == 1) {
+    const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
+    pinned = static_cast<int32_t>(dg.of(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
+  }
   // the digit holding the want-th best entry (0: keep every eligible entry)
   if (tid == 0) s_digit = 0u;
   __syncthreads();
-  if (e[2] > static_cast<uint32_t>(want) && dg.width > 0) {
-    const uint32_t* g = a.lhist + 4096 * row;
+  if (dg.width > 0) {
     const int nb = 1 << dg.width;
     // thread i owns bins nb-1-4i .. nb-4-4i (top down)
     uint32_t c[4], mine = 0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int bin = nb - 1 - 4 * tid - j;
-      c[j] = bin >= 0 ? g[bin] : 0u;
+      c[j] = bin >= 0 ? g[bin] - (bin == pinned ? 1u : 0u) : 0u;
       mine += c[j];
     }
     uint32_t incl = mine;
@@ -479,11 +535,14 @@ __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
     }
     if (lane == 31) warp_cnt[warp] = static_cast<int>(incl);
     __syncthreads();
-    uint32_t base = 0u;
-    for (int w = 0; w < warp; ++w) base += static_cast<uint32_t>(warp_cnt[w]);
+    uint32_t base = 0u, total = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+      base += w < warp ? static_cast<uint32_t>(warp_cnt[w]) : 0u;
+      total += static_cast<uint32_t>(warp_cnt[w]);
+    }
     uint32_t above = base + incl - mine;
     const uint32_t k = static_cast<uint32_t>(want);
-    if (above < k && k <= above + mine) {
+    if (total > k && above < k && k <= above + mine) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (above + c[j] >= k) {
@@ -567,18 +626,72 @@ __device__ bool load_candidates(const DevArgs& a, int t, int which, Row& r, uint
   return true;
 }
 
-// Copies the row's keys into shared memory (when it fits) and points the
-// row at them.
-__device__ void cache_keys(Row& r, uint32_t* keys, int32_t cap) {
-  if (r.len > cap) return;
-  for (int32_t s = threadIdx.x; s < r.len; s += kThreads) keys[s] = r.key_from_global(s);
+// Copies the row's keys into shared memory (when it fits), points the row at
+// them, and returns the row's statistics gathered on the way. Dense rows are
+// read as float4, two loads in flight per thread.
+__device__ Stats cache_keys(Row& r, uint32_t* keys, int32_t cap, Shared& sh, bool& cached) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  cached = r.len <= cap;
+  uint32_t cnt = 0u, kmax = 0u, kmin = 0xffffffffu;
+  auto take = [&](int32_t s, uint32_t k) {
+    if (cached) keys[s] = k;
+    if (k != 0u) {
+      ++cnt;
+      kmax = max(kmax, k);
+      kmin = min(kmin, k);
+    }
+  };
+  if (!r.consumer) {
+    const int32_t nv = r.len >> 2;
+    const float4* v4 = reinterpret_cast<const float4*>(r.vals);
+    for (int32_t base = 0; base < nv; base += 2 * kThreads) {
+      float4 f[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int32_t i = base + u * kThreads + tid;
+        if (i < nv) f[u] = v4[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int32_t i = base + u * kThreads + tid;
+        if (i < nv) {
+          take(4 * i, order_key(f[u].x));
+          take(4 * i + 1, order_key(f[u].y));
+          take(4 * i + 2, order_key(f[u].z));
+          take(4 * i + 3, order_key(f[u].w));
+        }
+      }
+    }
+    for (int32_t s = 4 * nv + tid; s < r.len; s += kThreads) take(s, order_key(r.vals[s]));
+  } else {
+#pragma unroll 4
+    for (int32_t s = tid; s < r.len; s += kThreads) take(s, r.key_from_global(s));
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+  }
   __syncthreads();
-  r.cached = keys;
+  if (lane == 0) {
+    sh.red[warp][0] = cnt;
+    sh.red[warp][1] = kmax;
+    sh.red[warp][2] = kmin;
+  }
+  __syncthreads();
+  Stats st{0u, 0u, 0xffffffffu};
+  for (int w = 0; w < kWarps; ++w) {
+    st.E += sh.red[w][0];
+    st.kmax = max(st.kmax, sh.red[w][1]);
+    st.kmin = min(st.kmin, sh.red[w][2]);
+  }
+  if (cached) r.cached = keys;
+  return st;
 }
 
-// grid.x = token, grid.y = 0: position TopK, 1: source candidate blocks.
 // Dynamic shared memory: `region` words for the row's keys (or a long row's
-// candidates), then kSampleKeys + kCandCap words for the sample path.
+// candidates), then kHeadWords + kCandCap words for the sample and
+// histogram paths.
 __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key_cap,
                                                           int32_t region) {
   extern __shared__ uint32_t keys[];
@@ -601,10 +714,43 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
     if (r.len > key_cap) {
       if (a.lchunks > 0)
         (void)load_candidates(a, t, which, r, keys, reinterpret_cast<int32_t*>(keys) + kLongCandCap);
+      written = select_ascending(r, want, out, sh, scratch);
+    } else if (a.fhist != nullptr) {
+      // the score stage's histogram gives the threshold bin up front: one
+      // pass caches the row, the entries at or above it are compacted in row
+      // order and ranked exactly
+      int32_t pinned = -1;
+      if (blocks) {
+        const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
+        pinned = static_cast<int32_t>(
+            hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
+      }
+      uint32_t E;
+      const uint32_t t_lo = hist_threshold(
+          a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins, pinned, want, scratch, sh, E);
+      bool cached;
+      const Stats st = cache_keys(r, keys, key_cap, sh, cached);
+      int32_t* cand = reinterpret_cast<int32_t*>(scratch + kHeadWords);
+      const int n = st.E <= static_cast<uint32_t>(want) ? 0 : compact_at_least(r, t_lo, cand, kCandCap, sh);
+      if (st.E <= static_cast<uint32_t>(want)) {
+        written = ordered_output(r, 0u, 0, out, sh);
+      } else if (n >= want && n <= kCandCap) {
+        Row cr = r;
+        cr.idx = cand;
+        cr.len = n;
+        const Stats cs = row_stats(cr, sh);
+        uint32_t thr;
+        int32_t need_eq;
+        radix_threshold(cr, want, cs, thr, need_eq, sh);
+        written = ordered_output(cr, thr, need_eq, out, sh);
+      } else {
+        written = select_ascending(r, want, out, sh, nullptr, &st);
+      }
     } else {
-      cache_keys(r, keys, key_cap);
+      bool cached;
+      const Stats st = cache_keys(r, keys, key_cap, sh, cached);
+      written = select_ascending(r, want, out, sh, scratch, &st);
     }
-    written = select_ascending(r, want, out, sh, scratch);
     if (blocks) {                      // the pinned last visible block
       if (tid == 0) out[written] = (r.V + kBlock - 1) / kBlock - 1;
       written += 1;
@@ -619,12 +765,14 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
   cudaError_t e;
   if (d.lchunks > 0) {
-    e = cudaMemsetAsync(d.lext, 0, d.long_zero_bytes, s);
-    if (e != cudaSuccess) return e;
     const dim3 g(static_cast<unsigned>(d.lchunks), static_cast<unsigned>(d.T),
                  d.mode == QLI_CAND_SOURCE ? 2u : 1u);
-    lstat_kernel<<<g, kThreads, 0, s>>>(d);
-    lhist_kernel<<<g, kThreads, 0, s>>>(d);
+    if (d.fhist == nullptr) {   // no score-stage histogram: build the statistics here
+      e = cudaMemsetAsync(d.lext, 0, d.long_zero_bytes, s);
+      if (e != cudaSuccess) return e;
+      lstat_kernel<<<g, kThreads, 0, s>>>(d);
+      lhist_kernel<<<g, kThreads, 0, s>>>(d);
+    }
     lcompact_kernel<<<g, kThreads, 0, s>>>(d);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -633,16 +781,20 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   const int32_t cap = static_cast<int32_t>(longest < kSmemKeys ? longest : kSmemKeys);
   // candidate rows need room for kLongCandCap keys and ids
   const int32_t region = d.lchunks > 0 ? (cap > 2 * kLongCandCap ? cap : 2 * kLongCandCap) : cap;
-  const int smem = 4 * (region + kSampleKeys + kCandCap);
+  const int smem = 4 * (region + kHeadWords + kCandCap);
   static std::atomic<uint64_t> done{0};
   e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel),
-                        4 * (kSmemKeys + kSampleKeys + kCandCap), done);
+                        4 * (kSmemKeys + kHeadWords + kCandCap), done);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(d.T), d.mode == QLI_CAND_SOURCE ? 2u : 1u);
   select_kernel<<<grid, kThreads, smem, s>>>(d, cap, region);
   return cudaGetLastError();
 }
 
-int select_launches(const DevArgs& d) { return d.T > 0 ? (d.lchunks > 0 ? 4 : 1) : 0; }
+int select_launches(const DevArgs& d) {
+  if (d.T == 0) return 0;
+  if (d.lchunks == 0) return 1;
+  return d.fhist != nullptr ? 2 : 4;
+}
 
 }  // namespace qli
