@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -105,6 +106,25 @@ bool use_stream_path(const qli_args& a);
 // Raises `func`'s dynamic shared-memory limit to `bytes` once per device
 // (`done` holds one bit per device ordinal below 64; others always set it).
 cudaError_t ensure_smem_limit(const void* func, int bytes, std::atomic<uint64_t>& done);
+
+// Launches `kernel` with programmatic stream serialisation: it may begin
+// while the previous kernel on the stream finishes, and must call pdl_wait()
+// before reading that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 WsLayout workspace_layout(const qli_args& a);
 DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L);

@@ -62,10 +62,24 @@ __device__ void cta_scan_store(int32_t n, F f, int32_t* out) {
   if (tid == 0) out[n] = carry;
 }
 
-// One CTA. Sanitises the metadata (clamping it so no later kernel can leave
+constexpr int kZeroChunk = 64 * 1024;
+
+// Block 0 sanitises the metadata (clamping it so no later kernel can leave
 // its buffers, and flagging what was clamped), then writes V(t), the request
-// of every token and the token groups that share one score tile.
+// of every token and the token groups that share one score tile. Blocks 1..
+// zero the score stage's selection histograms (16 KB per row) in 64 KB
+// chunks.
+
 __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
+  pdl_trigger();
+  if (blockIdx.x > 0) {
+    const size_t bytes = sizeof(uint32_t) * kHistBins * 2 * static_cast<size_t>(a.T);
+    const size_t lo = static_cast<size_t>(blockIdx.x - 1) * kZeroChunk;
+    uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.fhist) + lo);
+    const size_t n = (min(bytes, lo + kZeroChunk) - lo) / sizeof(uint4);
+    for (size_t i = threadIdx.x; i < n; i += blockDim.x) p[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
   const int tid = threadIdx.x;
   __shared__ uint32_t s_err;
   if (tid == 0) s_err = 0u;
@@ -228,7 +242,10 @@ __global__ void __launch_bounds__(kPrepThreads) cand_prep_kernel(DevArgs a, int3
 }  // namespace
 
 cudaError_t launch_plan(const DevArgs& d, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(d);
+  const size_t hist_bytes =
+      d.fhist ? sizeof(uint32_t) * kHistBins * 2 * static_cast<size_t>(d.T) : 0;
+  const unsigned zero_blocks = static_cast<unsigned>((hist_bytes + kZeroChunk - 1) / kZeroChunk);
+  plan_kernel<<<1 + zero_blocks, 1024, 0, s>>>(d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (d.mode == QLI_CAND_CONSUMER && d.T > 0) {

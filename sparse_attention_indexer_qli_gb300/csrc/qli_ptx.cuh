@@ -102,6 +102,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// ---- programmatic dependent launch -----------------------------------------
+// A kernel launched with programmatic stream serialisation may start before
+// its predecessor finishes; pdl_wait() blocks until the predecessor grid has
+// completed and its writes are visible (a no-op for a normal launch), so it
+// must precede every read of the predecessor's outputs. pdl_trigger() lets
+// the next kernel in the stream begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- proxy / tcgen05 fences ---------------------------------------------
 // Makes generic-proxy writes to shared memory visible to the async proxy
 // (the tensor core reads its operands through it).

@@ -334,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
   Smem& S = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();   // the plan's outputs (and zeroed histograms) are ready
   const int32_t U = a.unit_start[a.T];
   const int32_t u0 = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
   const int32_t u1 = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
@@ -675,12 +677,11 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
     CUtensorMap tm_page, tm_blk;
     if (!encode_k_map(d, d.R, &tm_page) || !encode_k_map(d, kBlock, &tm_blk))
       return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(d.fhist, 0, sizeof(uint32_t) * kHistBins * 2 * static_cast<size_t>(d.T), s);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream::stream_kernel), stream::kSmemBytes, g_smem_stream_stream_kernel);
     if (e != cudaSuccess) return e;
-    e = ensure_smem_limit(reinterpret_cast<const void*>(stream::stream_kernel), stream::kSmemBytes, g_smem_stream_stream_kernel);
-    if (e != cudaSuccess) return e;
-    stream::stream_kernel<<<d.num_sms, stream::kThreads, stream::kSmemBytes, s>>>(tm_page, tm_blk, d);
-    return cudaGetLastError();
+    e = launch_pdl(stream::stream_kernel, dim3(d.num_sms), dim3(stream::kThreads),
+                   stream::kSmemBytes, s, tm_page, tm_blk, d);
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
   if (d.use_prefill_kernel) return launch_prefill(d, s);
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_tile_kernel), kSmemBytes, g_smem_score_tile_kernel);

@@ -496,6 +496,8 @@ __global__ void __launch_bounds__(kThreads) lhist_kernel(DevArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int warp_cnt[kWarps];
   __shared__ uint32_t s_digit;
   Row r;
@@ -696,6 +698,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
                                                           int32_t region) {
   extern __shared__ uint32_t keys[];
   uint32_t* scratch = keys + region;
+  pdl_wait();
   __shared__ Shared sh;
   const int t = blockIdx.x, which = blockIdx.y, tid = threadIdx.x;
   const bool blocks = which == 1;
@@ -773,7 +776,12 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
       lstat_kernel<<<g, kThreads, 0, s>>>(d);
       lhist_kernel<<<g, kThreads, 0, s>>>(d);
     }
-    lcompact_kernel<<<g, kThreads, 0, s>>>(d);
+    if (d.fhist != nullptr) {
+      e = launch_pdl(lcompact_kernel, g, dim3(kThreads), 0, s, d);
+      if (e != cudaSuccess) return e;
+    } else {
+      lcompact_kernel<<<g, kThreads, 0, s>>>(d);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -787,8 +795,8 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
                         4 * (kSmemKeys + kHeadWords + kCandCap), done);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(d.T), d.mode == QLI_CAND_SOURCE ? 2u : 1u);
-  select_kernel<<<grid, kThreads, smem, s>>>(d, cap, region);
-  return cudaGetLastError();
+  e = launch_pdl(select_kernel, grid, dim3(kThreads), static_cast<size_t>(smem), s, d, cap, region);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int select_launches(const DevArgs& d) {

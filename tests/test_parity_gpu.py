@@ -175,6 +175,46 @@ def test_repeat_calls_reuse_workspace():
     assert torch.equal(a, b) and torch.equal(ca, cb)
 
 
+@pytest.mark.parametrize("mode", ["none", "source", "consumer"])
+def test_stages_and_graph_replay_equal_one_call(mode):
+    """PLAN, SCORE and SELECT queued one by one, and a CUDA graph of the whole
+    call (whose kernels start early and wait on their predecessors on the
+    device), give what one plain call gives, over a dirty workspace."""
+    import torch
+    case = synth.make_case(31, [100000, 2500, 9000], [1, 2, 1], N=64, ratio=2, topk=512,
+                           cand_mode=mode, cand_blocks=256 if mode != "none" else 0,
+                           cand_policy="messy" if mode == "consumer" else "valid")
+    call = qli.Call(**synth.upload(case, "cuda"))
+    ws = call.alloc_workspace()
+    idx, cand = call.run(ws)
+    torch.cuda.synchronize()
+    want = (idx.clone(), None if cand is None else cand.clone())
+
+    def same():
+        torch.cuda.synchronize()
+        assert torch.equal(call.indices, want[0])
+        if want[1] is not None:
+            assert torch.equal(call.cand, want[1])
+
+    for rep in range(2):                       # the second pass starts from a used workspace
+        call.indices.fill_(-7)
+        for stage in (qli.STAGE_PLAN, qli.STAGE_SCORE, qli.STAGE_SELECT):
+            call.run_stage(stage, ws)
+        same()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            call.run(ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for rep in range(3):
+        call.indices.fill_(-7)
+        g.replay()
+        same()
+    assert call.device_error(ws) == 0
+
+
 def test_parity_long_rows():
     """Rows longer than one CTA's shared memory take the multi-CTA selection
     (statistics, histogram, compaction, exact ranking of the candidates)."""
