@@ -182,3 +182,55 @@ def head_term(s: int, w_bits: int, qs_bits: int) -> float:
 
 def pair_score(prep: Prepared, t: int, j: int) -> float:
     return float(lib().oracle_pair_score(ctypes.byref(prep.s), int(t), int(j)))
+
+
+# ---- query quantiser and index-K writer (qli_quant_oracle.c) ---------------
+
+QUANT_ERRORS = {-1: "invalid argument", -2: "non-finite input", -5: "slot out of range"}
+
+
+def _quant_fn(name, restype, argtypes):
+    f = getattr(lib(), name)
+    f.restype = restype
+    f.argtypes = argtypes
+    return f
+
+
+def bf16_bits_to_f32(b: int) -> float:
+    return float(_quant_fn("oracle_bf16_to_f32", ctypes.c_float, [ctypes.c_uint16])(int(b)))
+
+
+def quantize_rows(x_bf16: np.ndarray):
+    """Per-row INT8 quantisation of BF16 rows (given as uint16 bit patterns,
+    shape [..., D]). Returns (codes int8 [..., D], scales uint16 [...] FP16 bits)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    D = x.shape[-1]
+    rows = x.size // D if D else 0
+    q = np.empty(x.shape, dtype=np.int8)
+    s = np.empty(x.shape[:-1], dtype=np.uint16)
+    f = _quant_fn("oracle_quantize_rows", ctypes.c_int,
+                  [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p])
+    rc = f(_ptr(x), rows, D, _ptr(q), _ptr(s))
+    if rc != 0:
+        raise OracleError(QUANT_ERRORS.get(rc, str(rc)))
+    return q, s
+
+
+def write_index_k(k_bf16: np.ndarray, slot: np.ndarray, pages: np.ndarray, rows_per_page: int,
+                  k_offset: int, scale_offset: int) -> int:
+    """Quantises the n rows of k_bf16 ([n, D] uint16 BF16 bits) and writes
+    them into `pages` ([num_pages, page_stride] uint8, modified in place) at
+    slot[i] = page * R + row. Returns the oracle's status (0, or -5 when a
+    slot lies past the pool; valid rows are written either way)."""
+    k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
+    sl = np.ascontiguousarray(slot, dtype=np.int64)
+    assert pages.flags.c_contiguous and pages.dtype == np.uint8 and pages.ndim == 2
+    f = _quant_fn("oracle_write_index_k", ctypes.c_int,
+                  [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                   ctypes.c_int64, ctypes.c_int64])
+    rc = f(_ptr(k), k.shape[0], k.shape[1], _ptr(sl), _ptr(pages), pages.shape[0],
+           pages.shape[1], rows_per_page, k_offset, scale_offset)
+    if rc not in (0, -5):
+        raise OracleError(QUANT_ERRORS.get(rc, str(rc)))
+    return int(rc)

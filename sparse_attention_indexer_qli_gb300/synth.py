@@ -178,6 +178,21 @@ class Case:
         return self.k_scale[self.k_row_start[b]:self.k_row_start[b + 1]]
 
 
+def bf16_rows(seed: int, shape, sigma: float = 1.0, stream: int = 40) -> np.ndarray:
+    """Seeded BF16 activations (uint16 bit patterns): N(0, sigma) values cut
+    to BF16 by dropping the low 16 bits of their FP32 patterns."""
+    x = (_rng(seed, stream).standard_normal(size=shape) * sigma).astype(np.float32)
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def slots_of(case: "Case", b: int, positions: np.ndarray) -> np.ndarray:
+    """Page slots (page * R + row) of request b's compressed positions under
+    the case's block table: the slot mapping a cache writer is given."""
+    R = case.rows_per_page
+    pos = np.asarray(positions, dtype=np.int64)
+    return case.block_table[b, pos // R].astype(np.int64) * R + pos % R
+
+
 def make_case(seed: int, raw_lens: Sequence[int], q_lens: Sequence[int], N: int,
               ratio: int, topk: int, cand_mode: str = "none", cand_blocks: int = 0,
               rows_per_page: Optional[int] = None, page_stride: Optional[int] = None,

@@ -1,5 +1,5 @@
 """Mutation check of the oracle's pins: each mutant plants one plausible
-mistake in a copy of oracle/qli_oracle.c (built on the CPU into a temporary
+mistake in a copy of oracle/qli_oracle.c (or oracle/qli_quant_oracle.c) (built on the CPU into a temporary
 directory, never touching the real oracle); the pin suite must fail on every
 one of them. This shows the pins constrain each step of the definition."""
 import os
@@ -54,5 +54,42 @@ def test_pins_kill_mutant(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
+
+
+# ---- the query quantiser and index-K writer (qli_quant_oracle.c) -----------
+
+QSRC = os.path.join(ROOT, "oracle", "qli_quant_oracle.c")
+
+QUANT_MUTANTS = {
+    "divisor-128": ("const float quotient = amax / 127.0f;", "const float quotient = amax / 128.0f;"),
+    "scale-not-fp16": ("const float sf = (float)s;", "const float sf = quotient;"),
+    "floor-not-round": ("float r = rintf(oracle_bf16_to_f32(x[d]) / sf);",
+                        "float r = floorf(oracle_bf16_to_f32(x[d]) / sf);"),
+    "clamp-at-128": ("if (r < -127.0f) r = -127.0f;", "if (r < -128.0f) r = -128.0f;"),
+    "no-saturation": ("if (isinf((float)s)) s = (_Float16)65504.0f;", ";"),
+    "amax-signed": ("const float a = fabsf(v);", "const float a = v;"),
+    "row-from-slot-div": ("const int64_t page = m / R, row = m % R;",
+                          "const int64_t page = m % R, row = m / R;"),
+    "scale-stride-1": ("memcpy(p + scale_offset + row * 2, &s, 2);",
+                       "memcpy(p + scale_offset + row, &s, 2);"),
+    "padding-written": ("const int64_t m = slot[i];", "const int64_t m = slot[i] < 0 ? 0 : slot[i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(QUANT_MUTANTS))
+def test_quant_pins_kill_mutant(name, tmp_path):
+    src = open(QSRC).read()
+    old, new = QUANT_MUTANTS[name]
+    assert src.count(old) == 1, "mutation anchor not found: %s" % name
+    mut = tmp_path / "qli_quant_oracle_mut.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libqmut.so"
+    subprocess.run(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
+                    "-ffp-contract=off", SRC, str(mut), "-o", str(lib), "-lm"], check=True)
+    env = dict(os.environ, ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_quant_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "mutant %s survived the pins:\n%s" % (name, r.stdout[-2000:])
