@@ -63,6 +63,8 @@ __device__ void cta_scan_store(int32_t n, F f, int32_t* out) {
 }
 
 constexpr int kZeroChunk = 64 * 1024;
+constexpr int kPlanReqCache = 1024;   // requests whose metadata block 0 keeps in shared memory
+constexpr int kPlanTokCache = 4096;   // tokens whose tile counts block 0 keeps in shared memory
 
 // Block 0 sanitises the metadata (clamping it so no later kernel can leave
 // its buffers, and flagging what was clamped), then writes V(t), the request
@@ -82,12 +84,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   }
   const int tid = threadIdx.x;
   __shared__ uint32_t s_err;
+  // requests' sanitised metadata and tokens' tile counts stay in shared
+  // memory when they fit (the global copies are written either way)
+  __shared__ int32_t s_q0[kPlanReqCache], s_q1[kPlanReqCache], s_lk[kPlanReqCache],
+      s_res[kPlanReqCache];
+  __shared__ int32_t s_tiles[kPlanTokCache];
+  const bool req_small = a.B <= kPlanReqCache;
+  const bool dense_stream = a.stream_path && a.mode != QLI_CAND_CONSUMER;
+  const bool tok_small = dense_stream && a.T <= kPlanTokCache;
   if (tid == 0) s_err = 0u;
-  for (int t = tid; t < a.T; t += blockDim.x) {
-    a.tok_V[t] = 0;
-    a.tok_b[t] = -1;
-  }
-  for (int g = tid; g < a.Gmax; g += blockDim.x) a.grp_cnt[g] = 0;
+  if (!a.stream_path)
+    for (int g = tid; g < a.Gmax; g += blockDim.x) a.grp_cnt[g] = 0;
   __syncthreads();
 
   // every request on its own: clamp the query range into [0, T], the
@@ -95,16 +102,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   uint32_t e = 0u;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const int32_t c0 = a.cu[b], c1 = a.cu[b + 1];
+    int32_t lk = a.k_lens[b];
+    int32_t res = a.residual ? a.residual[b] : 0;
     const int32_t q0 = min(max(c0, 0), a.T);
     const int32_t q1 = min(max(c1, q0), a.T);
     if (c0 != q0 || c1 != q1 || (b == 0 && c0 != 0) || (b == a.B - 1 && c1 != a.T))
       e |= QLI_DEVERR_SEQLENS;
-    int32_t lk = a.k_lens[b];
     if (lk < 0 || lk > a.cap) {
       e |= QLI_DEVERR_KLEN;
       lk = lk < 0 ? 0 : static_cast<int32_t>(a.cap);
     }
-    int32_t res = a.residual ? a.residual[b] : 0;
     if (res < 0 || res >= a.ratio) {
       e |= QLI_DEVERR_RESIDUAL;
       res = 0;
@@ -113,44 +120,71 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
     a.req_q1[b] = q1;
     a.req_lk[b] = lk;
     a.req_res[b] = res;
+    if (req_small) {
+      s_q0[b] = q0;
+      s_q1[b] = q1;
+      s_lk[b] = lk;
+      s_res[b] = res;
+    }
   }
   if (e) atomicOr(&s_err, e);
   __syncthreads();
-  // first token group of every request (groups never span two requests)
-  cta_scan_store<1024>(a.B, [&](int32_t b) { return (a.req_q1[b] - a.req_q0[b] + a.G - 1) / a.G; },
-                       a.req_g0);
+  const int32_t* q0s = req_small ? s_q0 : a.req_q0;
+  const int32_t* q1s = req_small ? s_q1 : a.req_q1;
+  const int32_t* lks = req_small ? s_lk : a.req_lk;
+  const int32_t* ress = req_small ? s_res : a.req_res;
+  if (!a.stream_path) {
+    // first token group of every request (groups never span two requests)
+    cta_scan_store<1024>(a.B, [&](int32_t b) { return (q1s[b] - q0s[b] + a.G - 1) / a.G; },
+                         a.req_g0);
+  }
   if (tid == 0) {
     *a.err = s_err;   // first writer of this call: resets the word
     *a.counter = 0u;
   }
-  __syncthreads();
 
-  // one warp per request, lanes over its tokens and groups
-  const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  for (int b = warp; b < a.B; b += nwarps) {
-    const int32_t q0 = a.req_q0[b], q1 = a.req_q1[b], lk = a.req_lk[b], res = a.req_res[b];
-    const int32_t qlen = q1 - q0;
-    for (int i = lane; i < qlen; i += 32) {
-      a.tok_V[q0 + i] = visible_count(lk, res, a.ratio, qlen, i);
-      a.tok_b[q0 + i] = b;
+  // every token: its request is the last one starting at or before it (the
+  // sanitised starts never decrease for valid metadata; a token no request
+  // covers keeps V = 0 and request -1)
+  for (int t = tid; t < a.T; t += blockDim.x) {
+    int32_t lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (q0s[mid] <= t) lo = mid; else hi = mid - 1;
     }
-    const int32_t ng = (qlen + a.G - 1) / a.G;
-    for (int gi = lane; gi < ng; gi += 32) {
-      const int32_t g = a.req_g0[b] + gi;
-      if (g < a.Gmax) {
-        a.grp_t0[g] = q0 + gi * a.G;
-        a.grp_cnt[g] = min(a.G, qlen - gi * a.G);
-      }
+    int32_t V = 0, owner = -1;
+    if (a.B > 0 && q0s[lo] <= t && t < q1s[lo]) {
+      owner = lo;
+      V = visible_count(lks[lo], ress[lo], a.ratio, q1s[lo] - q0s[lo], t - q0s[lo]);
     }
+    a.tok_V[t] = V;
+    a.tok_b[t] = owner;
+    if (tok_small) s_tiles[t] = (V + kTile - 1) / kTile;
   }
   __syncthreads();
-  if (a.stream_path && a.mode != QLI_CAND_CONSUMER) {
+
+  if (dense_stream) {
     // stream path, dense modes: token t owns ceil(V(t)/128) score tiles
-    cta_scan_store<1024>(a.T, [&](int32_t t) { return (a.tok_V[t] + kTile - 1) / kTile; },
-                         a.unit_start);
+    cta_scan_store<1024>(
+        a.T, [&](int32_t t) { return tok_small ? s_tiles[t] : (a.tok_V[t] + kTile - 1) / kTile; },
+        a.unit_start);
   } else if (!a.stream_path) {
-    // group path: group g owns ceil(tiles/64) units of up to 64 tiles, where
-    // its last (most advanced) token sees ceil(V/128) tiles
+    // group path: one warp per request, lanes over its groups
+    const int warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    for (int b = warp; b < a.B; b += nwarps) {
+      const int32_t q0 = q0s[b], qlen = q1s[b] - q0;
+      const int32_t ng = (qlen + a.G - 1) / a.G;
+      for (int gi = lane; gi < ng; gi += 32) {
+        const int32_t g = a.req_g0[b] + gi;
+        if (g < a.Gmax) {
+          a.grp_t0[g] = q0 + gi * a.G;
+          a.grp_cnt[g] = min(a.G, qlen - gi * a.G);
+        }
+      }
+    }
+    __syncthreads();
+    // group g owns ceil(tiles/64) units of up to 64 tiles, where its last
+    // (most advanced) token sees ceil(V/128) tiles
     cta_scan_store<1024>(
         a.Gmax,
         [&](int32_t g) {

@@ -102,6 +102,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// Pulls a kernel-parameter tensor map into the descriptor cache ahead of its
+// first TMA use.
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 // ---- programmatic dependent launch -----------------------------------------
 // A kernel launched with programmatic stream serialisation may start before
 // its predecessor finishes; pdl_wait() blocks until the predecessor grid has

@@ -335,14 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
-  pdl_wait();   // the plan's outputs (and zeroed histograms) are ready
-  const int32_t U = a.unit_start[a.T];
-  const int32_t u0 = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
-  const int32_t u1 = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
-  if (u0 >= u1) return;
-  const int32_t nk = u1 - u0;
-  const bool consumer = a.mode == QLI_CAND_CONSUMER;
-
+  // setup that reads nothing the plan writes runs while the plan finishes
+  if (tid == 0) {
+    prefetch_tensormap(&tm_page);
+    prefetch_tensormap(&tm_blk);
+  }
   if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
   if (tid == 32) {
     for (int s = 0; s < kKStages; ++s) {
@@ -360,6 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  pdl_wait();   // the plan's outputs (and zeroed histograms) are ready
+  const int32_t U = a.unit_start[a.T];
+  const int32_t u0 = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
+  const int32_t u1 = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
+  if (u0 >= u1) {
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+  const int32_t nk = u1 - u0;
+  const bool consumer = a.mode == QLI_CAND_CONSUMER;
   bool ok = true;
 
   if (warp == 0) {

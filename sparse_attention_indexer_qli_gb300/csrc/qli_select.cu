@@ -33,8 +33,9 @@ constexpr int kCandCap = 8192;         // candidates the sample / histogram path
 struct Shared {
   uint32_t hist[256];
   int warp_a[kWarps], warp_b[kWarps];
+  int chunk_w[2][kWarps];
   uint32_t red[kWarps][3];
-  uint32_t sel[2];
+  uint32_t sel[3];
 };
 
 // A row of the selection: entry s has a key (0 = not eligible) and an id.
@@ -299,58 +300,194 @@ __device__ int compact_at_least(const Row& r, uint32_t t_lo, int32_t* idx, int c
   return total;
 }
 
-// Threshold from a row's 4096-bin histogram of the top 12 key bits (built by
-// the score stage): copies it to `hs`, drops one count from bin `pinned`
-// (the pinned last block, which the block row does not rank; -1: none), and
-// returns the lowest key of the bin holding the want-th best entry — or 1
-// (every eligible key) when the row has no more than `want` entries. E is
-// the row's eligible count.
-__device__ uint32_t hist_threshold(const uint32_t* g, int32_t pinned, int32_t want, uint32_t* hs,
-                                   Shared& sh, uint32_t& E) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kHistBins; i += kThreads) hs[i] = g[i];
-  __syncthreads();
-  if (tid == 0 && pinned >= 0) hs[pinned] -= 1u;
-  __syncthreads();
-  // thread i owns bins 4095-4i .. 4092-4i (top down)
-  uint32_t c[4], mine = 0u;
+// Block-wide inclusive scan of one value per thread (thread order); returns
+// the thread's inclusive sum and the block total. Two barriers.
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t& total, Shared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    c[j] = hs[kHistBins - 1 - 4 * tid - j];
-    mine += c[j];
-  }
-  uint32_t incl = mine;
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
+  __syncthreads();                       // the previous scan's readers are done
   if (lane == 31) sh.warp_a[warp] = static_cast<int>(incl);
-  if (tid == 0) sh.sel[0] = 0u;
   __syncthreads();
-  uint32_t base = 0u, total = 0u;
-  for (int w = 0; w < kWarps; ++w) {
-    base += w < warp ? static_cast<uint32_t>(sh.warp_a[w]) : 0u;
-    total += static_cast<uint32_t>(sh.warp_a[w]);
-  }
-  E = total;
-  const uint32_t k = static_cast<uint32_t>(want);
-  if (total > k) {
-    uint32_t above = base + incl - mine;
-    if (above < k && k <= above + mine) {
+  uint32_t w = static_cast<uint32_t>(sh.warp_a[lane]), wincl = w;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (above + c[j] >= k) {
-          sh.sel[0] = static_cast<uint32_t>(kHistBins - 1 - 4 * tid - j);
-          break;
-        }
-        above += c[j];
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  total = __shfl_sync(0xffffffffu, wincl, 31);
+  return incl + __shfl_sync(0xffffffffu, wincl - w, warp);
+}
+
+// Where the want-th best entry of a row sits in its 4096-bin histogram of
+// the top 12 key bits (built by the score stage): bin `sel`, `above` entries
+// in higher bins, `cbin` in bin sel itself; E = the row's eligible count.
+// `pinned` (-1: none) is the bin of the pinned last block, which the block
+// row does not rank. Thread i holds bins 4095-4i .. 4092-4i (one 16-byte
+// load).
+struct HistSel {
+  uint32_t sel, above, cbin, E;
+};
+static_assert(kHistBins == 4 * kThreads, "one 16-byte histogram load per thread");
+
+__device__ HistSel hist_select(const uint32_t* g, int32_t pinned, int32_t want, Shared& sh) {
+  const int tid = threadIdx.x;
+  const int q = kHistBins / 4 - 1 - tid;
+  const uint4 v = __ldcg(reinterpret_cast<const uint4*>(g) + q);
+  uint32_t c[4] = {v.w, v.z, v.y, v.x};                     // bins 4q+3 .. 4q
+  if (pinned >= 0 && (pinned >> 2) == q) c[3 - (pinned & 3)] -= 1u;
+  const uint32_t mine = c[0] + c[1] + c[2] + c[3];
+  uint32_t E;
+  const uint32_t incl = block_scan(mine, E, sh);
+  const uint32_t k = static_cast<uint32_t>(want);
+  uint32_t above = incl - mine;
+  if (E > k && above < k && k <= incl) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (above + c[j] >= k) {
+        sh.sel[0] = static_cast<uint32_t>(4 * q + 3 - j);
+        sh.sel[1] = above;
+        sh.sel[2] = c[j];
+        break;
       }
+      above += c[j];
     }
   }
   __syncthreads();
-  const uint32_t t_lo = total > k ? (sh.sel[0] << (32 - kHistBits)) : 1u;
+  HistSel h{sh.sel[0], sh.sel[1], sh.sel[2], E};
   __syncthreads();
-  return t_lo == 0u ? 1u : t_lo;
+  return h;
+}
+
+// One pass over a row in global memory keeping, in row order, every entry
+// whose key is at least t_lo: its key to ckeys[] and its id (position) to
+// cid[]; returns how many (written only while below cap). Chunks of 4096
+// entries, thread i taking entries 4i..4i+3 of a chunk with one 16-byte
+// load; the loads of up to kBatch chunks are issued before the first is
+// used. One barrier per chunk.
+template <bool kConsumer>
+__device__ int compact_from_row(const Row& r, uint32_t t_lo, uint32_t* ckeys, int32_t* cid,
+                                int cap, Shared& sh) {
+  constexpr int kBatch = 6;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned below = (1u << lane) - 1u;
+  const int32_t nchunks = (r.len + 4 * kThreads - 1) / (4 * kThreads);
+  const float4* v4 = reinterpret_cast<const float4*>(r.vals);
+  int base = 0;
+  for (int32_t c0 = 0; c0 < nchunks; c0 += kBatch) {
+    float4 f[kBatch];
+    int32_t blk[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int32_t s0 = (c0 + u) * 4 * kThreads + 4 * tid;
+      f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      blk[u] = 0;
+      if (s0 < r.len) {
+        f[u] = __ldcg(v4 + (s0 >> 2));
+        if (kConsumer) blk[u] = __ldcg(r.blocks + (s0 >> 3));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (c0 + u >= nchunks) break;                         // block-uniform
+      const int32_t s0 = (c0 + u) * 4 * kThreads + 4 * tid;
+      const int32_t id0 = kConsumer ? blk[u] * kBlock + (s0 & (kBlock - 1)) : s0;
+      const uint32_t k[4] = {order_key(f[u].x), order_key(f[u].y), order_key(f[u].z),
+                             order_key(f[u].w)};
+      unsigned keep = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = s0 + j < r.len && (!kConsumer || id0 + j < r.V) && k[j] >= t_lo;
+        keep |= ok ? (1u << j) : 0u;
+      }
+      const int cnt = __popc(keep);
+      const unsigned b0 = __ballot_sync(0xffffffffu, cnt & 1), b1 = __ballot_sync(0xffffffffu, cnt & 2),
+                     b2 = __ballot_sync(0xffffffffu, cnt & 4);
+      const int pre = __popc(b0 & below) + 2 * __popc(b1 & below) + 4 * __popc(b2 & below);
+      const int wsum = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+      const int par = (c0 + u) & 1;                         // two buffers: one barrier per chunk
+      if (lane == 0) sh.chunk_w[par][warp] = wsum;
+      __syncthreads();
+      const int w = sh.chunk_w[par][lane];
+      int wincl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += y;
+      }
+      int at = base + __shfl_sync(0xffffffffu, wincl - w, warp) + pre;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if ((keep >> j) & 1u) {
+          if (at < cap) {
+            ckeys[at] = k[j];
+            cid[at] = id0 + j;
+          }
+          ++at;
+        }
+      }
+      base += __shfl_sync(0xffffffffu, wincl, 31);
+    }
+  }
+  __syncthreads();
+  return base;
+}
+
+// Exact threshold among n candidate keys (any order) whose top 12 bits
+// already single out bin `sel`: the k-th largest key of that bin (k >= 1),
+// in the convention of ordered_output (take keys > thr and the first
+// need_eq keys == thr). 10-bit digits on the remaining 20 bits, histogram
+// in `hist` (1024 words of shared memory); stops as soon as the chosen
+// digit's entries are exactly the ones still needed.
+__device__ void refine_threshold(const uint32_t* ckeys, int n, uint32_t sel, int32_t k,
+                                 uint32_t* hist, Shared& sh, uint32_t& thr, int32_t& need_eq) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t prefix = sel << (32 - kHistBits), mask = ~0u << (32 - kHistBits);
+  int hi = 31 - kHistBits;
+  while (hi >= 0) {
+    const int width = hi + 1 < 10 ? hi + 1 : 10;
+    const int shift = hi + 1 - width;
+    const int nb = 1 << width;
+    hist[tid] = 0u;
+    __syncthreads();
+    for (int b = 0; b < n; b += kThreads) {
+      const int s = b + tid;
+      const uint32_t key = s < n ? ckeys[s] : 0u;
+      const bool live = s < n && (key & mask) == prefix;
+      const uint32_t d = live ? (key >> shift) & static_cast<uint32_t>(nb - 1) : 0xffffffffu;
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      if (live && (__ffs(peers) - 1) == lane) atomicAdd(&hist[d], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    // thread i holds digit nb-1-i (top down)
+    const uint32_t c = tid < nb ? hist[nb - 1 - tid] : 0u;
+    uint32_t total;
+    const uint32_t incl = block_scan(c, total, sh);
+    if (tid < nb && incl - c < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= incl) {
+      sh.sel[0] = static_cast<uint32_t>(nb - 1 - tid);
+      sh.sel[1] = static_cast<uint32_t>(k) - (incl - c);
+      sh.sel[2] = c;
+    }
+    __syncthreads();
+    prefix |= sh.sel[0] << shift;
+    mask |= static_cast<uint32_t>(nb - 1) << shift;
+    k = static_cast<int32_t>(sh.sel[1]);
+    const uint32_t in_digit = sh.sel[2];
+    __syncthreads();
+    if (in_digit == static_cast<uint32_t>(k)) {
+      // every key of this digit is needed: take all keys >= its lowest key
+      thr = prefix == 0u ? 0u : prefix - 1u;
+      need_eq = 0;
+      return;
+    }
+    hi = shift - 1;
+  }
+  thr = prefix;
+  need_eq = k;
 }
 
 // Writes the ids of the `want` best entries of `r` in ascending id order to
@@ -728,26 +865,40 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
         pinned = static_cast<int32_t>(
             hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
       }
-      uint32_t E;
-      const uint32_t t_lo = hist_threshold(
-          a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins, pinned, want, scratch, sh, E);
-      bool cached;
-      const Stats st = cache_keys(r, keys, key_cap, sh, cached);
-      int32_t* cand = reinterpret_cast<int32_t*>(scratch + kHeadWords);
-      const int n = st.E <= static_cast<uint32_t>(want) ? 0 : compact_at_least(r, t_lo, cand, kCandCap, sh);
-      if (st.E <= static_cast<uint32_t>(want)) {
-        written = ordered_output(r, 0u, 0, out, sh);
-      } else if (n >= want && n <= kCandCap) {
-        Row cr = r;
-        cr.idx = cand;
-        cr.len = n;
-        const Stats cs = row_stats(cr, sh);
-        uint32_t thr;
-        int32_t need_eq;
-        radix_threshold(cr, want, cs, thr, need_eq, sh);
-        written = ordered_output(cr, thr, need_eq, out, sh);
-      } else {
-        written = select_ascending(r, want, out, sh, nullptr, &st);
+      const HistSel hs = hist_select(a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins,
+                                     pinned, want, sh);
+      // candidates: keys to the key region, ids to the scratch head, then
+      // 1024 words of digit histogram
+      const int cap = min(region, kHeadWords + kCandCap - 1024);
+      const uint32_t n = hs.above + hs.cbin;
+      bool done = false;
+      if (hs.E <= static_cast<uint32_t>(want)) {
+        written = ordered_output(r, 0u, 0, out, sh);        // every eligible entry, in order
+        done = true;
+      } else if (n <= static_cast<uint32_t>(cap)) {
+        int32_t* cid = reinterpret_cast<int32_t*>(scratch);
+        const uint32_t t_lo = hs.sel << (32 - kHistBits);
+        const int got = r.consumer ? compact_from_row<true>(r, t_lo, keys, cid, cap, sh)
+                                   : compact_from_row<false>(r, t_lo, keys, cid, cap, sh);
+        if (got == static_cast<int>(n)) {
+          uint32_t thr;
+          int32_t need_eq;
+          refine_threshold(keys, got, hs.sel, want - static_cast<int32_t>(hs.above),
+                           scratch + kHeadWords + kCandCap - 1024, sh, thr, need_eq);
+          Row cr = r;
+          cr.cached = keys;
+          cr.ids = cid;
+          cr.idx = nullptr;
+          cr.len = got;
+          cr.consumer = false;
+          written = ordered_output(cr, thr, need_eq, out, sh);
+          done = true;
+        }
+      }
+      if (!done) {                      // a bin too full for the candidate space
+        bool cached;
+        const Stats st = cache_keys(r, keys, key_cap, sh, cached);
+        written = select_ascending(r, want, out, sh, scratch, &st);
       }
     } else {
       bool cached;
