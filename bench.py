@@ -500,6 +500,152 @@ def run_e2e(args, sets, workspace, stream, world):
             "h2d_bytes_per_step": h2d // args.steps, "d2h_bytes_per_step": d2h // args.steps}
 
 
+# ------------------------------------------------ query quantiser / K writer
+
+OP_ROWS = {"quantize_q": 4096 * 64, "write_index_k": 2 * 32768}
+
+
+def op_inputs(op: str, seed: int, case=None):
+    """Host inputs of one step of the quantiser / writer workloads: the
+    prefill workload's 4096 query tokens x 64 heads, or the index-K rows of
+    its two 65536-token requests (ratio 2, 32768 compressed rows each) with
+    their slots under `case`'s block table."""
+    if op == "quantize_q":
+        return {"x": synth.bf16_rows(seed, (4096, 64, 128), sigma=1.0)}
+    slots = np.concatenate([synth.slots_of(case, b, np.arange(int(case.k_lens[b])))
+                            for b in range(case.B)])
+    return {"x": synth.bf16_rows(seed, (slots.size, 128), sigma=2.0), "slots": slots,
+            "case": case}
+
+
+def op_bytes(op: str, rows: int) -> int:
+    """Algorithmic bytes: 256 B of BF16 read and 128 + 2 B written per row,
+    plus the 8-byte slot of each written index-K row."""
+    return rows * (256 + 130 + (8 if op == "write_index_k" else 0))
+
+
+def run_op(args):
+    import torch
+
+    from sparse_attention_indexer_qli_gb300 import qli
+    world, rank, local = dist_setup()
+    qli.lib()
+    op = args.op
+    nsets = 3
+    pool_case = (synth.make_case(100 * rank + 7, [65536, 65536], [1, 1], N=64, ratio=2, topk=2048)
+                 if op == "write_index_k" else None)
+    host = [op_inputs(op, 1000 * s + 100 * rank + 7, pool_case) for s in range(nsets)]
+    rows = OP_ROWS[op]
+    dev_x = [torch.from_numpy(h["x"].view(np.int16)).cuda() for h in host]
+    if op == "quantize_q":
+        q = torch.empty((4096, 64, 128), dtype=torch.int8, device="cuda")
+        sc = torch.empty((4096, 64), dtype=torch.int16, device="cuda")
+
+        def launch(i):
+            qli.quantize_q(dev_x[i], q, sc)
+        outs = [q, sc]
+        workload = "prefill-queries-t4096-n64-d128-bf16"
+    else:
+        case = host[0]["case"]
+        pool = torch.zeros((case.num_pages, case.page_stride), dtype=torch.uint8, device="cuda")
+        dev_slots = [torch.from_numpy(h["slots"]).cuda() for h in host]
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def launch(i):
+            qli.write_index_k(dev_x[i], dev_slots[i], pool, rows_per_page=case.rows_per_page,
+                              page_stride=case.page_stride, k_offset=case.k_offset,
+                              scale_offset=case.scale_offset, err_word=err)
+        outs = []
+        workload = "prefill-index-k-2x32768-rows-r2-pages64"
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda").fill_(1)
+    stream = torch.cuda.current_stream()
+    for k in range(args.warmup):
+        launch(k % nsets)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for k in range(args.steps):
+            flush.max()                      # evict the previous step's data from L2 (reads only)
+            evs[k][0].record(stream)
+            launch((args.warmup + k) % nsets)
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = sum(a.elapsed_time(b) for a, b in evs)
+    ms_max = reduce_max(ms, world)
+    value = reduce_sum(rows * args.steps, world) / (ms_max / 1e3)
+    per_ms = ms / args.steps
+    achieved = op_bytes(op, rows) / (per_ms / 1e3) / 1e9
+    peak, kind = peaks()
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": None, "kernel": "quant_kernel",
+            "peak_source": kind, "kernel_ms": per_ms, "algorithmic_bytes": op_bytes(op, rows)}
+
+    # e2e: inputs from pinned host memory, outputs (codes and scales) back
+    pin = [torch.from_numpy(h["x"].view(np.int16)).pin_memory() for h in host]
+    pin_slots = ([torch.from_numpy(h["slots"]).pin_memory() for h in host]
+                 if op == "write_index_k" else None)
+    out_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    if op == "write_index_k":
+        out_h = [torch.empty(1, dtype=torch.int32, pin_memory=True)]
+        outs = [err]
+
+    def e2e_step(k):
+        i = k % nsets
+        dev_x[i].copy_(pin[i], non_blocking=True)
+        if pin_slots is not None:
+            dev_slots[i].copy_(pin_slots[i], non_blocking=True)
+        launch(i)
+        for h, o in zip(out_h, outs):
+            h.copy_(o, non_blocking=True)
+    for k in range(args.warmup):
+        e2e_step(k)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        e2e_step(args.warmup + k)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(t0.elapsed_time(t1), world)
+    h2d = pin[0].numel() * 2 + (pin_slots[0].numel() * 8 if pin_slots is not None else 0)
+    d2h = sum(h.numel() * h.element_size() for h in out_h)
+    e2e = {"value": reduce_sum(rows * args.steps, world) / (e2e_ms / 1e3), "unit": "rows/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = 16384
+        xs = host[0]["x"].reshape(-1, 128)[:n]
+        t_0 = time.perf_counter()
+        if op == "quantize_q":
+            oracle.quantize_rows(xs)
+        else:
+            c = host[0]["case"]
+            pages = np.zeros((c.num_pages, c.page_stride), dtype=np.uint8)
+            oracle.write_index_k(xs, host[0]["slots"][:n], pages, c.rows_per_page, c.k_offset,
+                                 c.scale_offset)
+        spent = time.perf_counter() - t_0
+        cpu = {"value": n / spent, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of %d rows of the workload (%.3f s)" % (n, rows, spent)}
+    if rank != 0:
+        return
+    line = {
+        "metric": "%s rows/s (%% of HBM roof)" % op, "value": value, "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16->int8", "data": "synthetic",
+        "config": {"workload": workload, "rows_per_step": rows,
+                   "l2": "a 256 MB read between steps evicts the previous step (outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,6 +653,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--op", default="index", choices=["index", "quantize_q", "write_index_k"],
+                    help="index: the indexer (default); the others time the query quantiser "
+                         "or the index-K cache writer alone")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -515,7 +664,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.impl == "reference":
+    if args.op != "index":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": args.op,
+                              "unavailable": "the reference arm times the indexer only"}))
+            return
+        run_op(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

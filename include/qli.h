@@ -171,6 +171,52 @@ qli_status qli_read_device_error(const void *workspace, uint32_t *host_word, voi
  * on one stream. Inputs, outputs, stream and errors are as for qli_run. */
 qli_status qli_run_static(const qli_args *a, void *stream);
 
+/* ---- Query quantiser and index-K cache writer -------------------------------
+ * The two steps either side of the indexer's paged gather. The guide's
+ * section "数据流" (data flow): the indexer's projected queries are quantised
+ * per head to INT8, each head with a scale representable in FP16; head
+ * weights and K scales are FP16; the page allocator packs the index K and
+ * its FP16 scales after the KV inside each page.
+ *
+ * One row x of D = 128 BF16 values (passed as 16-bit patterns) becomes 128
+ * INT8 codes and one FP16 scale:
+ *     amax = max_d |x_d|
+ *     s    = FP16(amax / 127)   FP32 quotient, then round to nearest even;
+ *                               capped at 65504
+ *     q_d  = clamp(rint(x_d / s), -127, 127)   FP32 quotient, ties to even
+ * A row whose s rounds to zero (amax below 127 * 2^-25, e.g. all zeros)
+ * gets codes 0 and scale +0. Inf and NaN inputs are outside the contract
+ * (their codes are unspecified; nothing is read or written out of bounds).
+ * The pages do not spell the formula out; this is the plain symmetric
+ * absmax reading of "INT8 with a representable FP16 scale": the stored FP16
+ * value is the one divided by, so q * s is the dequantised value. */
+
+/* Quantises `rows` rows of 128 BF16 values, contiguous at x (16-byte
+ * aligned), to codes q_out [rows, 128] (16-byte aligned) and FP16 scales
+ * scale_out [rows] (2-byte aligned). For the indexer's queries, rows = T * N
+ * and x is [T, N, 128]: q_out is then the TND q (q_stride_t = N * 128,
+ * q_stride_h = 128) and scale_out the [T, N] q_scale. Device pointers; one
+ * kernel on `stream`; asynchronous. rows = 0 launches nothing. */
+qli_status qli_quantize_q(const uint16_t *x, int64_t rows, int8_t *q_out, uint16_t *scale_out,
+                          void *stream);
+
+/* Quantises n new index-K rows (k: [n, 128] BF16, 16-byte aligned) and
+ * writes row i into the PA_BBND page pool `cache` at slot_mapping[i] =
+ * page * rows_per_page + row: codes at cache + page * page_stride +
+ * k_offset + row * 128, FP16 scale at cache + page * page_stride +
+ * scale_offset + row * 2 (the layout qli_run reads). A negative slot is
+ * padding: nothing is written. A slot at or past num_pages * rows_per_page
+ * is skipped and, when err_word is not NULL, sets QLI_DEVERR_PAGE in that
+ * device word (OR'ed in; the caller clears it). The slots of one call must
+ * be distinct. cache, page_stride and k_offset must be multiples of 16 bytes
+ * and scale_offset of 2; rows_per_page is 64 or 128 and k_offset +
+ * rows_per_page * 128 and scale_offset + rows_per_page * 2 must fit in a
+ * page. Device pointers; one kernel on `stream`; asynchronous. */
+qli_status qli_write_index_k(const uint16_t *k, int64_t n, const int64_t *slot_mapping,
+                             uint8_t *cache, int64_t num_pages, int64_t page_stride,
+                             int32_t rows_per_page, int64_t k_offset, int64_t scale_offset,
+                             uint32_t *err_word, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *qli_status_string(qli_status s);
 

@@ -76,10 +76,12 @@ qli_status validate(const qli_args* a) {
   return QLI_OK;
 }
 
+}  // namespace
+
 // Per device ordinal below 64: 0 = not yet queried, -1 = not an sm_103
 // device, otherwise its SM count. Device properties never change within a
 // process, so they are queried once.
-std::atomic<int> g_device_sms[64];
+static std::atomic<int> g_device_sms[64];
 
 qli_status device_sms(int* sms) {
   int dev = 0, major = 0, minor = 0;
@@ -97,8 +99,6 @@ qli_status device_sms(int* sms) {
   *sms = known;
   return QLI_OK;
 }
-
-}  // namespace
 
 cudaError_t ensure_smem_limit(const void* func, int bytes, std::atomic<uint64_t>& done) {
   int dev = 0;

@@ -126,6 +126,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// QLI_OK and the current device's SM count if it is an sm_103 GPU,
+// QLI_ERR_DEVICE otherwise (QLI_ERR_CUDA if the runtime fails).
+qli_status device_sms(int* sms);
+
 WsLayout workspace_layout(const qli_args& a);
 DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L);
 

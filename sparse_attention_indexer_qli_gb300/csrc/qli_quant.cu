@@ -1,0 +1,179 @@
+// Query quantiser and index-K cache writer: the steps either side of the
+// indexer's paged gather (guide "DeepSeek V4.1 QLI V2 与候选集成", section
+// 数据流: queries quantised per head to INT8 with an FP16-representable scale;
+// index K and its FP16 scales packed after the KV inside each page).
+//
+// Both are one pass over HBM: read 256 B of BF16 per row, write 128 B of
+// codes and a 2 B scale. A half-warp owns a row (lane j holds values
+// 8j..8j+7, one 16-byte load), so a warp instruction moves two rows; each
+// warp keeps two row pairs in flight. Per row:
+//   amax = max |x|, s = FP16(amax / 127) (FP32 quotient, round to nearest
+//   even, capped at 65504), q = clamp(rint(x / s), -127, 127) with an FP32
+//   quotient; s rounding to zero gives codes 0 and scale +0.
+#include <cuda_fp16.h>
+
+#include "qli_internal.h"
+#include "qli_ptx.cuh"
+
+namespace qli {
+namespace {
+
+constexpr int kQThreads = 256;
+constexpr int kQWarps = kQThreads / 32;
+constexpr int kQDepth = 2;            // row pairs in flight per warp
+constexpr int kRowValues = 128;
+
+__device__ __forceinline__ uint32_t code_byte(float x, float sf) {
+  int c = __float2int_rn(__fdiv_rn(x, sf));
+  c = min(max(c, -127), 127);
+  return static_cast<uint32_t>(c) & 0xffu;
+}
+
+// The half-warp's row: v = this lane's 8 BF16 values. All 32 lanes call it
+// (the reduction stays inside each half). Returns the lane's 8 codes.
+__device__ __forceinline__ uint2 quant_half_row(const uint4 v, uint16_t& scale_bits) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  uint16_t sb = __half_as_ushort(__float2half_rn(__fdiv_rn(m, 127.0f)));
+  if (sb == 0x7c00u) sb = 0x7bffu;    // +inf: the largest finite FP16
+  const float sf = __half2float(__ushort_as_half(sb));
+  uint32_t lo = 0u, hi = 0u;
+  if (sf != 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lo |= code_byte(x[i], sf) << (8 * i);
+      hi |= code_byte(x[4 + i], sf) << (8 * i);
+    }
+  } else {
+    sb = 0u;
+  }
+  scale_bits = sb;
+  return make_uint2(lo, hi);
+}
+
+// Row r's destination: the plain [rows, 128] layout, or a page slot.
+struct DenseOut {
+  int8_t* q;
+  uint16_t* scale;
+  __device__ __forceinline__ bool dest(int64_t r, uint2*& codes, uint16_t*& sc) const {
+    codes = reinterpret_cast<uint2*>(q + r * kRowValues);
+    sc = scale + r;
+    return true;
+  }
+};
+
+struct PagedOut {
+  const int64_t* slot;
+  uint8_t* cache;
+  int64_t slots_total, page_stride, k_offset, scale_offset;
+  int32_t R;
+  uint32_t* err;
+  __device__ __forceinline__ bool dest(int64_t r, uint2*& codes, uint16_t*& sc) const {
+    const int64_t m = __ldg(slot + r);
+    if (m < 0) return false;                       // padding
+    if (m >= slots_total) {
+      if (err != nullptr) atomicOr(err, QLI_DEVERR_PAGE);
+      return false;
+    }
+    const int64_t page = m / R, row = m - page * R;
+    uint8_t* p = cache + page * page_stride;
+    codes = reinterpret_cast<uint2*>(p + k_offset + row * kRowValues);
+    sc = reinterpret_cast<uint16_t*>(p + scale_offset + row * 2);
+    return true;
+  }
+};
+
+template <class Out>
+__global__ void __launch_bounds__(kQThreads) quant_kernel(const uint16_t* __restrict__ x,
+                                                          int64_t rows, Out out) {
+  const int lane = threadIdx.x & 31, half = lane >> 4, j = lane & 15;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kQWarps;
+  const int64_t warp = static_cast<int64_t>(blockIdx.x) * kQWarps + (threadIdx.x >> 5);
+  // a warp takes row pairs warp, warp + nwarps, ... kQDepth at a time
+  for (int64_t p0 = warp; 2 * p0 < rows; p0 += kQDepth * nwarps) {
+    uint4 v[kQDepth];
+#pragma unroll
+    for (int d = 0; d < kQDepth; ++d) {
+      const int64_t r = 2 * (p0 + d * nwarps) + half;
+      v[d] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows) v[d] = __ldcs(reinterpret_cast<const uint4*>(x + r * kRowValues) + j);
+    }
+#pragma unroll
+    for (int d = 0; d < kQDepth; ++d) {
+      const int64_t r = 2 * (p0 + d * nwarps) + half;
+      uint16_t sb;
+      const uint2 c = quant_half_row(v[d], sb);
+      uint2* codes;
+      uint16_t* sc;
+      if (r < rows && out.dest(r, codes, sc)) {
+        codes[j] = c;
+        if (j == 0) *sc = sb;
+      }
+    }
+  }
+}
+
+unsigned quant_grid(int64_t rows, int sms) {
+  const int64_t pairs = (rows + 1) / 2;
+  const int64_t want = (pairs + kQWarps - 1) / kQWarps;
+  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kQThreads);
+  return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace qli
+
+extern "C" qli_status qli_quantize_q(const uint16_t* x, int64_t rows, int8_t* q_out,
+                                     uint16_t* scale_out, void* stream) {
+  using namespace qli;
+  if (rows < 0) return QLI_ERR_INVALID_ARG;
+  if (rows == 0) return QLI_OK;
+  if (!x || !q_out || !scale_out) return QLI_ERR_INVALID_ARG;
+  if (!aligned_to(x, 16) || !aligned_to(q_out, 16) || !aligned_to(scale_out, 2))
+    return QLI_ERR_ALIGNMENT;
+  int sms = 0;
+  const qli_status st = device_sms(&sms);
+  if (st != QLI_OK) return st;
+  quant_kernel<DenseOut><<<quant_grid(rows, sms), kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, rows, DenseOut{q_out, scale_out});
+  return cudaGetLastError() == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+extern "C" qli_status qli_write_index_k(const uint16_t* k, int64_t n, const int64_t* slot_mapping,
+                                        uint8_t* cache, int64_t num_pages, int64_t page_stride,
+                                        int32_t rows_per_page, int64_t k_offset,
+                                        int64_t scale_offset, uint32_t* err_word, void* stream) {
+  using namespace qli;
+  if (n < 0 || num_pages < 0) return QLI_ERR_INVALID_ARG;
+  if (n == 0) return QLI_OK;
+  if (!k || !slot_mapping || !cache) return QLI_ERR_INVALID_ARG;
+  if (rows_per_page != 64 && rows_per_page != 128) return QLI_ERR_UNSUPPORTED;
+  if (page_stride <= 0 || k_offset < 0 || scale_offset < 0 ||
+      k_offset + static_cast<int64_t>(rows_per_page) * 128 > page_stride ||
+      scale_offset + static_cast<int64_t>(rows_per_page) * 2 > page_stride)
+    return QLI_ERR_INVALID_ARG;
+  if (!aligned_to(k, 16) || !aligned_to(cache, 16) || page_stride % 16 != 0 || k_offset % 16 != 0 ||
+      scale_offset % 2 != 0 || !aligned_to(slot_mapping, 8) ||
+      (err_word != nullptr && !aligned_to(err_word, 4)))
+    return QLI_ERR_ALIGNMENT;
+  int sms = 0;
+  const qli_status st = device_sms(&sms);
+  if (st != QLI_OK) return st;
+  const PagedOut out{slot_mapping, cache, num_pages * rows_per_page, page_stride, k_offset,
+                     scale_offset, rows_per_page, err_word};
+  quant_kernel<PagedOut><<<quant_grid(n, sms), kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      k, n, out);
+  return cudaGetLastError() == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}

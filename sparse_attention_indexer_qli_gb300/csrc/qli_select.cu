@@ -38,6 +38,23 @@ struct Shared {
   uint32_t sel[3];
 };
 
+static_assert(kWarps == 32, "per-warp tables are read one entry per lane");
+
+// Sum of per_warp[] over the warps before this one, and the block total:
+// one shared-memory read per lane and a warp scan.
+__device__ __forceinline__ int warps_before(const int* per_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int x = per_warp[lane];
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  total = __shfl_sync(0xffffffffu, incl, 31);
+  return __shfl_sync(0xffffffffu, incl - x, warp);
+}
+
 // A row of the selection: entry s has a key (0 = not eligible) and an id.
 struct Row {
   const float* vals;      // score row
@@ -113,6 +130,19 @@ struct Stats {
   uint32_t E, kmax, kmin;
 };
 
+// Block totals of the per-warp statistics in sh.red (every thread gets them).
+__device__ __forceinline__ Stats block_stats_from(const Shared& sh) {
+  const int lane = threadIdx.x & 31;
+  Stats st{sh.red[lane][0], sh.red[lane][1], sh.red[lane][2]};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    st.E += __shfl_xor_sync(0xffffffffu, st.E, o);
+    st.kmax = max(st.kmax, __shfl_xor_sync(0xffffffffu, st.kmax, o));
+    st.kmin = min(st.kmin, __shfl_xor_sync(0xffffffffu, st.kmin, o));
+  }
+  return st;
+}
+
 __device__ Stats row_stats(const Row& r, Shared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t cnt = 0u, kmax = 0u, kmin = 0xffffffffu;
@@ -136,12 +166,7 @@ __device__ Stats row_stats(const Row& r, Shared& sh) {
     sh.red[warp][2] = kmin;
   }
   __syncthreads();
-  Stats st{0u, 0u, 0xffffffffu};
-  for (int w = 0; w < kWarps; ++w) {
-    st.E += sh.red[w][0];
-    st.kmax = max(st.kmax, sh.red[w][1]);
-    st.kmin = min(st.kmin, sh.red[w][2]);
-  }
+  Stats st = block_stats_from(sh);
   return st;
 }
 
@@ -237,16 +262,9 @@ __device__ int ordered_output(const Row& r, uint32_t thr, int32_t need_eq, int32
     sh.warp_b[warp] = eq_cnt;
   }
   __syncthreads();
-  int gt_before = 0, eq_before = 0, total_gt = 0, total_eq = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    const int x = sh.warp_a[w], y = sh.warp_b[w];
-    if (w < warp) {
-      gt_before += x;
-      eq_before += y;
-    }
-    total_gt += x;
-    total_eq += y;
-  }
+  int total_gt, total_eq;
+  const int gt_before = warps_before(sh.warp_a, total_gt);
+  const int eq_before = warps_before(sh.warp_b, total_eq);
   int at = gt_before + min(need_eq, eq_before);
   int eq_seen = eq_before;
   for (int32_t base = lo; base < hi; base += 32) {
@@ -281,11 +299,8 @@ __device__ int compact_at_least(const Row& r, uint32_t t_lo, int32_t* idx, int c
   __syncthreads();
   if (lane == 0) sh.warp_a[warp] = cnt;
   __syncthreads();
-  int at = 0, total = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    at += w < warp ? sh.warp_a[w] : 0;
-    total += sh.warp_a[w];
-  }
+  int total;
+  int at = warps_before(sh.warp_a, total);
   if (total <= cap) {
     for (int32_t base = lo; base < hi; base += 32) {
       const int32_t s = base + lane;
@@ -674,11 +689,9 @@ __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
     }
     if (lane == 31) warp_cnt[warp] = static_cast<int>(incl);
     __syncthreads();
-    uint32_t base = 0u, total = 0u;
-    for (int w = 0; w < kWarps; ++w) {
-      base += w < warp ? static_cast<uint32_t>(warp_cnt[w]) : 0u;
-      total += static_cast<uint32_t>(warp_cnt[w]);
-    }
+    int total_i;
+    const uint32_t base = static_cast<uint32_t>(warps_before(warp_cnt, total_i));
+    const uint32_t total = static_cast<uint32_t>(total_i);
     uint32_t above = base + incl - mine;
     const uint32_t k = static_cast<uint32_t>(want);
     if (total > k && above < k && k <= above + mine) {
@@ -707,11 +720,8 @@ __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
   __syncthreads();
   if (lane == 0) warp_cnt[warp] = cnt;
   __syncthreads();
-  int at = 0, total = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    at += w < warp ? warp_cnt[w] : 0;
-    total += warp_cnt[w];
-  }
+  int total;
+  int at = warps_before(warp_cnt, total);
   const int64_t segbase = (row * a.lchunks + blockIdx.x) * static_cast<int64_t>(kLongChunkCap);
   for (int32_t b = wlo; b < whi; b += 32) {
     const int32_t s = b + lane;
@@ -818,12 +828,7 @@ __device__ Stats cache_keys(Row& r, uint32_t* keys, int32_t cap, Shared& sh, boo
     sh.red[warp][2] = kmin;
   }
   __syncthreads();
-  Stats st{0u, 0u, 0xffffffffu};
-  for (int w = 0; w < kWarps; ++w) {
-    st.E += sh.red[w][0];
-    st.kmax = max(st.kmax, sh.red[w][1]);
-    st.kmin = min(st.kmin, sh.red[w][2]);
-  }
+  Stats st = block_stats_from(sh);
   if (cached) r.cached = keys;
   return st;
 }

@@ -55,7 +55,7 @@ class Args(ctypes.Structure):
 
 EXPORTS = ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage", "qli_launch_count",
            "qli_scores_layout", "qli_read_device_error", "qli_status_string", "qli_abi_version",
-           "qli_args_size", "qli_run_static"]
+           "qli_args_size", "qli_run_static", "qli_quantize_q", "qli_write_index_k"]
 
 _lib = None
 
@@ -85,6 +85,11 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.qli_status_string.restype = ctypes.c_char_p
     L.qli_abi_version.restype = c_int32
     L.qli_args_size.restype = c_int64
+    L.qli_quantize_q.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p]
+    L.qli_quantize_q.restype = c_int32
+    L.qli_write_index_k.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_int64,
+                                    c_int32, c_int64, c_int64, c_void_p, c_void_p]
+    L.qli_write_index_k.restype = c_int32
     for name in ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage",
                  "qli_launch_count", "qli_scores_layout", "qli_read_device_error"]:
         getattr(L, name).restype = c_int32
@@ -232,3 +237,43 @@ def run(*args, workspace=None, stream=None, **kw):
     c = Call(*args, **kw)
     ws = c.alloc_workspace() if workspace is None else workspace
     return c.run(ws, stream)
+
+
+def quantize_q(x, q_out=None, scale_out=None, stream=None):
+    """qli_quantize_q: BF16 rows x [..., 128] (torch.bfloat16 or int16/uint16
+    bit patterns, CUDA, contiguous) -> (codes int8 [..., 128], FP16 scale bits
+    int16 [...]). For the indexer's queries x is [T, N, 128]."""
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous CUDA tensor")
+    if x.element_size() != 2 or x.shape[-1] != 128:
+        raise TypeError("x must hold 16-bit BF16 patterns with 128 values per row")
+    rows = x.numel() // 128
+    if q_out is None:
+        q_out = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scale_out is None:
+        scale_out = torch.empty(x.shape[:-1], dtype=torch.int16, device=x.device)
+    _require_cuda("q_out", q_out, torch.int8)
+    _check(lib().qli_quantize_q(_ptr(x), rows, _ptr(q_out), _ptr(scale_out), _stream(stream)),
+           "qli_quantize_q")
+    return q_out, scale_out
+
+
+def write_index_k(k, slot_mapping, cache, *, rows_per_page: int, page_stride: int,
+                  k_offset: int, scale_offset: int, err_word=None, stream=None):
+    """qli_write_index_k: quantises the rows of k [n, 128] (BF16 patterns,
+    CUDA, contiguous) and writes them into the page pool `cache` (uint8, CUDA)
+    at slot_mapping [n] (int64: page * rows_per_page + row; negative = skip)."""
+    import torch
+    _require_cuda("slot_mapping", slot_mapping, torch.int64)
+    _require_cuda("cache", cache, torch.uint8)
+    _require_cuda("err_word", err_word, torch.int32)
+    if not isinstance(k, torch.Tensor) or not k.is_cuda or not k.is_contiguous() \
+            or k.element_size() != 2 or k.dim() != 2 or k.shape[1] != 128:
+        raise TypeError("k must be a contiguous CUDA [n, 128] tensor of BF16 patterns")
+    if slot_mapping.numel() != k.shape[0]:
+        raise ValueError("one slot per row")
+    num_pages = cache.numel() // page_stride
+    _check(lib().qli_write_index_k(_ptr(k), k.shape[0], _ptr(slot_mapping), _ptr(cache),
+                                   num_pages, page_stride, rows_per_page, k_offset, scale_offset,
+                                   _ptr(err_word), _stream(stream)), "qli_write_index_k")

@@ -199,3 +199,46 @@ def test_torch_packing_matches_numpy_packing():
     a = case.pack_pages_numpy(filler=False)
     b = case.pack_pages_torch("cpu", filler=False).numpy()
     assert (a == b).all()
+
+
+# ---- query quantiser and index-K writer: host validation only --------------
+
+A16 = 1 << 20          # a fake, 16-byte-aligned address (never dereferenced)
+
+
+def test_quantize_q_validation(L):
+    f = L.qli_quantize_q
+    assert f(None, 0, None, None, None) == qli.OK             # nothing to do, nothing launched
+    assert f(A16, -1, A16, A16, None) == 1                    # QLI_ERR_INVALID_ARG
+    assert f(None, 4, A16, A16, None) == 1
+    assert f(A16, 4, None, A16, None) == 1
+    assert f(A16 + 8, 4, A16, A16, None) == 6                 # QLI_ERR_ALIGNMENT
+    assert f(A16, 4, A16 + 4, A16, None) == 6
+    assert f(A16, 4, A16, A16 + 1, None) == 6
+
+
+def _w(L, **kw):
+    a = dict(k=A16, n=4, slot=A16, cache=A16, num_pages=10, page_stride=131072,
+             R=64, k_off=65536, s_off=65536 + 8192, err=None)
+    a.update(kw)
+    return L.qli_write_index_k(a["k"], a["n"], a["slot"], a["cache"], a["num_pages"],
+                               a["page_stride"], a["R"], a["k_off"], a["s_off"], a["err"], None)
+
+
+def test_write_index_k_validation(L):
+    assert _w(L, n=0, k=None, slot=None, cache=None) == qli.OK
+    assert _w(L, n=-1) == 1
+    assert _w(L, k=None) == 1
+    assert _w(L, slot=None) == 1
+    assert _w(L, cache=None) == 1
+    assert _w(L, num_pages=-1) == 1
+    assert _w(L, R=32) == 2                                     # QLI_ERR_UNSUPPORTED
+    assert _w(L, k_off=131072 - 64 * 128 + 16) == 1             # index K past the page
+    assert _w(L, s_off=131072 - 64 * 2 + 2) == 1                # scales past the page
+    assert _w(L, k=A16 + 8) == 6
+    assert _w(L, cache=A16 + 8) == 6
+    assert _w(L, page_stride=131072 + 8) == 6
+    assert _w(L, k_off=65536 + 8) == 6
+    assert _w(L, s_off=65536 + 8192 + 1) == 6
+    assert _w(L, slot=A16 + 4) == 6
+    assert _w(L, err=A16 + 2) == 6
