@@ -184,7 +184,7 @@ def tensor_peak():
 def profiled_traffic():
     """Per-launch DRAM traffic of the score kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "stream_kernel_decode_b64_r1.md")
+    path = os.path.join(ROOT, "profiles", "stream_kernel_decode_b64_ratio1.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()

@@ -6,7 +6,7 @@
 // Both are one pass over HBM: read 256 B of BF16 per row, write 128 B of
 // codes and a 2 B scale. A half-warp owns a row (lane j holds values
 // 8j..8j+7, one 16-byte load), so a warp instruction moves two rows; each
-// warp keeps two row pairs in flight. Per row:
+// warp keeps four row pairs in flight. Per row:
 //   amax = max |x|, s = FP16(amax / 127) (FP32 quotient, round to nearest
 //   even, capped at 65504), q = clamp(rint(x / s), -127, 127) with an FP32
 //   quotient; s rounding to zero gives codes 0 and scale +0.
@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kQThreads = 256;
 constexpr int kQWarps = kQThreads / 32;
-constexpr int kQDepth = 2;            // row pairs in flight per warp
+constexpr int kQDepth = 4;            // row pairs in flight per warp
 constexpr int kRowValues = 128;
 
 __device__ __forceinline__ uint32_t code_byte(float x, float sf) {

@@ -476,6 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int ctid = tid - 32 * kConvWarp0 - 128 * grp;   // 0..127 within the group
     int32_t btok0 = -1, btok1 = -1;          // token staged in the group's two stages
+    int32_t wtok = -1;                       // token whose w * q_scale this thread holds
+    __half wq_own = __ushort_as_half(0);
     Cursor c;
     c.init(a, u0);
     if (grp == 1) c.next(a, u0 + 1);
@@ -488,12 +490,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       const int32_t t = c.t;
       const int slot = k % kSlots;
       const bool second = (k >> 1) & 1;      // which of the group's two stages
-      // the token's weights and (on a token change) its queries are staged
-      // before waiting for the K tile, so their global loads overlap the TMA;
-      // every load is issued before the first conversion
-      const int64_t wo = static_cast<int64_t>(t) * a.N + ctid;
+      // on a token change its weights and queries are loaded before waiting
+      // for the K tile, so the global loads overlap the TMA; within a token
+      // the weight * Q scale product stays in a register
       const bool has_w = ctid < a.N;
-      const uint16_t wb = has_w ? a.w[wo] : 0, qb = has_w ? a.qs[wo] : 0;
+      if (wtok != t) {
+        wtok = t;
+        const int64_t wo = static_cast<int64_t>(t) * a.N + ctid;
+        const uint16_t wb = has_w ? a.w[wo] : 0, qb = has_w ? a.qs[wo] : 0;
+        wq_own = __hmul(__ushort_as_half(wb), __ushort_as_half(qb));
+      }
       if ((second ? btok1 : btok0) != t) {
         // queries of token t: FP16 * 2^-10, K-major, 128-byte swizzle
         constexpr int kPer = 64 * 16 / 128;   // chunks per thread at N = 64
@@ -515,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         }
         if (second) btok1 = t; else btok0 = t;
       }
-      if (has_w) S.wq[slot][ctid] = __hmul(__ushort_as_half(wb), __ushort_as_half(qb));
+      if (has_w) S.wq[slot][ctid] = wq_own;
       if (!mbar_wait_warp(&S.full[sk], (k / kKStages) & 1)) { ok = false; break; }
       // this thread's K row, stored 128-byte swizzled by the TMA: logical
       // chunk ch (K elements 16ch..16ch+15) sits at chunk ch ^ (row & 7); a

@@ -378,19 +378,20 @@ __device__ HistSel hist_select(const uint32_t* g, int32_t pinned, int32_t want, 
   return h;
 }
 
-// One pass over a row in global memory keeping, in row order, every entry
-// whose key is at least t_lo: its key to ckeys[] and its id (position) to
-// cid[]; returns how many (written only while below cap). Chunks of 4096
-// entries, thread i taking entries 4i..4i+3 of a chunk with one 16-byte
-// load; the loads of up to kBatch chunks are issued before the first is
-// used. One barrier per chunk.
-template <bool kConsumer>
-__device__ int compact_from_row(const Row& r, uint32_t t_lo, uint32_t* ckeys, int32_t* cid,
-                                int cap, Shared& sh) {
+// One pass over entries [begin, end) of a row in global memory keeping, in
+// row order, every eligible entry whose key passes keep(): its key to
+// ckeys[] and its id (position) to cid[] (shared or global memory); returns
+// how many (written only while below cap). Chunks of 4096 entries, thread i
+// taking entries 4i..4i+3 of a chunk with one 16-byte load (begin is a
+// multiple of 4); the loads of up to kBatch chunks are issued before the
+// first is used. One barrier per chunk.
+template <bool kConsumer, class Keep>
+__device__ int compact_range(const Row& r, int32_t begin, int32_t end, Keep keep_key,
+                             uint32_t* ckeys, int32_t* cid, int cap, Shared& sh) {
   constexpr int kBatch = 6;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned below = (1u << lane) - 1u;
-  const int32_t nchunks = (r.len + 4 * kThreads - 1) / (4 * kThreads);
+  const int32_t nchunks = (end - begin + 4 * kThreads - 1) / (4 * kThreads);
   const float4* v4 = reinterpret_cast<const float4*>(r.vals);
   int base = 0;
   for (int32_t c0 = 0; c0 < nchunks; c0 += kBatch) {
@@ -398,10 +399,10 @@ __device__ int compact_from_row(const Row& r, uint32_t t_lo, uint32_t* ckeys, in
     int32_t blk[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int32_t s0 = (c0 + u) * 4 * kThreads + 4 * tid;
+      const int32_t s0 = begin + (c0 + u) * 4 * kThreads + 4 * tid;
       f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       blk[u] = 0;
-      if (s0 < r.len) {
+      if (s0 < end) {
         f[u] = __ldcg(v4 + (s0 >> 2));
         if (kConsumer) blk[u] = __ldcg(r.blocks + (s0 >> 3));
       }
@@ -409,14 +410,14 @@ __device__ int compact_from_row(const Row& r, uint32_t t_lo, uint32_t* ckeys, in
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       if (c0 + u >= nchunks) break;                         // block-uniform
-      const int32_t s0 = (c0 + u) * 4 * kThreads + 4 * tid;
+      const int32_t s0 = begin + (c0 + u) * 4 * kThreads + 4 * tid;
       const int32_t id0 = kConsumer ? blk[u] * kBlock + (s0 & (kBlock - 1)) : s0;
       const uint32_t k[4] = {order_key(f[u].x), order_key(f[u].y), order_key(f[u].z),
                              order_key(f[u].w)};
       unsigned keep = 0u;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const bool ok = s0 + j < r.len && (!kConsumer || id0 + j < r.V) && k[j] >= t_lo;
+        const bool ok = s0 + j < end && (!kConsumer || id0 + j < r.V) && k[j] != 0u && keep_key(k[j]);
         keep |= ok ? (1u << j) : 0u;
       }
       const int cnt = __popc(keep);
@@ -650,127 +651,129 @@ __global__ void __launch_bounds__(kThreads) lhist_kernel(DevArgs a) {
 __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int warp_cnt[kWarps];
-  __shared__ uint32_t s_digit;
+  __shared__ Shared sh;
   Row r;
   int32_t want, lo, hi;
   const int t = blockIdx.y, which = blockIdx.z;
   if (!long_row(a, t, which, r, want, lo, hi)) return;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t row = 2 * static_cast<int64_t>(t) + which;
-  // digits: the score stage's top-12-bit histogram when there is one, else
-  // the 12 bits below the row's common prefix (lstat / lhist)
-  const bool fused = a.fhist != nullptr;
-  const uint32_t* e = a.lext + 4 * row;
-  const LongDigit dg = fused ? LongDigit() : LongDigit(e[0], ~e[1]);
-  const uint32_t* g = fused ? a.fhist + row * kHistBins : a.lhist + 4096 * row;
-  int32_t pinned = -1;     // the pinned last block is counted but not ranked
-  if (fused && which == 1) {
-    const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
-    pinned = static_cast<int32_t>(dg.of(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
-  }
-  // the digit holding the want-th best entry (0: keep every eligible entry)
-  if (tid == 0) s_digit = 0u;
-  __syncthreads();
-  if (dg.width > 0) {
-    const int nb = 1 << dg.width;
-    // thread i owns bins nb-1-4i .. nb-4-4i (top down)
-    uint32_t c[4], mine = 0u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int bin = nb - 1 - 4 * tid - j;
-      c[j] = bin >= 0 ? g[bin] - (bin == pinned ? 1u : 0u) : 0u;
-      mine += c[j];
+  const int64_t segbase = (row * a.lchunks + blockIdx.x) * static_cast<int64_t>(kLongChunkCap);
+  uint32_t* okey = a.lkey + segbase;
+  int32_t* oid = a.lid + segbase;
+  int total;
+  if (a.fhist != nullptr) {
+    // the score stage's top-12-bit histogram: keep the bin holding the
+    // want-th best entry and everything above it (every eligible entry when
+    // the row has no more than `want`); the pinned last block is counted in
+    // the block histogram but not ranked
+    int32_t pinned = -1;
+    if (which == 1) {
+      const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
+      pinned = static_cast<int32_t>(
+          hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
     }
-    uint32_t incl = mine;
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_cnt[warp] = static_cast<int>(incl);
+    const HistSel hs = hist_select(a.fhist + row * kHistBins, pinned, want, sh);
+    const uint32_t t_lo = hs.E > static_cast<uint32_t>(want) ? hs.sel << (32 - kHistBits) : 1u;
+    const auto keep = [t_lo](uint32_t k) { return k >= t_lo; };
+    total = r.consumer ? compact_range<true>(r, lo, hi, keep, okey, oid, kLongChunkCap, sh)
+                       : compact_range<false>(r, lo, hi, keep, okey, oid, kLongChunkCap, sh);
+  } else {
+    // the 12 bits below the row's common prefix (lstat / lhist): the digit
+    // holding the want-th best entry (0: keep every eligible entry)
+    const uint32_t* e = a.lext + 4 * row;
+    const LongDigit dg(e[0], ~e[1]);
+    const uint32_t* g = a.lhist + 4096 * row;
+    if (tid == 0) sh.sel[0] = 0u;
     __syncthreads();
-    int total_i;
-    const uint32_t base = static_cast<uint32_t>(warps_before(warp_cnt, total_i));
-    const uint32_t total = static_cast<uint32_t>(total_i);
-    uint32_t above = base + incl - mine;
-    const uint32_t k = static_cast<uint32_t>(want);
-    if (total > k && above < k && k <= above + mine) {
+    if (dg.width > 0) {
+      const int nb = 1 << dg.width;
+      // thread i holds digits nb-1-4i .. nb-4-4i (top down)
+      uint32_t c[4], mine = 0u;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (above + c[j] >= k) {
-          s_digit = static_cast<uint32_t>(nb - 1 - 4 * tid - j);
-          break;
+        const int bin = nb - 1 - 4 * tid - j;
+        c[j] = bin >= 0 ? g[bin] : 0u;
+        mine += c[j];
+      }
+      uint32_t E;
+      const uint32_t incl = block_scan(mine, E, sh);
+      uint32_t above = incl - mine;
+      const uint32_t k = static_cast<uint32_t>(want);
+      if (E > k && above < k && k <= incl) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (above + c[j] >= k) {
+            sh.sel[0] = static_cast<uint32_t>(nb - 1 - 4 * tid - j);
+            break;
+          }
+          above += c[j];
         }
-        above += c[j];
       }
     }
     __syncthreads();
-  }
-  const uint32_t dmin = s_digit;
-  // ordered compaction of the chunk's entries with digit >= dmin
-  const int32_t seg = ((hi - lo + kWarps - 1) / kWarps + 31) & ~31;
-  const int32_t wlo = lo + warp * seg, whi = min(hi, wlo + seg);
-  const unsigned below = (1u << lane) - 1u;
-  int cnt = 0;
-  for (int32_t b = wlo; b < whi; b += 32) {
-    const int32_t s = b + lane;
-    const uint32_t key = s < whi ? r.key(s) : 0u;
-    cnt += __popc(__ballot_sync(0xffffffffu, key != 0u && dg.of(key) >= dmin));
-  }
-  __syncthreads();
-  if (lane == 0) warp_cnt[warp] = cnt;
-  __syncthreads();
-  int total;
-  int at = warps_before(warp_cnt, total);
-  const int64_t segbase = (row * a.lchunks + blockIdx.x) * static_cast<int64_t>(kLongChunkCap);
-  for (int32_t b = wlo; b < whi; b += 32) {
-    const int32_t s = b + lane;
-    const uint32_t key = s < whi ? r.key(s) : 0u;
-    const bool keep = key != 0u && dg.of(key) >= dmin;
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    const int dst = at + __popc(m & below);
-    if (keep && dst < kLongChunkCap) {
-      a.lkey[segbase + dst] = key;
-      a.lid[segbase + dst] = r.id(s);
-    }
-    at += __popc(m);
+    const uint32_t dmin = sh.sel[0];
+    const auto keep = [dg, dmin](uint32_t k) { return dg.of(k) >= dmin; };
+    total = r.consumer ? compact_range<true>(r, lo, hi, keep, okey, oid, kLongChunkCap, sh)
+                       : compact_range<false>(r, lo, hi, keep, okey, oid, kLongChunkCap, sh);
   }
   if (tid == 0) a.lcount[row * a.lchunks + blockIdx.x] = total;
 }
 
 // Replaces a long row by its candidates (keys and ids in shared memory, in
 // position order) when every segment fits; returns false to rank from L2.
+// Thread c reads chunk c's count; a block scan places the segments; then
+// every thread copies entries, four loads in flight. `offs` is shared
+// scratch of at least kThreads + 1 words.
 __device__ bool load_candidates(const DevArgs& a, int t, int which, Row& r, uint32_t* keys,
-                                int32_t* ids) {
-  __shared__ int s_total, s_over;
+                                int32_t* ids, int32_t* offs, Shared& sh) {
+  const int tid = threadIdx.x;
   const int64_t row = 2 * static_cast<int64_t>(t) + which;
   const int32_t nch = (r.len + kLongChunk - 1) / kLongChunk;
-  if (threadIdx.x == 0) {
-    int tot = 0, over = 0;
-    for (int c = 0; c < nch; ++c) {
-      const int n = a.lcount[row * a.lchunks + c];
-      over |= n > kLongChunkCap;
-      tot += n;
-    }
-    s_total = tot;
-    s_over = over || tot > kLongCandCap;
-  }
+  if (nch > kThreads) return false;                          // block-uniform
+  const int n = tid < nch ? a.lcount[row * a.lchunks + tid] : 0;
+  const int over = __syncthreads_or(n > kLongChunkCap);
+  uint32_t total_u;
+  const uint32_t incl = block_scan(static_cast<uint32_t>(n), total_u, sh);
+  const int total = static_cast<int>(total_u);
+  if (over || total > kLongCandCap) return false;
+  if (tid < nch) offs[tid] = static_cast<int32_t>(incl) - n;
+  if (tid == 0) offs[nch] = total;
   __syncthreads();
-  if (s_over) return false;
-  int base = 0;
-  for (int c = 0; c < nch; ++c) {
-    const int n = a.lcount[row * a.lchunks + c];
-    const int64_t seg = (row * a.lchunks + c) * static_cast<int64_t>(kLongChunkCap);
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      keys[base + i] = a.lkey[seg + i];
-      ids[base + i] = a.lid[seg + i];
+  const int64_t seg0 = row * a.lchunks * static_cast<int64_t>(kLongChunkCap);
+  for (int base = 0; base < total; base += 4 * kThreads) {
+    uint32_t kk[4];
+    int32_t ii[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * kThreads + tid;
+      kk[u] = 0u;
+      ii[u] = 0;
+      if (i < total) {
+        int lo = 0, hi = nch - 1;           // the chunk whose segment holds entry i
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (offs[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const int64_t at = seg0 + static_cast<int64_t>(lo) * kLongChunkCap + (i - offs[lo]);
+        kk[u] = __ldcg(a.lkey + at);
+        ii[u] = __ldcg(a.lid + at);
+      }
     }
-    base += n;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * kThreads + tid;
+      if (i < total) {
+        keys[i] = kk[u];
+        ids[i] = ii[u];
+      }
+    }
   }
   __syncthreads();
   r.cached = keys;
   r.ids = ids;
-  r.len = s_total;
+  r.idx = nullptr;
+  r.len = total;
   r.consumer = false;
   return true;
 }
@@ -857,9 +860,37 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
     written = nb;
   } else {
     if (r.len > key_cap) {
-      if (a.lchunks > 0)
-        (void)load_candidates(a, t, which, r, keys, reinterpret_cast<int32_t*>(keys) + kLongCandCap);
-      written = select_ascending(r, want, out, sh, scratch);
+      // long row: its candidates (every entry in or above the threshold bin
+      // or digit) were compacted by lcompact_kernel
+      int32_t* cid = reinterpret_cast<int32_t*>(keys) + kLongCandCap;
+      int32_t* offs = reinterpret_cast<int32_t*>(scratch);
+      bool done = false;
+      if (a.lchunks > 0 && a.fhist != nullptr) {
+        int32_t pinned = -1;
+        if (blocks) {
+          const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
+          pinned = static_cast<int32_t>(
+              hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
+        }
+        const HistSel hs = hist_select(
+            a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins, pinned, want, sh);
+        if (hs.E > static_cast<uint32_t>(want) &&
+            load_candidates(a, t, which, r, keys, cid, offs, sh)) {
+          if (static_cast<uint32_t>(r.len) == hs.above + hs.cbin) {
+            uint32_t thr;
+            int32_t need_eq;
+            refine_threshold(keys, r.len, hs.sel, want - static_cast<int32_t>(hs.above),
+                             scratch + kHeadWords + kCandCap - 1024, sh, thr, need_eq);
+            written = ordered_output(r, thr, need_eq, out, sh);
+          } else {
+            written = select_ascending(r, want, out, sh, nullptr);
+          }
+          done = true;
+        }
+      } else if (a.lchunks > 0) {
+        (void)load_candidates(a, t, which, r, keys, cid, offs, sh);
+      }
+      if (!done) written = select_ascending(r, want, out, sh, nullptr);
     } else if (a.fhist != nullptr) {
       // the score stage's histogram gives the threshold bin up front: one
       // pass caches the row, the entries at or above it are compacted in row
@@ -883,8 +914,9 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
       } else if (n <= static_cast<uint32_t>(cap)) {
         int32_t* cid = reinterpret_cast<int32_t*>(scratch);
         const uint32_t t_lo = hs.sel << (32 - kHistBits);
-        const int got = r.consumer ? compact_from_row<true>(r, t_lo, keys, cid, cap, sh)
-                                   : compact_from_row<false>(r, t_lo, keys, cid, cap, sh);
+        const auto keep = [t_lo](uint32_t k) { return k >= t_lo; };
+        const int got = r.consumer ? compact_range<true>(r, 0, r.len, keep, keys, cid, cap, sh)
+                                   : compact_range<false>(r, 0, r.len, keep, keys, cid, cap, sh);
         if (got == static_cast<int>(n)) {
           uint32_t thr;
           int32_t need_eq;
