@@ -377,6 +377,7 @@ def run_ours(args):
         gs[1].replay()
         ev[2].record(stream)
         gs[2].replay()
+        ev[3].record(stream)
 
     for k in range(args.warmup):
         whole[k % nsets].replay()
@@ -396,14 +397,23 @@ def run_ours(args):
 
     # the score kernel's own duration: K staged steps, events between stages
     for k in range(args.warmup):
-        staged_step(k, [torch.cuda.Event(enable_timing=True) for _ in range(3)])
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        staged_step(k, [torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for k in range(args.steps):
         staged_step(args.warmup + k, evs[k])
     torch.cuda.synchronize()
     score_ms = [e[1].elapsed_time(e[2]) for e in evs]
     score_ms_avg = sum(score_ms) / len(score_ms)
     roof = roofline(idx, sets, args, score_ms_avg)
+    # an on-chip wait that gave up (200 ms) or another disturbance would show
+    # as a step far slower than its stages timed one by one
+    staged_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / len(evs)
+    err = sets[0][1].device_error(workspace)
+    if err != 0 or ms / args.steps > 3 * staged_ms:
+        sys.stderr.write("timed region disturbed: device error %d, %.3f ms per step against "
+                         "%.3f ms for the stages timed one by one\n"
+                         % (err, ms / args.steps, staged_ms))
+        sys.exit(3)
 
     # e2e: the public call from pinned host buffers, copies inside the timed region
     e2e = run_e2e(args, sets, workspace, stream, world)

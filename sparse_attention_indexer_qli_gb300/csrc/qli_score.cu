@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
 // (token, tile) list, so the token's queries stay in shared memory across
 // its tiles. Warp roles:
 //   warp 0      producer: TMA copies of the tile's INT8 K rows (128-byte
-//               swizzle) and FP16 scales into an 8-stage shared-memory ring
+//               swizzle) and FP16 scales into an 11-stage shared-memory ring
 //               (whole pages for dense tiles; 1 KB + 16 B per 8-position
 //               block in consumer mode); for dense tiles lane j resolves the
 //               page IDs of tile k0+j once per 32 tiles, so no block-table
@@ -251,11 +251,22 @@ __global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
 //   warps 10-17 epilogue, two groups of four taking alternate tiles: the
 //               golden chain per position (a 64-long dependent FP32 add chain,
 //               so two tiles are summed at once), score store, block max
-// TMEM: 4 stages x (64 A columns + 64 accumulator columns).
+// An M=128, K=16 tcgen05.mma costs about the same for N = 64 as for N = 128
+// (about 117 cycles), so with one token's 64 heads per tile the tensor core
+// needs about 8 x 117 cycles per tile: the pipeline is built to keep it fed.
 namespace stream {
 
-constexpr int kKStages = 8;                          // shared-memory K ring
-constexpr int kStages = 4;                           // TMEM / query stages
+constexpr int kKStages = 11;                         // shared-memory K ring
+// TMEM holds two rings: the MMA's A operands (the converted K tiles, 64
+// columns each), freed when the tensor core has read them, and the
+// accumulators (64 columns each), freed when the epilogue has loaded them.
+// Converters therefore wait only on the tensor core, and the tensor core
+// only on the epilogue.
+constexpr int kASlots = 5;                           // columns 0 .. 319
+constexpr int kDSlots = 3;                           // columns 320 .. 511
+constexpr uint32_t kSlotCols = 64;
+constexpr uint32_t kDCol0 = kASlots * kSlotCols;
+static_assert(kDCol0 + kDSlots * kSlotCols == 512, "TMEM column budget");
 // warp roles: 0 producer, 1 MMA, then two groups of four converter warps,
 // then two groups of four epilogue warps
 constexpr int kConvWarp0 = 2, kEpiWarp0 = kConvWarp0 + 8, kWarpsTotal = kEpiWarp0 + 8;
@@ -265,24 +276,30 @@ constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per s
 constexpr int kSBytes = kTile * 2;                   // 256 B of FP16 scales per stage
 constexpr int kBBytes = 64 * kHeadDim * 2;           // 16 KB: up to 64 heads, FP16
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kStageCols = 128;                 // A: 64 columns, D: 64 columns
 
-// wq and K scales of tile k live in slot k % kSlots: the epilogue releases a
-// TMEM stage as soon as its accumulator is in registers, so the converter of
-// tile k + 4 may already be running while tile k's golden chain is summed.
-constexpr int kSlots = 8;
+// wq and K scales of tile k live in slot k % kSlots, written by the
+// converter and read by the epilogue after it has released the tile's
+// accumulator. The converter of tile k + kSlots waits for the MMA of tile
+// k + kSlots - kASlots, which needed the accumulator slot that the epilogue
+// of tile k + kSlots - kASlots - kDSlots released; for kSlots >= 10 (even)
+// that is a later tile of the same epilogue group, so tile k's epilogue has
+// finished reading its slot.
+constexpr int kSlots = 16;
+static_assert(kSlots >= 2 + kASlots + kDSlots && kSlots % 2 == 0, "wq / ks slot reuse distance");
 
 struct Smem {
   uint8_t k[kKStages][kKBytes];                      // 1024-aligned (offset 0)
-  uint8_t b[kStages][kBBytes];                       // 1024-aligned
+  uint8_t b[2][kBBytes];                             // 1024-aligned; one per converter group
   uint8_t sc[kKStages][kSBytes];
   __half wq[kSlots][64];
   float ks[kSlots][kTile];
   uint64_t full[kKStages], empty[kKStages];
-  uint64_t afull[kStages], dfull[kStages], tempty[kStages];
+  uint64_t afull[kASlots], afree[kASlots], dfull[kDSlots], dfree[kDSlots];
+  uint64_t kready[kSlots];                           // wq / ks of the slot's tile written
   uint32_t tmem_base;
 };
 constexpr int kSmemBytes = static_cast<int>(sizeof(Smem)) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "stream kernel shared memory");
 
 // Walks the CTA's units in order: (token, tile within the token).
 struct Cursor {
@@ -346,11 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 4);
     }
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.afull[s], 4);
-      mbar_init(&S.dfull[s], 1);
-      mbar_init(&S.tempty[s], 4);
+    for (int s = 0; s < kASlots; ++s) {
+      mbar_init(&S.afull[s], 4);      // the converting group's four warps
+      mbar_init(&S.afree[s], 1);      // MMA commit
     }
+    for (int s = 0; s < kDSlots; ++s) {
+      mbar_init(&S.dfull[s], 1);      // MMA commit
+      mbar_init(&S.dfree[s], 4);      // the epilogue group's four warps
+    }
+    for (int s = 0; s < kSlots; ++s) mbar_init(&S.kready[s], 4);   // converter warps
     fence_mbar_init();
   }
   tc_fence_before();
@@ -451,22 +472,23 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       const uint32_t idesc = idesc_f16_m128(static_cast<uint32_t>(a.N));
       int k = 0;
       for (; k < nk; ++k) {
-        const int s = k % kStages;
-        const uint32_t ph = (k / kStages) & 1;
-        if (!mbar_wait_bounded(&S.afull[s], ph)) { ok = false; break; }
+        const int sa = k % kASlots, sd = k % kDSlots;
+        if (!mbar_wait_bounded(&S.afull[sa], (k / kASlots) & 1)) { ok = false; break; }
+        if (!mbar_wait_bounded(&S.dfree[sd], ((k / kDSlots) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t a_col = tmem + s * kStageCols;
-        const uint32_t d_col = a_col + 64;
-        const uint32_t b0 = smem_u32(&S.b[s][0]);
+        const uint32_t a_col = tmem + sa * kSlotCols;
+        const uint32_t d_col = tmem + kDCol0 + sd * kSlotCols;
+        const uint32_t b0 = smem_u32(&S.b[k & 1][0]);     // the converting group's queries
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const uint32_t kb = kk >> 2, koff = (kk & 3) * 32;
           mma_f16_ts(d_col, a_col + kk * 8, sdesc_k_sw128(b0 + kb * (a.N * 128) + koff), idesc,
                      kk > 0 ? 1u : 0u);
         }
-        mma_commit(&S.dfull[s]);
+        mma_commit(&S.afree[sa]);
+        mma_commit(&S.dfull[sd]);
       }
-      if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) % kStages], ((k - 1) / kStages) & 1);
+      if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) % kDSlots], ((k - 1) / kDSlots) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else if (warp < kEpiWarp0) {
@@ -475,21 +497,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     const int row = 32 * (warp & 3) + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int ctid = tid - 32 * kConvWarp0 - 128 * grp;   // 0..127 within the group
-    int32_t btok0 = -1, btok1 = -1;          // token staged in the group's two stages
+    int32_t btok = -1;                       // token whose queries sit in the group's buffer
     int32_t wtok = -1;                       // token whose w * q_scale this thread holds
     __half wq_own = __ushort_as_half(0);
     Cursor c;
     c.init(a, u0);
     if (grp == 1) c.next(a, u0 + 1);
     for (int k = grp; k < nk; k += 2) {
-      const int s = k % kStages, sk = k % kKStages;
-      const uint32_t ph = (k / kStages) & 1;
-      // the TMEM stage and its query buffer must be free (tile k-4 drained)
-      if (!mbar_wait_warp(&S.tempty[s], ph ^ 1)) { ok = false; break; }
+      const int sa = k % kASlots, sk = k % kKStages;
+      // the A slot must be free: the tensor core has read tile k - kASlots
+      if (!mbar_wait_warp(&S.afree[sa], ((k / kASlots) & 1) ^ 1)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
       const int slot = k % kSlots;
-      const bool second = (k >> 1) & 1;      // which of the group's two stages
       // on a token change its weights and queries are loaded before waiting
       // for the K tile, so the global loads overlap the TMA; within a token
       // the weight * Q scale product stays in a register
@@ -500,7 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         const uint16_t wb = has_w ? a.w[wo] : 0, qb = has_w ? a.qs[wo] : 0;
         wq_own = __hmul(__ushort_as_half(wb), __ushort_as_half(qb));
       }
-      if ((second ? btok1 : btok0) != t) {
+      if (btok != t) {
+        // the group's previous tile may still be in the tensor core, reading
+        // this buffer: its MMA completes before the buffer is rewritten (that
+        // phase cannot be overtaken: the MMA of tile k + 3 needs this tile)
+        if (k >= 2 && !mbar_wait_warp(&S.afree[(k - 2) % kASlots], ((k - 2) / kASlots) & 1)) {
+          ok = false;
+          break;
+        }
         // queries of token t: FP16 * 2^-10, K-major, 128-byte swizzle
         constexpr int kPer = 64 * 16 / 128;   // chunks per thread at N = 64
         uint2 v[kPer];
@@ -517,9 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           const int idx = ctid + 128 * i;
           const int n = idx >> 4, ch = idx & 15;
           if (idx < a.N * 16)
-            *reinterpret_cast<uint4*>(&S.b[s][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v[i]);
+            *reinterpret_cast<uint4*>(&S.b[grp][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v[i]);
         }
-        if (second) btok1 = t; else btok0 = t;
+        btok = t;
       }
       if (has_w) S.wq[slot][ctid] = wq_own;
       if (!mbar_wait_warp(&S.full[sk], (k / kKStages) & 1)) { ok = false; break; }
@@ -536,19 +563,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         raw[ch] = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
       S.ks[slot][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[sk]);
+      if (lane == 0) {
+        mbar_arrive(&S.empty[sk]);
+        mbar_arrive(&S.kready[slot]);
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t regs[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) cvt_row16(raw[4 * half + j], &regs[8 * j]);
-        tmem_st_32x32b_x32(tmem + lane_addr + s * kStageCols + 32 * half, regs);
+        tmem_st_32x32b_x32(tmem + lane_addr + sa * kSlotCols + 32 * half, regs);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.afull[s]);
+      if (lane == 0) mbar_arrive(&S.afull[sa]);
       c.next(a, u0 + k + 1);
       c.next(a, u0 + k + 2);
     }
@@ -563,27 +593,30 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     if (grp == 1) c.next(a, u0 + 1);
     int32_t vt = -1, V = 0;          // V of the current token, loaded once per token
     for (int k = grp; k < nk; k += 2) {
-      const int s = k % kStages;
-      const uint32_t ph = (k / kStages) & 1;
+      const int sd = k % kDSlots;
       if (c.t != vt) {
         vt = c.t;
         V = a.tok_V[vt];
       }
-      bool w1 = mbar_wait_warp(&S.afull[s], ph);
-      bool w2 = w1 && mbar_wait_warp(&S.dfull[s], ph);
+      // kready orders the converter's wq / ks writes before this epilogue's
+      // reads (its phase cannot run two ahead: the converter of tile
+      // k + kSlots needs an accumulator slot this group releases later);
+      // dfull says the accumulator is complete
+      const int slot = k % kSlots;
+      bool w1 = mbar_wait_warp(&S.kready[slot], (k / kSlots) & 1);
+      bool w2 = w1 && mbar_wait_warp(&S.dfull[sd], (k / kDSlots) & 1);
       if (!(w1 && w2)) { ok = false; break; }
       tc_fence_after();
       const int32_t t = c.t;
-      const int slot = k % kSlots;
-      const uint32_t d_col = tmem + lane_addr + s * kStageCols + 64;
+      const uint32_t d_col = tmem + lane_addr + kDCol0 + sd * kSlotCols;
       uint32_t r0[32], r1[32];
       tmem_ld_32x32b_x32(d_col, r0);                  // heads 0-31
       if (a.N == 64) tmem_ld_32x32b_x32(d_col + 32, r1);   // heads 32-63 (uniform)
       tmem_ld_wait();
-      // the accumulator is in registers: hand the TMEM stage back now
+      // the accumulator is in registers: hand its slot back now
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.tempty[s]);
+      if (lane == 0) mbar_arrive(&S.dfree[sd]);
       const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[slot][0]);
       float acc = 0.0f;
 #pragma unroll

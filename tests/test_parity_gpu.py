@@ -215,6 +215,39 @@ def test_stages_and_graph_replay_equal_one_call(mode):
     assert call.device_error(ws) == 0
 
 
+@pytest.mark.parametrize("idx", [2, 5])
+def test_back_to_back_graph_replays_never_time_out(idx):
+    """Hundreds of back-to-back replays of a CUDA graph of the whole call on a
+    full-size workload. Each kernel overlaps its neighbours (programmatic
+    launch) and every on-chip wait must complete: a wait that gave up would
+    cost 200 ms and set the timeout bit in the device error word, which the
+    plan kernel resets at each call, so the word is read every ten calls."""
+    import time
+
+    import torch
+    case = synth.config(idx)
+    call = qli.Call(**synth.upload(case, "cuda"))
+    ws = call.alloc_workspace()
+    idx_out, _ = call.run(ws)
+    torch.cuda.synchronize()
+    want = idx_out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            call.run(ws)
+    torch.cuda.current_stream().wait_stream(s)
+    t0 = time.perf_counter()
+    for rep in range(300):
+        g.replay()
+        if rep % 10 == 9:
+            assert call.device_error(ws) == 0, rep
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 2.0
+    assert torch.equal(call.indices, want)
+
+
 def test_parity_long_rows():
     """Rows longer than one CTA's shared memory take the multi-CTA selection
     (statistics, histogram, compaction, exact ranking of the candidates)."""
