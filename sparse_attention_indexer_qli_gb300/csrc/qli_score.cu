@@ -242,18 +242,26 @@ __global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
 //               block in consumer mode); for dense tiles lane j resolves the
 //               page IDs of tile k0+j once per 32 tiles, so no block-table
 //               load sits between two copies
-//   warp 1      MMA: 8 x tcgen05.mma (A from TMEM, B = the token's queries
-//               from shared memory), committed to the stage's barrier
-//   warps 2-9   converters, two groups of four taking alternate tiles: row =
+//   warps 1-2   MMA, one issuing thread per tile parity: 8 x tcgen05.mma
+//               (A from TMEM, B = the token's queries from shared memory),
+//               committed to the A slot's and the accumulator's barriers.
+//               Back-to-back MMAs into rotating accumulators cost about 59
+//               cycles each, but a commit stalls its thread about 128 cycles
+//               and each barrier probe about 60, so one issuer would leave
+//               the tensor core idle; two hide each other's bookkeeping.
+//   warps 3-10  converters, two groups of four taking alternate tiles: row =
 //               position; INT8 -> FP16 in registers, stored to TMEM as the
 //               MMA's A operand; queries -> FP16 * 2^-10 in 128-byte-swizzled
 //               shared memory when the token changes
-//   warps 10-17 epilogue, two groups of four taking alternate tiles: the
+//   warps 11-18 epilogue, two groups of four taking alternate tiles: the
 //               golden chain per position (a 64-long dependent FP32 add chain,
 //               so two tiles are summed at once), score store, block max
-// An M=128, K=16 tcgen05.mma costs about the same for N = 64 as for N = 128
-// (about 117 cycles), so with one token's 64 heads per tile the tensor core
-// needs about 8 x 117 cycles per tile: the pipeline is built to keep it fed.
+// Each tile parity p runs converter group p -> MMA warp p -> epilogue group
+// p, and owns A slots p, p + 2 and accumulator slots p, p + 2: the two
+// parities are independent in-order pipelines (sharing only the K ring), so
+// every barrier's previous phase belongs to the same parity and has already
+// been consumed. (With an odd slot count, one parity's epilogue could meet a
+// slot still a phase behind, waiting on the other parity's MMA issuer.)
 namespace stream {
 
 constexpr int kKStages = 11;                         // shared-memory K ring
@@ -262,16 +270,18 @@ constexpr int kKStages = 11;                         // shared-memory K ring
 // accumulators (64 columns each), freed when the epilogue has loaded them.
 // Converters therefore wait only on the tensor core, and the tensor core
 // only on the epilogue.
-constexpr int kASlots = 5;                           // columns 0 .. 319
-constexpr int kDSlots = 3;                           // columns 320 .. 511
+constexpr int kASlots = 4;                           // columns 0 .. 255
+constexpr int kDSlots = 4;                           // columns 256 .. 511
+static_assert(kASlots % 2 == 0 && kDSlots % 2 == 0, "each tile parity owns its slots");
 constexpr uint32_t kSlotCols = 64;
 constexpr uint32_t kDCol0 = kASlots * kSlotCols;
 static_assert(kDCol0 + kDSlots * kSlotCols == 512, "TMEM column budget");
 // warp roles: 0 producer, 1 MMA, then two groups of four converter warps,
 // then two groups of four epilogue warps
-constexpr int kConvWarp0 = 2, kEpiWarp0 = kConvWarp0 + 8, kWarpsTotal = kEpiWarp0 + 8;
+constexpr int kMmaWarp0 = 1, kConvWarp0 = 3, kEpiWarp0 = kConvWarp0 + 8,
+              kWarpsTotal = kEpiWarp0 + 8;
 constexpr int kThreads = 32 * kWarpsTotal;
-static_assert(kThreads == 576, "stream kernel block size");
+static_assert(kThreads == 608, "stream kernel block size");
 constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per stage
 constexpr int kSBytes = kTile * 2;                   // 256 B of FP16 scales per stage
 constexpr int kBBytes = 64 * kHeadDim * 2;           // 16 KB: up to 64 heads, FP16
@@ -342,8 +352,9 @@ __device__ __forceinline__ void cvt_row16(const uint4 v, uint32_t* out8) {
 // tm_page: box of R rows x 128 B (a whole page's index K); tm_blk: box of
 // 8 rows x 128 B (one candidate block). Both use the 128-byte swizzle, so
 // row r's 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
-// 18 warps: the four SM sub-partitions hold 5, 5, 4 and 4 of them in 16K
-// registers each, which caps a thread at 96 registers
+// 19 warps: the four SM sub-partitions hold 5, 5, 5 and 4 of them in 16K
+// registers each, which caps a thread at 96 registers (allocated in steps of
+// 8): a larger per-thread budget would make the launch fail
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_blk,
     DevArgs a) {
@@ -466,12 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         (void)mbar_wait_bounded(&S.full[k % kKStages], (k / kKStages) & 1);
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
+  } else if (warp < kConvWarp0) {
+    // ---------------- MMA issuers: warp kMmaWarp0 + p takes tiles k = p mod 2
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_m128(static_cast<uint32_t>(a.N));
-      int k = 0;
-      for (; k < nk; ++k) {
+      int last = -1;
+      for (int k = warp - kMmaWarp0; k < nk; k += 2) {
         const int sa = k % kASlots, sd = k % kDSlots;
         if (!mbar_wait_bounded(&S.afull[sa], (k / kASlots) & 1)) { ok = false; break; }
         if (!mbar_wait_bounded(&S.dfree[sd], ((k / kDSlots) & 1) ^ 1)) { ok = false; break; }
@@ -487,8 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         }
         mma_commit(&S.afree[sa]);
         mma_commit(&S.dfull[sd]);
+        last = k;
       }
-      if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) % kDSlots], ((k - 1) / kDSlots) & 1);
+      // this thread's MMAs are complete before the block tears down TMEM
+      if (last >= 0) (void)mbar_wait_bounded(&S.dfull[last % kDSlots], (last / kDSlots) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else if (warp < kEpiWarp0) {
@@ -522,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       }
       if (btok != t) {
         // the group's previous tile may still be in the tensor core, reading
-        // this buffer: its MMA completes before the buffer is rewritten (that
-        // phase cannot be overtaken: the MMA of tile k + 3 needs this tile)
+        // this buffer: its MMA completes before the buffer is rewritten
         if (k >= 2 && !mbar_wait_warp(&S.afree[(k - 2) % kASlots], ((k - 2) / kASlots) & 1)) {
           ok = false;
           break;
