@@ -405,15 +405,17 @@ def run_ours(args):
     score_ms = [e[1].elapsed_time(e[2]) for e in evs]
     score_ms_avg = sum(score_ms) / len(score_ms)
     roof = roofline(idx, sets, args, score_ms_avg)
-    # an on-chip wait that gave up (200 ms) or another disturbance would show
-    # as a step far slower than its stages timed one by one
+    # an on-chip wait that gave up (200 ms) sets the device error word; any
+    # other disturbance (a profiler serialising the kernels, a neighbour on
+    # the GPU) shows as steps far slower than their stages timed one by one
     staged_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / len(evs)
     err = sets[0][1].device_error(workspace)
-    if err != 0 or ms / args.steps > 3 * staged_ms:
-        sys.stderr.write("timed region disturbed: device error %d, %.3f ms per step against "
-                         "%.3f ms for the stages timed one by one\n"
-                         % (err, ms / args.steps, staged_ms))
+    if err != 0:
+        sys.stderr.write("device error word %d after the timed region: not a valid run\n" % err)
         sys.exit(3)
+    if ms / args.steps > 3 * staged_ms:
+        sys.stderr.write("warning: %.3f ms per step against %.3f ms for the stages timed one by "
+                         "one: the timed region was disturbed\n" % (ms / args.steps, staged_ms))
 
     # e2e: the public call from pinned host buffers, copies inside the timed region
     e2e = run_e2e(args, sets, workspace, stream, world)
