@@ -102,6 +102,33 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
       : "memory");
 }
 
+// An L2 policy that marks lines for early eviction: for data read exactly
+// once (the index-K stream), so that it does not push out what a later
+// kernel reads again (score rows, histograms).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_3d / bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* tmap, int32_t x, int32_t y,
+                                                 int32_t z, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Pulls a kernel-parameter tensor map into the descriptor cache ahead of its
 // first TMA use.
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {

@@ -403,6 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
 
   if (warp == 0) {
     // ---------------- producer
+    // index K is read once: its lines leave L2 first, ahead of the score
+    // rows and histograms the selection reads next
+    const uint64_t kpol = l2_policy_evict_first();
     Cursor c;
     c.init(a, u0);
     int issued = 0;
@@ -441,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           for (int p = 0; p < npages; ++p) {
             const int32_t page = p == 0 ? p0 : p1;
             const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
-            tma_load_3d(&S.k[s][p * a.R * kHeadDim], &tm_page, 0, 0, page, &S.full[s]);
-            bulk_g2s(&S.sc[s][p * a.R * 2], pg + a.s_off, a.R * 2, &S.full[s]);
+            tma_load_3d_hint(&S.k[s][p * a.R * kHeadDim], &tm_page, 0, 0, page, &S.full[s], kpol);
+            bulk_g2s_hint(&S.sc[s][p * a.R * 2], pg + a.s_off, a.R * 2, &S.full[s], kpol);
           }
         }
       } else {
@@ -463,8 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           }
           const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
           const int32_t row = pos0 % a.R;
-          tma_load_3d(&S.k[s][lane * kBlock * kHeadDim], &tm_blk, 0, row, page, &S.full[s]);
-          bulk_g2s(&S.sc[s][lane * kBlock * 2], pg + a.s_off + row * 2, kBlock * 2, &S.full[s]);
+          tma_load_3d_hint(&S.k[s][lane * kBlock * kHeadDim], &tm_blk, 0, row, page, &S.full[s], kpol);
+          bulk_g2s_hint(&S.sc[s][lane * kBlock * 2], pg + a.s_off + row * 2, kBlock * 2, &S.full[s],
+                        kpol);
         }
         c.next(a, u0 + k + 1);
       }
