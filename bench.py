@@ -409,6 +409,9 @@ def run_ours(args):
     # other disturbance (a profiler serialising the kernels, a neighbour on
     # the GPU) shows as steps far slower than their stages timed one by one
     staged_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / len(evs)
+    stage_ms = {"plan": sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs),
+                "score": score_ms_avg,
+                "select": sum(e[2].elapsed_time(e[3]) for e in evs) / len(evs)}
     err = sets[0][1].device_error(workspace)
     if err != 0:
         sys.stderr.write("device error word %d after the timed region: not a valid run\n" % err)
@@ -444,6 +447,7 @@ def run_ours(args):
             "launch": "one CUDA graph per input set holding the whole call",
         },
         "roofline": roof,
+        "stage_ms": stage_ms,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

@@ -349,10 +349,14 @@ struct HistSel {
 };
 static_assert(kHistBins == 4 * kThreads, "one 16-byte histogram load per thread");
 
-__device__ HistSel hist_select(const uint32_t* g, int32_t pinned, int32_t want, Shared& sh) {
+// This thread's 16-byte word of a row's histogram (see hist_select).
+__device__ __forceinline__ uint4 hist_word(const uint32_t* g) {
+  return __ldcg(reinterpret_cast<const uint4*>(g) + (kHistBins / 4 - 1 - static_cast<int>(threadIdx.x)));
+}
+
+__device__ HistSel hist_select_word(const uint4 v, int32_t pinned, int32_t want, Shared& sh) {
   const int tid = threadIdx.x;
   const int q = kHistBins / 4 - 1 - tid;
-  const uint4 v = __ldcg(reinterpret_cast<const uint4*>(g) + q);
   uint32_t c[4] = {v.w, v.z, v.y, v.x};                     // bins 4q+3 .. 4q
   if (pinned >= 0 && (pinned >> 2) == q) c[3 - (pinned & 3)] -= 1u;
   const uint32_t mine = c[0] + c[1] + c[2] + c[3];
@@ -376,6 +380,11 @@ __device__ HistSel hist_select(const uint32_t* g, int32_t pinned, int32_t want, 
   HistSel h{sh.sel[0], sh.sel[1], sh.sel[2], E};
   __syncthreads();
   return h;
+}
+
+__device__ __forceinline__ HistSel hist_select(const uint32_t* g, int32_t pinned, int32_t want,
+                                               Shared& sh) {
+  return hist_select_word(hist_word(g), pinned, want, sh);
 }
 
 // One pass over entries [begin, end) of a row in global memory keeping, in
@@ -451,6 +460,129 @@ __device__ int compact_range(const Row& r, int32_t begin, int32_t end, Keep keep
   }
   __syncthreads();
   return base;
+}
+
+// Ordered compaction of a row of at most kShortChunks * 4096 entries whose
+// threshold bin is known (t_lo: the bin's lowest key). The row is read in
+// chunks of 4096 entries, thread i taking entries 4i..4i+3 of each chunk
+// with one 16-byte load (all issued together); the keys go to `cache`
+// (shared memory, the row's length) and a keep bit per entry stays in a
+// register. The row-order offset of thread i's kept entries in chunk c is
+// (kept entries of chunks before c) + (kept entries of chunk c in threads
+// before i): packed warp scans give all chunks' offsets at once (8-bit
+// fields within a warp, 16-bit fields across warps) with one block barrier.
+// Kept keys go to ckeys[], their ids to cid[] (written only while below
+// cap); returns how many there are.
+constexpr int kShortChunks = 8;
+constexpr int kCandHalf = (kHeadWords + kCandCap - 1024) / 2;   // 5632
+
+template <bool kConsumer>
+__device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint32_t* ckeys,
+                             int32_t* cid, int cap, Shared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t nch = (r.len + 4 * kThreads - 1) / (4 * kThreads);
+  const float4* v4 = reinterpret_cast<const float4*>(r.vals);
+  float4 f[kShortChunks];
+  int32_t blk[kShortChunks];
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const int32_t s0 = c * 4 * kThreads + 4 * tid;
+    f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    blk[c] = 0;
+    if (c < nch && s0 < r.len) {
+      f[c] = __ldcg(v4 + (s0 >> 2));
+      if (kConsumer) blk[c] = __ldcg(r.blocks + (s0 >> 3));
+    }
+  }
+  const auto id_of = [&](int c, int j) {
+    const int32_t s = c * 4 * kThreads + 4 * tid + j;
+    return kConsumer ? blk[c] * kBlock + (s & (kBlock - 1)) : s;
+  };
+  // keys to the cache, keep bits to `keep` (bit 4c + j), counts per chunk
+  // as 8-bit fields (chunks 0-3 in mine[0], 4-7 in mine[1])
+  uint32_t keep = 0u, mine[2] = {0u, 0u};
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const int32_t s0 = c * 4 * kThreads + 4 * tid;
+    if (c < nch && s0 < r.len) {
+      const uint4 k4 = make_uint4(order_key(f[c].x), order_key(f[c].y), order_key(f[c].z),
+                                  order_key(f[c].w));
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      uint32_t n = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = s0 + j < r.len && (!kConsumer || id_of(c, j) < r.V) && kk[j] >= t_lo;
+        keep |= ok ? (1u << (4 * c + j)) : 0u;
+        n += ok ? 1u : 0u;
+      }
+      *reinterpret_cast<uint4*>(cache + s0) = k4;      // s0 + 3 < the row's padded length
+      mine[c >> 2] |= n << (8 * (c & 3));
+    }
+  }
+  // within the warp: at most 32 x 4 per field
+  uint32_t incl[2] = {mine[0], mine[1]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl[h], o);
+      if (lane >= o) incl[h] += y;
+    }
+  }
+  __syncthreads();                       // earlier users of chunk_w are done
+  if (lane == 31) {
+    sh.chunk_w[0][warp] = static_cast<int>(incl[0]);
+    sh.chunk_w[1][warp] = static_cast<int>(incl[1]);
+  }
+  __syncthreads();
+  // across warps: lane l holds warp l's totals, widened to 16-bit fields
+  uint32_t wide[4];
+  {
+    const uint32_t lo = static_cast<uint32_t>(sh.chunk_w[0][lane]);
+    const uint32_t hi = static_cast<uint32_t>(sh.chunk_w[1][lane]);
+    wide[0] = (lo & 0xffu) | (((lo >> 8) & 0xffu) << 16);
+    wide[1] = ((lo >> 16) & 0xffu) | ((lo >> 24) << 16);
+    wide[2] = (hi & 0xffu) | (((hi >> 8) & 0xffu) << 16);
+    wide[3] = ((hi >> 16) & 0xffu) | ((hi >> 24) << 16);
+  }
+  uint32_t wincl[4] = {wide[0], wide[1], wide[2], wide[3]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wincl[h], o);
+      if (lane >= o) wincl[h] += y;
+    }
+  }
+  int total = 0;
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const uint32_t shift = 16 * (c & 1);
+    const int tot_c = static_cast<int>((__shfl_sync(0xffffffffu, wincl[c >> 1], 31) >> shift) & 0xffffu);
+    const int bw = static_cast<int>(
+        ((__shfl_sync(0xffffffffu, wincl[c >> 1] - wide[c >> 1], warp) >> shift) & 0xffffu));
+    const int bt = static_cast<int>((((incl[c >> 2] - mine[c >> 2]) >> (8 * (c & 3))) & 0xffu));
+    int at = total + bw + bt;
+    total += tot_c;
+    const uint32_t bits = (keep >> (4 * c)) & 0xfu;
+    if (bits) {
+      const int32_t s0 = c * 4 * kThreads + 4 * tid;
+      const uint4 k4 = *reinterpret_cast<const uint4*>(cache + s0);
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if ((bits >> j) & 1u) {
+          if (at < cap) {
+            ckeys[at] = kk[j];
+            cid[at] = id_of(c, j);
+          }
+          ++at;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  return total;
 }
 
 // Exact threshold among n candidate keys (any order) whose top 12 bits
@@ -850,6 +982,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
   const int32_t width = blocks ? a.C : a.topk;
   int32_t* out = blocks ? a.cand_out + static_cast<int64_t>(t) * a.C
                         : a.idx_out + static_cast<int64_t>(t) * a.topk;
+  // the row's histogram word is requested before the row's metadata, so the
+  // two round trips overlap
+  const uint4 fh_word = a.fhist != nullptr
+                            ? hist_word(a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins)
+                            : make_uint4(0u, 0u, 0u, 0u);
   int32_t want;
   Row r = row_of(a, t, which, want);
   int32_t written = 0;
@@ -892,38 +1029,49 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
       }
       if (!done) written = select_ascending(r, want, out, sh, nullptr);
     } else if (a.fhist != nullptr) {
-      // the score stage's histogram gives the threshold bin up front: one
-      // pass caches the row, the entries at or above it are compacted in row
-      // order and ranked exactly
+      // the score stage's histogram gives the threshold bin up front: the
+      // entries at or above it are compacted in row order in one pass over
+      // the row and ranked exactly
       int32_t pinned = -1;
       if (blocks) {
         const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
         pinned = static_cast<int32_t>(
             hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
       }
-      const HistSel hs = hist_select(a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins,
-                                     pinned, want, sh);
-      // candidates: keys to the key region, ids to the scratch head, then
-      // 1024 words of digit histogram
-      const int cap = min(region, kHeadWords + kCandCap - 1024);
+      const HistSel hs = hist_select_word(fh_word, pinned, want, sh);
+      // candidates: a row of 2 to kShortChunks chunks of 4096 entries caches
+      // its keys in the key region and puts the candidates' keys and ids in
+      // the scratch area (kCandHalf words each); a one-chunk or a longer row
+      // puts keys in the key region and ids in the scratch area (one chunk
+      // needs a single barrier that way). The scratch area's last 1024 words
+      // hold the refine's digit histogram.
+      const bool short_row = r.len > 4 * kThreads && r.len <= kShortChunks * 4 * kThreads;
+      uint32_t* ckeys = short_row ? scratch : keys;
+      int32_t* cid = reinterpret_cast<int32_t*>(short_row ? scratch + kCandHalf : scratch);
+      const int cap = short_row ? kCandHalf : min(region, kHeadWords + kCandCap - 1024);
       const uint32_t n = hs.above + hs.cbin;
       bool done = false;
       if (hs.E <= static_cast<uint32_t>(want)) {
         written = ordered_output(r, 0u, 0, out, sh);        // every eligible entry, in order
         done = true;
       } else if (n <= static_cast<uint32_t>(cap)) {
-        int32_t* cid = reinterpret_cast<int32_t*>(scratch);
         const uint32_t t_lo = hs.sel << (32 - kHistBits);
-        const auto keep = [t_lo](uint32_t k) { return k >= t_lo; };
-        const int got = r.consumer ? compact_range<true>(r, 0, r.len, keep, keys, cid, cap, sh)
-                                   : compact_range<false>(r, 0, r.len, keep, keys, cid, cap, sh);
+        int got;
+        if (short_row) {
+          got = r.consumer ? compact_short<true>(r, t_lo, keys, ckeys, cid, cap, sh)
+                           : compact_short<false>(r, t_lo, keys, ckeys, cid, cap, sh);
+        } else {
+          const auto keep = [t_lo](uint32_t k) { return k >= t_lo; };
+          got = r.consumer ? compact_range<true>(r, 0, r.len, keep, ckeys, cid, cap, sh)
+                           : compact_range<false>(r, 0, r.len, keep, ckeys, cid, cap, sh);
+        }
         if (got == static_cast<int>(n)) {
           uint32_t thr;
           int32_t need_eq;
-          refine_threshold(keys, got, hs.sel, want - static_cast<int32_t>(hs.above),
+          refine_threshold(ckeys, got, hs.sel, want - static_cast<int32_t>(hs.above),
                            scratch + kHeadWords + kCandCap - 1024, sh, thr, need_eq);
           Row cr = r;
-          cr.cached = keys;
+          cr.cached = ckeys;
           cr.ids = cid;
           cr.idx = nullptr;
           cr.len = got;
