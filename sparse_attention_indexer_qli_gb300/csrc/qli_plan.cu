@@ -197,6 +197,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   }
 }
 
+// Consumer mode: the last CTA to finish turns the per-token candidate counts
+// into the stream path's tile prefix (token t owns ceil(count/16) tiles of
+// 128 candidate positions).
+template <int NT>
+__device__ void consumer_units(const DevArgs& a) {
+  __shared__ bool s_last;
+  __threadfence();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (s_last && a.stream_path) {
+    __threadfence();
+    cta_scan_store<NT>(
+        a.T, [&](int32_t i) { return (__ldcg(&a.cand_cnt[i]) + kTile / kBlock - 1) / (kTile / kBlock); },
+        a.unit_start);
+  }
+}
+
 // Consumer mode, one CTA per token: keep the candidate IDs that name a block
 // with at least one visible position (0 <= id < ceil(V/8)), sort them
 // ascending and drop duplicates. The guide gives candidates as a padded list
@@ -259,19 +276,63 @@ __global__ void __launch_bounds__(kPrepThreads) cand_prep_kernel(DevArgs a, int3
     if (keys[k] != INT_MAX && (k == 0 || keys[k] != keys[k - 1])) out[pos++] = keys[k];
   if (tid == 0) a.cand_cnt[t] = total;
 
-  // the last CTA to finish turns the counts into the stream path's tile
-  // prefix: token t owns ceil(count/16) tiles of 128 candidate positions
-  __shared__ bool s_last;
-  __threadfence();
-  if (tid == 0) s_last = atomicAdd(a.counter, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (s_last && a.stream_path) {
-    __threadfence();
-    cta_scan_store<kPrepThreads>(
-        a.T, [&](int32_t i) { return (__ldcg(&a.cand_cnt[i]) + kTile / kBlock - 1) / (kTile / kBlock); },
-        a.unit_start);
-  }
+  consumer_units<kPrepThreads>(a);
 }
+
+// Consumer mode, the same result for contexts of up to kBitmapWords * 32
+// candidate blocks: one CTA per token marks the valid IDs in a bitmap of the
+// token's visible blocks (shared memory), then writes the set bits in
+// ascending order (one block scan of the per-thread bit counts): sorted,
+// without duplicates, in a few barriers.
+constexpr int kBitmapThreads = 512;
+constexpr int kBitmapWords = 16384;                  // 64 KB: 524288 blocks
+
+__global__ void __launch_bounds__(kBitmapThreads) cand_bitmap_kernel(DevArgs a, int32_t words) {
+  extern __shared__ uint32_t bm[];
+  __shared__ int32_t warp_sum[kBitmapThreads / 32];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t V = a.tok_V[t];
+  const int32_t nb = (V + kBlock - 1) / kBlock;
+  const int32_t nw = min((nb + 31) >> 5, words);
+  for (int i = tid; i < nw; i += kBitmapThreads) bm[i] = 0u;
+  __syncthreads();
+  const int32_t* row = a.cand_in + static_cast<int64_t>(t) * a.C;
+  for (int k = tid; k < a.C; k += kBitmapThreads) {
+    const int32_t id = row[k];
+    if (id >= 0 && id < nb && (id >> 5) < nw) atomicOr(&bm[id >> 5], 1u << (id & 31));
+  }
+  __syncthreads();
+  // thread i owns words [i * per, (i + 1) * per)
+  const int32_t per = (nw + kBitmapThreads - 1) / kBitmapThreads;
+  const int32_t w0 = tid * per, w1 = min(nw, w0 + per);
+  int cnt = 0;
+  for (int32_t w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+  int incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < kBitmapThreads / 32; ++w) {
+    if (w < warp) base += warp_sum[w];
+    total += warp_sum[w];
+  }
+  int pos = base + incl - cnt;
+  int32_t* out = a.cand_list + static_cast<int64_t>(t) * a.C;
+  for (int32_t w = w0; w < w1; ++w) {
+    uint32_t bits = bm[w];
+    while (bits) {
+      out[pos++] = (w << 5) + (__ffs(bits) - 1);
+      bits &= bits - 1u;
+    }
+  }
+  if (tid == 0) a.cand_cnt[t] = total;
+  consumer_units<kBitmapThreads>(a);
+}
+
+std::atomic<uint64_t> g_smem_cand_bitmap{0};
 
 }  // namespace
 
@@ -283,10 +344,22 @@ cudaError_t launch_plan(const DevArgs& d, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (d.mode == QLI_CAND_CONSUMER && d.T > 0) {
-    int32_t pow2 = 1;
-    while (pow2 < d.C) pow2 <<= 1;
-    if (pow2 < kPrepThreads) pow2 = kPrepThreads;
-    cand_prep_kernel<<<d.T, kPrepThreads, 0, s>>>(d, pow2);
+    // the bitmap covers every block a token can see: ceil(cap / 8) bits
+    const int64_t words = (static_cast<int64_t>(d.cap) / kBlock + 1 + 31) / 32;
+    if (words <= kBitmapWords) {
+      const int w = static_cast<int>(words);
+      if (4 * w > 48 * 1024) {
+        e = ensure_smem_limit(reinterpret_cast<const void*>(cand_bitmap_kernel), 4 * kBitmapWords,
+                              g_smem_cand_bitmap);
+        if (e != cudaSuccess) return e;
+      }
+      cand_bitmap_kernel<<<d.T, kBitmapThreads, 4 * w, s>>>(d, w);
+    } else {
+      int32_t pow2 = 1;
+      while (pow2 < d.C) pow2 <<= 1;
+      if (pow2 < kPrepThreads) pow2 = kPrepThreads;
+      cand_prep_kernel<<<d.T, kPrepThreads, 0, s>>>(d, pow2);
+    }
     e = cudaGetLastError();
   }
   return e;
