@@ -23,8 +23,8 @@ constexpr int kMaxTopK = 2048;
 constexpr int kMaxCand = 2048;
 constexpr int kPrefillUnitTiles = 64;   // position tiles per prefill work unit
 constexpr int kSmemKeys = 44 * 1024;    // keys one selection CTA holds in shared memory
-constexpr int kLongChunk = 16384;       // row entries per CTA in the long-row passes
-constexpr int kLongChunkCap = 2048;     // candidates kept per chunk
+constexpr int kLongChunk = 32768;       // row entries per CTA in the long-row passes
+constexpr int kLongChunkCap = 4096;     // candidates kept per chunk
 constexpr int kLongCandCap = 16384;     // candidates kept per long row
 
 // Everything a kernel needs, passed by value (a few hundred bytes).

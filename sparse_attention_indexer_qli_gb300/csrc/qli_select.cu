@@ -471,14 +471,15 @@ __device__ int compact_range(const Row& r, int32_t begin, int32_t end, Keep keep
 // (kept entries of chunks before c) + (kept entries of chunk c in threads
 // before i): packed warp scans give all chunks' offsets at once (8-bit
 // fields within a warp, 16-bit fields across warps) with one block barrier.
-// Kept keys go to ckeys[], their ids to cid[] (written only while below
-// cap); returns how many there are.
+// Kept keys go to ckeys[], their ids to cid[] (shared or global memory,
+// written only while below cap); a dense row's ids are id_base + entry.
+// Returns how many there are.
 constexpr int kShortChunks = 8;
 constexpr int kCandHalf = (kHeadWords + kCandCap - 1024) / 2;   // 5632
 
 template <bool kConsumer>
 __device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint32_t* ckeys,
-                             int32_t* cid, int cap, Shared& sh) {
+                             int32_t* cid, int cap, Shared& sh, int32_t id_base = 0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t nch = (r.len + 4 * kThreads - 1) / (4 * kThreads);
   const float4* v4 = reinterpret_cast<const float4*>(r.vals);
@@ -496,7 +497,7 @@ __device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint3
   }
   const auto id_of = [&](int c, int j) {
     const int32_t s = c * 4 * kThreads + 4 * tid + j;
-    return kConsumer ? blk[c] * kBlock + (s & (kBlock - 1)) : s;
+    return kConsumer ? blk[c] * kBlock + (s & (kBlock - 1)) : id_base + s;
   };
   // keys to the cache, keep bits to `keep` (bit 4c + j), counts per chunk
   // as 8-bit fields (chunks 0-3 in mine[0], 4-7 in mine[1])
@@ -780,7 +781,10 @@ __global__ void __launch_bounds__(kThreads) lhist_kernel(DevArgs a) {
     if (hist[i]) atomicAdd(&g[i], hist[i]);
 }
 
+// Dynamic shared memory: kLongChunk words caching the chunk's keys.
+static_assert(kLongChunk <= kShortChunks * 4 * kThreads, "a long-row chunk fits one ordered compaction");
 __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
+  extern __shared__ uint32_t lcache[];
   pdl_trigger();
   pdl_wait();
   __shared__ Shared sh;
@@ -807,9 +811,14 @@ __global__ void __launch_bounds__(kThreads) lcompact_kernel(DevArgs a) {
     }
     const HistSel hs = hist_select(a.fhist + row * kHistBins, pinned, want, sh);
     const uint32_t t_lo = hs.E > static_cast<uint32_t>(want) ? hs.sel << (32 - kHistBits) : 1u;
-    const auto keep = [t_lo](uint32_t k) { return k >= t_lo; };
-    total = r.consumer ? compact_range<true>(r, lo, hi, keep, okey, oid, kLongChunkCap, sh)
-                       : compact_range<false>(r, lo, hi, keep, okey, oid, kLongChunkCap, sh);
+    // the chunk as a row of its own (ids offset by its start): one ordered
+    // compaction with a single barrier, keys cached in shared memory
+    Row rc = r;
+    rc.vals = r.vals + lo;
+    if (r.consumer) rc.blocks = r.blocks + lo / kBlock;
+    rc.len = hi - lo;
+    total = r.consumer ? compact_short<true>(rc, t_lo, lcache, okey, oid, kLongChunkCap, sh)
+                       : compact_short<false>(rc, t_lo, lcache, okey, oid, kLongChunkCap, sh, lo);
   } else {
     // the 12 bits below the row's common prefix (lstat / lhist): the digit
     // holding the want-th best entry (0: keep every eligible entry)
@@ -1112,11 +1121,14 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
       lstat_kernel<<<g, kThreads, 0, s>>>(d);
       lhist_kernel<<<g, kThreads, 0, s>>>(d);
     }
+    static std::atomic<uint64_t> lc_done{0};
+    e = ensure_smem_limit(reinterpret_cast<const void*>(lcompact_kernel), 4 * kLongChunk, lc_done);
+    if (e != cudaSuccess) return e;
     if (d.fhist != nullptr) {
-      e = launch_pdl(lcompact_kernel, g, dim3(kThreads), 0, s, d);
+      e = launch_pdl(lcompact_kernel, g, dim3(kThreads), 4 * kLongChunk, s, d);
       if (e != cudaSuccess) return e;
     } else {
-      lcompact_kernel<<<g, kThreads, 0, s>>>(d);
+      lcompact_kernel<<<g, kThreads, 4 * kLongChunk, s>>>(d);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
