@@ -38,7 +38,7 @@ constexpr uint32_t kTmemCols = 512;
 struct Smem {
   uint8_t a[kStages][kABytes];   // 1024-aligned
   uint8_t b[kBBytes];            // 1024-aligned
-  __half wq[2][kMaxMmaN];        // by unit parity: a warp may still sum the previous unit
+  alignas(16) __half wq[2][kMaxMmaN];   // by unit parity: a warp may still sum the previous unit
   uint64_t full[kStages], empty[kStages], dfull[2], dempty[2], bfull, bempty;
   uint32_t tmem_base;
 };
@@ -267,7 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       const int32_t V1 = has1 ? a.tok_V[x.t0 + g1] : 0;
       const uint32_t c0 = static_cast<uint32_t>(g0 * a.N);
       const uint32_t c1 = wide ? c0 + 32 : static_cast<uint32_t>(g1 * a.N);
-      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[n & 1][0]);
+      // this warp's tokens' w * q_scale pairs, read 16 bytes (four head pairs)
+      // at a time from a base fixed for the unit
+      const uint4* w0 = reinterpret_cast<const uint4*>(&S.wq[n & 1][c0]);
+      const uint4* w1 = reinterpret_cast<const uint4*>(&S.wq[n & 1][c1]);
       for (int i = 0; i < x.ntiles; ++i, ++k) {
         const int ds = k & 1;
         if (!mbar_wait_warp(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
@@ -286,22 +289,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         float acc0 = 0.0f, acc1 = 0.0f;
         if (has0) {
 #pragma unroll
-          for (int kk = 0; kk < 32; kk += 2)
-            acc0 = head_pair_acc(acc0, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]),
-                                 wq2[(c0 + kk) >> 1]);
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = w0[q];
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int kk = 8 * q + 2 * i;
+              acc0 = head_pair_acc(acc0, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]), wv[i]);
+            }
+          }
         }
         if (has1) {
-          if (wide) {   // heads 32-63 of the same token continue its chain
+          float acc = wide ? acc0 : acc1;   // wide: heads 32-63 of the same token continue its chain
 #pragma unroll
-            for (int kk = 0; kk < 32; kk += 2)
-              acc0 = head_pair_acc(acc0, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
-                                   wq2[(c1 + kk) >> 1]);
-          } else {
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = w1[q];
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int kk = 0; kk < 32; kk += 2)
-              acc1 = head_pair_acc(acc1, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
-                                   wq2[(c1 + kk) >> 1]);
+            for (int i = 0; i < 4; ++i) {
+              const int kk = 8 * q + 2 * i;
+              acc = head_pair_acc(acc, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]), wv[i]);
+            }
           }
+          if (wide) acc0 = acc; else acc1 = acc;
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {

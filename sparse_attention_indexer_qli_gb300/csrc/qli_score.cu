@@ -301,7 +301,7 @@ struct Smem {
   uint8_t k[kKStages][kKBytes];                      // 1024-aligned (offset 0)
   uint8_t b[2][kBBytes];                             // 1024-aligned; one per converter group
   uint8_t sc[kKStages][kSBytes];
-  __half wq[kSlots][64];
+  alignas(16) __half wq[kSlots][64];
   float ks[kSlots][kTile];
   uint64_t full[kKStages], empty[kKStages];
   uint64_t afull[kASlots], afree[kASlots], dfull[kDSlots], dfree[kDSlots];
@@ -633,16 +633,28 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dfree[sd]);
-      const uint32_t* wq2 = reinterpret_cast<const uint32_t*>(&S.wq[slot][0]);
+      // w * q_scale pairs, four at a time (16-byte shared loads)
+      const uint4* wq4 = reinterpret_cast<const uint4*>(&S.wq[slot][0]);
       float acc = 0.0f;
 #pragma unroll
-      for (int kk = 0; kk < 32; kk += 2)
-        acc = head_pair_acc(acc, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]), wq2[kk >> 1]);
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = wq4[q];
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          acc = head_pair_acc(acc, __uint_as_float(r0[8 * q + 2 * i]),
+                              __uint_as_float(r0[8 * q + 2 * i + 1]), wv[i]);
+      }
       if (a.N == 64) {
 #pragma unroll
-        for (int kk = 0; kk < 32; kk += 2)
-          acc = head_pair_acc(acc, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]),
-                              wq2[(32 + kk) >> 1]);
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = wq4[4 + q];
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            acc = head_pair_acc(acc, __uint_as_float(r1[8 * q + 2 * i]),
+                                __uint_as_float(r1[8 * q + 2 * i + 1]), wv[i]);
+        }
       }
       const float score = __fmul_rn(acc, S.ks[slot][row]);
 
