@@ -271,64 +271,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       // at a time from a base fixed for the unit
       const uint4* w0 = reinterpret_cast<const uint4*>(&S.wq[n & 1][c0]);
       const uint4* w1 = reinterpret_cast<const uint4*>(&S.wq[n & 1][c1]);
+      // per-unit row pointers of the (up to two) tokens this warp scores
+      const int32_t ta = x.t0 + g0, tb = x.t0 + g1;
+      float* const srow0 = a.scores + static_cast<int64_t>(ta) * a.Lrow;
+      float* const srow1 = a.scores + static_cast<int64_t>(tb) * a.Lrow;
+      float* const brow0 = a.bscores + static_cast<int64_t>(ta) * a.Brow;
+      float* const brow1 = a.bscores + static_cast<int64_t>(tb) * a.Brow;
+      const float* const ksrow = a.ks32 + static_cast<int64_t>(x.b) * a.kstride;
+      const bool source = a.mode == QLI_CAND_SOURCE;
+      // one golden chain over 32 heads (a 32-column accumulator half)
+      const auto chain = [&](float acc, const uint32_t (&r)[32], const uint4* w) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 wq = w[q];
+          const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii)
+            acc = head_pair_acc(acc, __uint_as_float(r[8 * q + 2 * ii]),
+                                __uint_as_float(r[8 * q + 2 * ii + 1]), wv[ii]);
+        }
+        return acc;
+      };
+      const auto emit = [&](float acc, float ks, int32_t pos, int32_t V, float* srow, float* brow) {
+        const float score = __fmul_rn(acc, ks);
+        const bool elig = pos < V;
+        if (elig) srow[pos] = score;
+        if (source) {
+          float m = elig ? score : -INFINITY;
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          if ((row & (kBlock - 1)) == 0 && elig) brow[pos / kBlock] = m;
+        }
+      };
       for (int i = 0; i < x.ntiles; ++i, ++k) {
         const int ds = k & 1;
         if (!mbar_wait_warp(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const int32_t pos = (x.tile0 + i) * kTile + row;
-        const float ks = a.ks32[static_cast<int64_t>(x.b) * a.kstride + pos];
-        uint32_t r0[32], r1[32];
+        const float ks = ksrow[pos];
         const uint32_t base = tmem + lane_addr + ds * 256;
-        if (has0) tmem_ld_32x32b_x32(base + c0, r0);     // uniform across the warp
-        if (has1) tmem_ld_32x32b_x32(base + c1, r1);
-        tmem_ld_wait();
+        // the two 32-column halves one after the other (32 live registers):
+        // heads 0-31 and 32-63 of one token, or two tokens of 32 heads
+        uint32_t r[32];
+        float acc0 = 0.0f;
+        if (has0) {                           // uniform across the warp
+          tmem_ld_32x32b_x32(base + c0, r);
+          tmem_ld_wait();
+          acc0 = chain(0.0f, r, w0);
+        }
+        if (has1) {
+          tmem_ld_32x32b_x32(base + c1, r);
+          tmem_ld_wait();
+        }
         // the accumulator is in registers: hand the TMEM stage back now
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.dempty[ds]);
-        float acc0 = 0.0f, acc1 = 0.0f;
-        if (has0) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 w = w0[q];
-            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int kk = 8 * q + 2 * i;
-              acc0 = head_pair_acc(acc0, __uint_as_float(r0[kk]), __uint_as_float(r0[kk + 1]), wv[i]);
-            }
-          }
-        }
-        if (has1) {
-          float acc = wide ? acc0 : acc1;   // wide: heads 32-63 of the same token continue its chain
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 w = w1[q];
-            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int kk = 8 * q + 2 * i;
-              acc = head_pair_acc(acc, __uint_as_float(r1[kk]), __uint_as_float(r1[kk + 1]), wv[i]);
-            }
-          }
-          if (wide) acc0 = acc; else acc1 = acc;
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const bool has = j == 0 ? has0 : (!wide && has1);
-          if (!has) continue;                 // uniform across the warp
-          const int32_t t = x.t0 + (j == 0 ? g0 : g1);
-          const float score = __fmul_rn(j == 0 ? acc0 : acc1, ks);
-          const bool elig = pos < (j == 0 ? V0 : V1);
-          if (elig) a.scores[static_cast<int64_t>(t) * a.Lrow + pos] = score;
-          if (a.mode == QLI_CAND_SOURCE) {
-            float m = elig ? score : -INFINITY;
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            if ((row & (kBlock - 1)) == 0 && elig)
-              a.bscores[static_cast<int64_t>(t) * a.Brow + pos / kBlock] = m;
-          }
+        if (wide) {
+          if (has0) emit(chain(acc0, r, w1), ks, pos, V0, srow0, brow0);
+        } else {
+          if (has0) emit(acc0, ks, pos, V0, srow0, brow0);
+          if (has1) emit(chain(0.0f, r, w1), ks, pos, V1, srow1, brow1);
         }
       }
     }
