@@ -586,6 +586,129 @@ __device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint3
   return total;
 }
 
+// For a dense row of up to 32K entries without a score-stage histogram: one
+// coalesced pass (chunks of 4096 entries, thread i taking entries 4i..4i+3
+// of each) caches the keys in `cache` (shared memory) and counts their top
+// 12 bits in `hist` (4096 words of shared memory, zeroed here).
+__device__ void cache_and_count(const Row& r, uint32_t* cache, uint32_t* hist, Shared& sh) {
+  const int tid = threadIdx.x;
+  reinterpret_cast<uint4*>(hist)[tid] = make_uint4(0u, 0u, 0u, 0u);    // 4096 = 4 x kThreads
+  const int32_t nch = (r.len + 4 * kThreads - 1) / (4 * kThreads);
+  const float4* v4 = reinterpret_cast<const float4*>(r.vals);
+  float4 f[kShortChunks];
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const int32_t s0 = c * 4 * kThreads + 4 * tid;
+    f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nch && s0 < r.len) f[c] = __ldcg(v4 + (s0 >> 2));
+  }
+  __syncthreads();                       // the histogram is zero
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const int32_t s0 = c * 4 * kThreads + 4 * tid;
+    if (c < nch && s0 < r.len) {
+      const uint4 k4 = make_uint4(order_key(f[c].x), order_key(f[c].y), order_key(f[c].z),
+                                  order_key(f[c].w));
+      *reinterpret_cast<uint4*>(cache + s0) = k4;     // s0 + 3 < the row's padded length
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (s0 + j < r.len) atomicAdd(&hist[hist_bin(kk[j])], 1u);
+    }
+  }
+  __syncthreads();
+  (void)sh;
+}
+
+// Ordered compaction of a dense row whose keys sit in `cache` (see
+// cache_and_count): the entries with key >= t_lo, in row order, keys to
+// ckeys[] and positions to cid[] (written only while below cap), placed by
+// packed warp scans with one block barrier. Returns how many there are.
+__device__ int compact_cached(const Row& r, uint32_t t_lo, const uint32_t* cache, uint32_t* ckeys,
+                              int32_t* cid, int cap, Shared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t nch = (r.len + 4 * kThreads - 1) / (4 * kThreads);
+  uint32_t keep = 0u, mine[2] = {0u, 0u};
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const int32_t s0 = c * 4 * kThreads + 4 * tid;
+    if (c < nch && s0 < r.len) {
+      const uint4 k4 = *reinterpret_cast<const uint4*>(cache + s0);
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      uint32_t n = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = s0 + j < r.len && kk[j] >= t_lo;
+        keep |= ok ? (1u << (4 * c + j)) : 0u;
+        n += ok ? 1u : 0u;
+      }
+      mine[c >> 2] |= n << (8 * (c & 3));
+    }
+  }
+  uint32_t incl[2] = {mine[0], mine[1]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl[h], o);
+      if (lane >= o) incl[h] += y;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) {
+    sh.chunk_w[0][warp] = static_cast<int>(incl[0]);
+    sh.chunk_w[1][warp] = static_cast<int>(incl[1]);
+  }
+  __syncthreads();
+  uint32_t wide[4];
+  {
+    const uint32_t lo = static_cast<uint32_t>(sh.chunk_w[0][lane]);
+    const uint32_t hi = static_cast<uint32_t>(sh.chunk_w[1][lane]);
+    wide[0] = (lo & 0xffu) | (((lo >> 8) & 0xffu) << 16);
+    wide[1] = ((lo >> 16) & 0xffu) | ((lo >> 24) << 16);
+    wide[2] = (hi & 0xffu) | (((hi >> 8) & 0xffu) << 16);
+    wide[3] = ((hi >> 16) & 0xffu) | ((hi >> 24) << 16);
+  }
+  uint32_t wincl[4] = {wide[0], wide[1], wide[2], wide[3]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wincl[h], o);
+      if (lane >= o) wincl[h] += y;
+    }
+  }
+  int total = 0;
+#pragma unroll
+  for (int c = 0; c < kShortChunks; ++c) {
+    const uint32_t shift = 16 * (c & 1);
+    const int tot_c = static_cast<int>((__shfl_sync(0xffffffffu, wincl[c >> 1], 31) >> shift) & 0xffffu);
+    const int bw = static_cast<int>(
+        ((__shfl_sync(0xffffffffu, wincl[c >> 1] - wide[c >> 1], warp) >> shift) & 0xffffu));
+    const int bt = static_cast<int>((((incl[c >> 2] - mine[c >> 2]) >> (8 * (c & 3))) & 0xffu));
+    int at = total + bw + bt;
+    total += tot_c;
+    const uint32_t bits = (keep >> (4 * c)) & 0xfu;
+    if (bits) {
+      const int32_t s0 = c * 4 * kThreads + 4 * tid;
+      const uint4 k4 = *reinterpret_cast<const uint4*>(cache + s0);
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if ((bits >> j) & 1u) {
+          if (at < cap) {
+            ckeys[at] = kk[j];
+            cid[at] = s0 + j;
+          }
+          ++at;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
 // Exact threshold among n candidate keys (any order) whose top 12 bits
 // already single out bin `sel`: the k-th largest key of that bin (k >= 1),
 // in the convention of ordered_output (take keys > thr and the first
@@ -1095,9 +1218,41 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
         written = select_ascending(r, want, out, sh, scratch, &st);
       }
     } else {
-      bool cached;
-      const Stats st = cache_keys(r, keys, key_cap, sh, cached);
-      written = select_ascending(r, want, out, sh, scratch, &st);
+      bool done = false;
+      if (!r.consumer && r.len > 1024 && r.len <= kShortChunks * 4 * kThreads) {
+        // no score-stage histogram: count the row's top-12-bit bins here, in
+        // the same pass that caches its keys. Scratch: the histogram (later
+        // the refine's digit histogram), then candidate keys and positions.
+        uint32_t* hist = scratch;
+        uint32_t* ckeys = scratch + kHistBins;
+        constexpr int kCap = (kHeadWords + kCandCap - kHistBins) / 2;
+        int32_t* cid = reinterpret_cast<int32_t*>(ckeys + kCap);
+        cache_and_count(r, keys, hist, sh);
+        const HistSel hs = hist_select_word(
+            reinterpret_cast<const uint4*>(hist)[kHistBins / 4 - 1 - tid], -1, want, sh);
+        const uint32_t n = hs.above + hs.cbin;
+        if (hs.E > static_cast<uint32_t>(want) && n <= static_cast<uint32_t>(kCap)) {
+          const int got = compact_cached(r, hs.sel << (32 - kHistBits), keys, ckeys, cid, kCap, sh);
+          if (got == static_cast<int>(n)) {
+            uint32_t thr;
+            int32_t need_eq;
+            refine_threshold(ckeys, got, hs.sel, want - static_cast<int32_t>(hs.above), hist, sh,
+                             thr, need_eq);
+            Row cr = r;
+            cr.cached = ckeys;
+            cr.ids = cid;
+            cr.idx = nullptr;
+            cr.len = got;
+            written = ordered_output(cr, thr, need_eq, out, sh);
+            done = true;
+          }
+        }
+      }
+      if (!done) {
+        bool cached;
+        const Stats st = cache_keys(r, keys, key_cap, sh, cached);
+        written = select_ascending(r, want, out, sh, scratch, &st);
+      }
     }
     if (blocks) {                      // the pinned last visible block
       if (tid == 0) out[written] = (r.V + kBlock - 1) / kBlock - 1;
