@@ -456,44 +456,66 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+def _packed(tensors, device=None):
+    """One buffer holding the given tensors at 256-byte aligned offsets:
+    pinned host memory (device None) or device memory. Returns the buffer and
+    the tensors as views into it."""
+    import torch
+    offs, off = [], 0
+    for t in tensors:
+        if t is None:
+            offs.append(None)
+            continue
+        off = (off + 255) & ~255
+        offs.append(off)
+        off += t.numel() * t.element_size()
+    buf = (torch.empty(max(off, 1), dtype=torch.uint8, pin_memory=True) if device is None
+           else torch.empty(max(off, 1), dtype=torch.uint8, device=device))
+    views = []
+    for t, o in zip(tensors, offs):
+        if t is None:
+            views.append(None)
+            continue
+        n = t.numel() * t.element_size()
+        views.append(buf[o:o + n].view(t.dtype).view(t.shape))
+    return buf, views
+
+
 def run_e2e(args, sets, workspace, stream, world):
+    """The public call from host buffers: each step copies its inputs from
+    one pinned host buffer to one device buffer (the call's inputs are views
+    into it), runs the call, and copies its outputs (one device buffer) back
+    to pinned host memory, all inside the timed region."""
     import torch
 
     from sparse_attention_indexer_qli_gb300 import qli
     nsets = len(sets)
-    host, dev, calls = [], [], []
+    hbufs, dbufs, obufs, ohost, calls = [], [], [], [], []
     for case, call, _ in sets:
-        names = ["q", "cu_seqlens_q", "k_lens", "residual", "block_table", "head_weights",
-                 "q_scale", "cand_in"]
-        kw = {}
-        h = {}
-        for n, t in zip(names, call.keep[:3] + call.keep[3:4] + call.keep[5:9]):
-            if t is None:
-                kw[n] = None
-                continue
-            h[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
-            kw[n] = torch.empty_like(t)
-        host.append(h)
-        dev.append(kw)
-        c = qli.Call(kw["q"], kw["cu_seqlens_q"], kw["k_lens"], kw["residual"], call.keep[4],
-                     kw["block_table"], kw["head_weights"], kw["q_scale"], ratio=case.ratio,
+        ins = list(call.keep[:4]) + list(call.keep[5:9])   # everything but the page pool
+        hb, hviews = _packed([None if t is None else t.cpu() for t in ins])
+        for hv, t in zip(hviews, ins):
+            if t is not None:
+                hv.copy_(t.cpu())
+        db, dv = _packed(ins, device="cuda")
+        q, cu, kl, res, bt, hw, qs, cin = dv
+        ob, (idx_o, cand_o) = _packed([call.indices, call.cand], device="cuda")
+        c = qli.Call(q, cu, kl, res, call.keep[4], bt, hw, qs, ratio=case.ratio,
                      rows_per_page=case.rows_per_page, page_stride=case.page_stride,
                      k_offset=case.k_offset, scale_offset=case.scale_offset, topk=case.topk,
-                     cand_mode=case.cand_mode, cand_blocks=case.cand_blocks,
-                     cand_in=kw["cand_in"])
+                     cand_mode=case.cand_mode, cand_blocks=case.cand_blocks, cand_in=cin,
+                     indices_out=idx_o, cand_out=cand_o)
+        hbufs.append(hb)
+        dbufs.append(db)
+        obufs.append(ob)
+        ohost.append(torch.empty(ob.shape, dtype=torch.uint8, pin_memory=True))
         calls.append(c)
-    out_h = [torch.empty(c.indices.shape, dtype=torch.int32, pin_memory=True) for c in calls]
-    cand_h = [None if c.cand is None else torch.empty(c.cand.shape, dtype=torch.int32,
-                                                      pin_memory=True) for c in calls]
 
     def step(k):
         i = k % nsets
-        for n, h in host[i].items():
-            dev[i][n].copy_(h, non_blocking=True)
+        dbufs[i].copy_(hbufs[i], non_blocking=True)
         calls[i].run(workspace, stream)
-        out_h[i].copy_(calls[i].indices, non_blocking=True)
-        if cand_h[i] is not None:
-            cand_h[i].copy_(calls[i].cand, non_blocking=True)
+        ohost[i].copy_(obufs[i], non_blocking=True)
 
     for k in range(args.warmup):
         step(k)
@@ -508,10 +530,8 @@ def run_e2e(args, sets, workspace, stream, world):
     barrier(world)
     ms = reduce_max(t0.elapsed_time(t1), world)
     pairs = reduce_sum(sum(sets[(args.warmup + k) % nsets][2] for k in range(args.steps)), world)
-    h2d = sum(step_bytes_in(sets[(args.warmup + k) % nsets][0]) for k in range(args.steps))
-    d2h = sum(out_h[(args.warmup + k) % nsets].numel() * 4 +
-              (0 if cand_h[(args.warmup + k) % nsets] is None
-               else cand_h[(args.warmup + k) % nsets].numel() * 4) for k in range(args.steps))
+    h2d = sum(hbufs[(args.warmup + k) % nsets].numel() for k in range(args.steps))
+    d2h = sum(ohost[(args.warmup + k) % nsets].numel() for k in range(args.steps))
     return {"value": pairs / (ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": h2d // args.steps, "d2h_bytes_per_step": d2h // args.steps}
 
