@@ -9,7 +9,9 @@
 // warp keeps four row pairs in flight. Per row:
 //   amax = max |x|, s = FP16(amax / 127) (FP32 quotient, round to nearest
 //   even, capped at 65504), q = clamp(rint(x / s), -127, 127) with an FP32
-//   quotient; s rounding to zero gives codes 0 and scale +0.
+//   quotient; s rounding to zero gives codes 0 and scale +0. The per-element
+//   quotient comes from the row's reciprocal and one correction step (a
+//   multiply and two FMAs instead of a divide).
 #include <cuda_fp16.h>
 
 #include "qli_internal.h"
@@ -23,10 +25,26 @@ constexpr int kQWarps = kQThreads / 32;
 constexpr int kQDepth = 4;            // row pairs in flight per warp
 constexpr int kRowValues = 128;
 
-__device__ __forceinline__ uint32_t code_byte(float x, float sf) {
-  int c = __float2int_rn(__fdiv_rn(x, sf));
-  c = min(max(c, -127), 127);
-  return static_cast<uint32_t>(c) & 0xffu;
+// x / sf in FP32, rounded to nearest even, from y = RN(1 / sf): the product
+// q0 = RN(x * y) is within about an ulp of the quotient, so the residual
+// x - q0 * sf is exact in one FMA and RN(q0 + residual * y) is the correctly
+// rounded quotient (Markstein's correction step: P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990). Inputs are BF16 values and FP16 scales, so the domain
+// is finite: qli_check_quant_rounding compares every pair with IEEE
+// division.
+__device__ __forceinline__ float quotient(float x, float sf, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, sf, x);
+  return __fmaf_rn(r, y, q0);
+}
+
+__device__ __forceinline__ int code_of(float x, float sf, float y) {
+  return min(max(__float2int_rn(quotient(x, sf, y)), -127), 127);
+}
+
+__device__ __forceinline__ uint32_t code_byte(float x, float sf, float y) {
+  return static_cast<uint32_t>(code_of(x, sf, y)) & 0xffu;
 }
 
 // The half-warp's row: v = this lane's 8 BF16 values. All 32 lanes call it
@@ -49,10 +67,11 @@ __device__ __forceinline__ uint2 quant_half_row(const uint4 v, uint16_t& scale_b
   const float sf = __half2float(__ushort_as_half(sb));
   uint32_t lo = 0u, hi = 0u;
   if (sf != 0.0f) {
+    const float y = __frcp_rn(sf);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      lo |= code_byte(x[i], sf) << (8 * i);
-      hi |= code_byte(x[4 + i], sf) << (8 * i);
+      lo |= code_byte(x[i], sf, y) << (8 * i);
+      hi |= code_byte(x[4 + i], sf, y) << (8 * i);
     }
   } else {
     sb = 0u;
@@ -65,6 +84,7 @@ __device__ __forceinline__ uint2 quant_half_row(const uint4 v, uint16_t& scale_b
 struct DenseOut {
   int8_t* q;
   uint16_t* scale;
+  __device__ __forceinline__ int64_t key(int64_t r) const { return r; }
   __device__ __forceinline__ bool dest(int64_t r, uint2*& codes, uint16_t*& sc) const {
     codes = reinterpret_cast<uint2*>(q + r * kRowValues);
     sc = scale + r;
@@ -78,8 +98,9 @@ struct PagedOut {
   int64_t slots_total, page_stride, k_offset, scale_offset;
   int32_t R;
   uint32_t* err;
-  __device__ __forceinline__ bool dest(int64_t r, uint2*& codes, uint16_t*& sc) const {
-    const int64_t m = __ldg(slot + r);
+  // the slot, loaded with the row (before any store of the warp)
+  __device__ __forceinline__ int64_t key(int64_t r) const { return __ldg(slot + r); }
+  __device__ __forceinline__ bool dest(int64_t m, uint2*& codes, uint16_t*& sc) const {
     if (m < 0) return false;                       // padding
     if (m >= slots_total) {
       if (err != nullptr) atomicOr(err, QLI_DEVERR_PAGE);
@@ -102,11 +123,16 @@ __global__ void __launch_bounds__(kQThreads) quant_kernel(const uint16_t* __rest
   // a warp takes row pairs warp, warp + nwarps, ... kQDepth at a time
   for (int64_t p0 = warp; 2 * p0 < rows; p0 += kQDepth * nwarps) {
     uint4 v[kQDepth];
+    int64_t key[kQDepth];
 #pragma unroll
     for (int d = 0; d < kQDepth; ++d) {
       const int64_t r = 2 * (p0 + d * nwarps) + half;
       v[d] = make_uint4(0u, 0u, 0u, 0u);
-      if (r < rows) v[d] = __ldcs(reinterpret_cast<const uint4*>(x + r * kRowValues) + j);
+      key[d] = -1;
+      if (r < rows) {
+        v[d] = __ldcs(reinterpret_cast<const uint4*>(x + r * kRowValues) + j);
+        key[d] = out.key(r);
+      }
     }
 #pragma unroll
     for (int d = 0; d < kQDepth; ++d) {
@@ -115,11 +141,45 @@ __global__ void __launch_bounds__(kQThreads) quant_kernel(const uint16_t* __rest
       const uint2 c = quant_half_row(v[d], sb);
       uint2* codes;
       uint16_t* sc;
-      if (r < rows && out.dest(r, codes, sc)) {
+      if (r < rows && out.dest(key[d], codes, sc)) {
         codes[j] = c;
         if (j == 0) *sc = sb;
       }
     }
+  }
+}
+
+// Every pair a row can produce: block b takes scale bits b + 1, each thread
+// a strided share of the 65536 x patterns. A row has |x| <= amax, and
+// amax / s < 192 unless s is the 65504 cap (s = FP16(amax / 127): within
+// 2^-11 relative when normal, within 2^-25 when subnormal, s >= 2^-24), so
+// the pairs are |x| <= 256 s, and every finite x for s = 65504.
+// counts[0] += pairs whose code differs from clamp(rint(IEEE x / s));
+// counts[1] += pairs with |x| >= 2^-100 whose FP32 quotient differs from the
+// IEEE one (below that the residual x - q0 s can fall under the FP32 range and
+// the correction step loses its exactness; those quotients are < 2^-85 and
+// their codes 0 either way, which counts[0] covers).
+__global__ void __launch_bounds__(256) rounding_check_kernel(unsigned long long* counts) {
+  const float sf = __half2float(__ushort_as_half(static_cast<uint16_t>(blockIdx.x + 1)));
+  const float y = __frcp_rn(sf);
+  const float xmax = sf == 65504.0f ? 3.4028235e38f : 256.0f * sf;
+  unsigned code_bad = 0, quot_bad = 0;
+  for (uint32_t b = threadIdx.x; b < 65536u; b += blockDim.x) {
+    const float x = __uint_as_float(b << 16);
+    if (!(fabsf(x) <= xmax)) continue;              // also skips Inf and NaN
+    const float ieee = __fdiv_rn(x, sf);
+    const float fast = quotient(x, sf, y);
+    const int want = min(max(__float2int_rn(ieee), -127), 127);
+    code_bad += code_of(x, sf, y) != want;
+    quot_bad += fabsf(x) >= 7.88860905e-31f && __float_as_uint(fast) != __float_as_uint(ieee);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    code_bad += __shfl_xor_sync(0xffffffffu, code_bad, o);
+    quot_bad += __shfl_xor_sync(0xffffffffu, quot_bad, o);
+  }
+  if ((threadIdx.x & 31) == 0 && (code_bad | quot_bad)) {
+    atomicAdd(counts, code_bad);
+    atomicAdd(counts + 1, quot_bad);
   }
 }
 
@@ -175,5 +235,16 @@ extern "C" qli_status qli_write_index_k(const uint16_t* k, int64_t n, const int6
                      scale_offset, rows_per_page, err_word};
   quant_kernel<PagedOut><<<quant_grid(n, sms), kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       k, n, out);
+  return cudaGetLastError() == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+}
+
+extern "C" qli_status qli_check_quant_rounding(unsigned long long* counts, void* stream) {
+  using namespace qli;
+  if (!counts) return QLI_ERR_INVALID_ARG;
+  if (!aligned_to(counts, 8)) return QLI_ERR_ALIGNMENT;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), st) != cudaSuccess)
+    return QLI_ERR_CUDA;
+  rounding_check_kernel<<<0x7bff, 256, 0, st>>>(counts);
   return cudaGetLastError() == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }

@@ -55,7 +55,8 @@ class Args(ctypes.Structure):
 
 EXPORTS = ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage", "qli_launch_count",
            "qli_scores_layout", "qli_read_device_error", "qli_status_string", "qli_abi_version",
-           "qli_args_size", "qli_run_static", "qli_quantize_q", "qli_write_index_k"]
+           "qli_args_size", "qli_run_static", "qli_quantize_q", "qli_write_index_k",
+           "qli_check_quant_rounding"]
 
 _lib = None
 
@@ -90,6 +91,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.qli_write_index_k.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_int64,
                                     c_int32, c_int64, c_int64, c_void_p, c_void_p]
     L.qli_write_index_k.restype = c_int32
+    L.qli_check_quant_rounding.argtypes = [c_void_p, c_void_p]
+    L.qli_check_quant_rounding.restype = c_int32
     for name in ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage",
                  "qli_launch_count", "qli_scores_layout", "qli_read_device_error"]:
         getattr(L, name).restype = c_int32
@@ -257,6 +260,17 @@ def quantize_q(x, q_out=None, scale_out=None, stream=None):
     _check(lib().qli_quantize_q(_ptr(x), rows, _ptr(q_out), _ptr(scale_out), _stream(stream)),
            "qli_quantize_q")
     return q_out, scale_out
+
+
+def check_quant_rounding(stream=None):
+    """qli_check_quant_rounding: (code mismatches, quotient mismatches) of
+    the quantisers' division against IEEE FP32 division over every BF16 x and
+    every positive finite FP16 scale."""
+    import torch
+    counts = torch.empty(2, dtype=torch.int64, device="cuda")
+    _check(lib().qli_check_quant_rounding(_ptr(counts), _stream(stream)),
+           "qli_check_quant_rounding")
+    return tuple(int(v) for v in counts.cpu())
 
 
 def write_index_k(k, slot_mapping, cache, *, rows_per_page: int, page_stride: int,

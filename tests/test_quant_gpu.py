@@ -150,3 +150,10 @@ def test_written_cache_and_quantised_queries_feed_the_indexer():
     idx, _ = call.run(call.alloc_workspace())
     torch.cuda.synchronize()
     assert np.array_equal(idx.cpu().numpy()[:, 0, :], want)
+
+
+def test_division_matches_ieee_on_every_bf16_value_and_fp16_scale():
+    # the kernels' reciprocal-and-correction quotient against IEEE FP32
+    # division, exhaustively over every (x, scale) pair a row can produce
+    counts = qli.check_quant_rounding()
+    assert counts == (0, 0)
