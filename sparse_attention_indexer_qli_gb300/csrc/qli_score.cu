@@ -314,7 +314,25 @@ static_assert(kSmemBytes <= 227 * 1024, "stream kernel shared memory");
 // Walks the CTA's units in order: (token, tile within the token).
 struct Cursor {
   int32_t t, tile, end_t;
+  // The token owning unit u (< unit_start[T]): the last t with unit_start[t]
+  // <= u. The whole warp searches, 32 probes per round trip, so T <= 1024
+  // takes two rounds instead of a scalar search's log2(T) dependent loads.
   __device__ void init(const DevArgs& a, int32_t u) {
+    const int lane = threadIdx.x & 31;
+    int32_t lo = 0, hi = a.T;          // unit_start[lo] <= u < unit_start[hi]
+    while (hi - lo > 1) {
+      const int32_t step = (hi - lo + 31) >> 5;
+      const int32_t p = lo + (lane + 1) * step;
+      const bool le = p < hi && __ldg(a.unit_start + p) <= u;
+      lo += __popc(__ballot_sync(0xffffffffu, le)) * step;
+      hi = min(hi, lo + step);
+    }
+    t = lo;
+    tile = u - a.unit_start[t];
+    end_t = a.unit_start[t + 1];
+  }
+  // The same search by one thread (t and tile only).
+  __device__ void init_scalar(const DevArgs& a, int32_t u) {
     int32_t lo = 0, hi = a.T - 1;
     while (lo < hi) {
       const int32_t mid = (lo + hi + 1) >> 1;
@@ -322,7 +340,6 @@ struct Cursor {
     }
     t = lo;
     tile = u - a.unit_start[t];
-    end_t = a.unit_start[t + 1];
   }
   __device__ void next(const DevArgs& a, int32_t u_next) {
     ++tile;
@@ -414,10 +431,31 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       const int s = k % kKStages;
       const uint32_t ph = (k / kKStages) & 1;
       if (!consumer && (k & 31) == 0) {
-        // lane j resolves tile k+j: request, pages (one or two per tile)
+        // lane j resolves tile k+j: token, request, pages (one or two per
+        // tile). The token comes from the next 32 token boundaries after the
+        // base's (one load per lane): tile k+j lies in token c.t + (the
+        // boundaries at or below its unit), found by a shuffle search. The
+        // base (c.t, c.tile) is unit u0+k's token and tile, or a tile past
+        // that token's last when u0+k starts a later one.
+        const int32_t uj = u0 + k + lane;
+        const int32_t bi = c.t + 1 + lane;
+        const int32_t nb = bi <= a.T ? __ldg(a.unit_start + bi) : 0x7fffffff;
+        int32_t cnt = 0;
+#pragma unroll
+        for (int w = 16; w > 0; w >>= 1)
+          if (__shfl_sync(0xffffffffu, nb, cnt + w - 1) <= uj) cnt += w;
+        if (__shfl_sync(0xffffffffu, nb, cnt) <= uj) ++cnt;      // 0..32
+        const int32_t below = __shfl_sync(0xffffffffu, nb, cnt > 0 ? cnt - 1 : 0);
+        Cursor m;
+        m.t = c.t;
+        m.tile = 0;
         if (k + lane < nk) {
-          Cursor m;
-          m.init(a, u0 + k + lane);
+          if (cnt < 32) {
+            m.t = c.t + cnt;
+            m.tile = uj - (cnt > 0 ? below : u0 + k - c.tile);
+          } else {
+            m.init_scalar(a, uj);      // past 32 boundaries (tokens without tiles)
+          }
           const int32_t b = a.tok_b[m.t], V = a.tok_V[m.t];
           const int64_t row = static_cast<int64_t>(b) * a.bt_stride;
           const int32_t j0 = m.tile * kTile;
@@ -431,6 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           }
           if (!two) pg1 = -1;
         }
+        // the next batch's base: one tile past lane 31's (used only when
+        // tile k+32 exists, i.e. lane 31 resolved a tile)
+        c.t = __shfl_sync(0xffffffffu, m.t, 31);
+        c.tile = __shfl_sync(0xffffffffu, m.tile, 31) + 1;
       }
       if (lane == 0) ok = mbar_wait_bounded(&S.empty[s], ph ^ 1);
       ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -465,9 +465,9 @@ __device__ int compact_range(const Row& r, int32_t begin, int32_t end, Keep keep
 // Ordered compaction of a row of at most kShortChunks * 4096 entries whose
 // threshold bin is known (t_lo: the bin's lowest key). The row is read in
 // chunks of 4096 entries, thread i taking entries 4i..4i+3 of each chunk
-// with one 16-byte load (all issued together); the keys go to `cache`
-// (shared memory, the row's length) and a keep bit per entry stays in a
-// register. The row-order offset of thread i's kept entries in chunk c is
+// with one 16-byte load (all issued together); the raw values go to
+// `cache` (shared memory, the row's length), a keep bit per entry stays in a
+// register, and only kept entries are turned into keys. The row-order offset of thread i's kept entries in chunk c is
 // (kept entries of chunks before c) + (kept entries of chunk c in threads
 // before i): packed warp scans give all chunks' offsets at once (8-bit
 // fields within a warp, 16-bit fields across warps) with one block barrier.
@@ -477,14 +477,15 @@ __device__ int compact_range(const Row& r, int32_t begin, int32_t end, Keep keep
 constexpr int kShortChunks = 8;
 constexpr int kCandHalf = (kHeadWords + kCandCap - 1024) / 2;   // 5632
 
+// The row's entries as float4 chunks (thread i: entries 4i..4i+3 of each
+// chunk of 4096) and, for a consumer row, the block of each chunk's group of
+// eight; issued together, so one round trip covers the row.
 template <bool kConsumer>
-__device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint32_t* ckeys,
-                             int32_t* cid, int cap, Shared& sh, int32_t id_base = 0) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ void short_load(const Row& r, float4 (&f)[kShortChunks],
+                                           int32_t (&blk)[kShortChunks]) {
+  const int tid = threadIdx.x;
   const int32_t nch = (r.len + 4 * kThreads - 1) / (4 * kThreads);
   const float4* v4 = reinterpret_cast<const float4*>(r.vals);
-  float4 f[kShortChunks];
-  int32_t blk[kShortChunks];
 #pragma unroll
   for (int c = 0; c < kShortChunks; ++c) {
     const int32_t s0 = c * 4 * kThreads + 4 * tid;
@@ -495,29 +496,66 @@ __device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint3
       if (kConsumer) blk[c] = __ldcg(r.blocks + (s0 >> 3));
     }
   }
+}
+
+// order_key(x) >= t_lo as one unsigned range test on the raw FP32 bits u:
+// (u - lo) <= span. A threshold at or above 2^31 (non-negative values) keeps
+// lo' <= u <= 0x7fffffff with lo' = t_lo - 2^31, and also u = 0x80000000
+// (-0, whose key is +0's) when lo' = 0; a lower threshold keeps every u <=
+// ~t_lo (all non-negative values, -0, and the negative ones down to it).
+struct KeepRange {
+  uint32_t lo, span;
+  __device__ __forceinline__ explicit KeepRange(uint32_t t_lo) {
+    if (t_lo >= 0x80000000u) {
+      lo = t_lo - 0x80000000u;
+      span = lo == 0u ? 0x80000000u : 0x7fffffffu - lo;
+    } else {
+      lo = 0u;
+      span = ~t_lo;
+    }
+  }
+  __device__ __forceinline__ bool operator()(uint32_t u) const { return u - lo <= span; }
+};
+
+// Compacts a row of up to kShortChunks chunks already loaded by short_load:
+// raw values to `cache` (shared memory), then, in row order, the key and id
+// of every entry whose key is >= t_lo to ckeys / cid (written while below
+// cap). Per-chunk counts travel as packed 8-bit fields through one warp scan
+// and (widened to 16 bits) one cross-warp scan, so the whole compaction
+// takes one barrier pair. Returns how many entries passed.
+template <bool kConsumer>
+__device__ int compact_short_from(const Row& r, uint32_t t_lo, const float4 (&f)[kShortChunks],
+                                  const int32_t (&blk)[kShortChunks], uint32_t* cache,
+                                  uint32_t* ckeys, int32_t* cid, int cap, Shared& sh,
+                                  int32_t id_base = 0) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t nch = (r.len + 4 * kThreads - 1) / (4 * kThreads);
+  const KeepRange pass(t_lo);
   const auto id_of = [&](int c, int j) {
     const int32_t s = c * 4 * kThreads + 4 * tid + j;
     return kConsumer ? blk[c] * kBlock + (s & (kBlock - 1)) : id_base + s;
   };
-  // keys to the cache, keep bits to `keep` (bit 4c + j), counts per chunk
-  // as 8-bit fields (chunks 0-3 in mine[0], 4-7 in mine[1])
+  // raw values to the cache, keep bits to `keep` (bit 4c + j), counts per
+  // chunk as 8-bit fields (chunks 0-3 in mine[0], 4-7 in mine[1])
   uint32_t keep = 0u, mine[2] = {0u, 0u};
 #pragma unroll
   for (int c = 0; c < kShortChunks; ++c) {
     const int32_t s0 = c * 4 * kThreads + 4 * tid;
     if (c < nch && s0 < r.len) {
-      const uint4 k4 = make_uint4(order_key(f[c].x), order_key(f[c].y), order_key(f[c].z),
-                                  order_key(f[c].w));
-      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
-      uint32_t n = 0u;
+      const uint4 u4 = make_uint4(__float_as_uint(f[c].x), __float_as_uint(f[c].y),
+                                  __float_as_uint(f[c].z), __float_as_uint(f[c].w));
+      uint32_t m = (pass(u4.x) ? 1u : 0u) | (pass(u4.y) ? 2u : 0u) | (pass(u4.z) ? 4u : 0u) |
+                   (pass(u4.w) ? 8u : 0u);
+      const int32_t left = r.len - s0;
+      if (left < 4) m &= (1u << left) - 1u;
+      if (kConsumer) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool ok = s0 + j < r.len && (!kConsumer || id_of(c, j) < r.V) && kk[j] >= t_lo;
-        keep |= ok ? (1u << (4 * c + j)) : 0u;
-        n += ok ? 1u : 0u;
+        for (int j = 0; j < 4; ++j)
+          if (id_of(c, j) >= r.V) m &= ~(1u << j);
       }
-      *reinterpret_cast<uint4*>(cache + s0) = k4;      // s0 + 3 < the row's padded length
-      mine[c >> 2] |= n << (8 * (c & 3));
+      keep |= m << (4 * c);
+      *reinterpret_cast<uint4*>(cache + s0) = u4;      // s0 + 3 < the row's padded length
+      mine[c >> 2] |= static_cast<uint32_t>(__popc(m)) << (8 * (c & 3));
     }
   }
   // within the warp: at most 32 x 4 per field
@@ -568,13 +606,13 @@ __device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint3
     const uint32_t bits = (keep >> (4 * c)) & 0xfu;
     if (bits) {
       const int32_t s0 = c * 4 * kThreads + 4 * tid;
-      const uint4 k4 = *reinterpret_cast<const uint4*>(cache + s0);
-      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      const uint4 u4 = *reinterpret_cast<const uint4*>(cache + s0);
+      const uint32_t uu[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if ((bits >> j) & 1u) {
           if (at < cap) {
-            ckeys[at] = kk[j];
+            ckeys[at] = order_key(__uint_as_float(uu[j]));
             cid[at] = id_of(c, j);
           }
           ++at;
@@ -584,6 +622,16 @@ __device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint3
   }
   __syncthreads();
   return total;
+}
+
+// short_load + compact_short_from.
+template <bool kConsumer>
+__device__ int compact_short(const Row& r, uint32_t t_lo, uint32_t* cache, uint32_t* ckeys,
+                             int32_t* cid, int cap, Shared& sh, int32_t id_base = 0) {
+  float4 f[kShortChunks];
+  int32_t blk[kShortChunks];
+  short_load<kConsumer>(r, f, blk);
+  return compact_short_from<kConsumer>(r, t_lo, f, blk, cache, ckeys, cid, cap, sh, id_base);
 }
 
 // For a dense row of up to 32K entries without a score-stage histogram: one
@@ -770,8 +818,8 @@ __device__ void refine_threshold(const uint32_t* ckeys, int n, uint32_t sel, int
 // in row order, on which the exact selection runs. If the sample misjudges
 // (fewer than `want` or more than kCandCap candidates) the exact selection
 // runs on the whole row; the result is the same either way.
-__device__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh,
-                                uint32_t* scratch, const Stats* known = nullptr) {
+__device__ __noinline__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh,
+                                         uint32_t* scratch, const Stats* known = nullptr) {
   const Stats st = known ? *known : row_stats(r, sh);
   if (st.E <= static_cast<uint32_t>(want)) return ordered_output(r, 0u, 0, out, sh);
   if (scratch != nullptr && r.cached != nullptr && r.idx == nullptr && r.ids == nullptr &&
@@ -1045,7 +1093,8 @@ __device__ bool load_candidates(const DevArgs& a, int t, int which, Row& r, uint
 // Copies the row's keys into shared memory (when it fits), points the row at
 // them, and returns the row's statistics gathered on the way. Dense rows are
 // read as float4, two loads in flight per thread.
-__device__ Stats cache_keys(Row& r, uint32_t* keys, int32_t cap, Shared& sh, bool& cached) {
+__device__ __noinline__ Stats cache_keys(Row& r, uint32_t* keys, int32_t cap, Shared& sh,
+                                       bool& cached) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   cached = r.len <= cap;
   uint32_t cnt = 0u, kmax = 0u, kmin = 0xffffffffu;
@@ -1100,9 +1149,53 @@ __device__ Stats cache_keys(Row& r, uint32_t* keys, int32_t cap, Shared& sh, boo
   return st;
 }
 
+// A row longer than the key region: its candidates (every entry in or above
+// the threshold bin or digit) were compacted by lcompact_kernel; they are
+// ranked here, or the row is ranked from L2 when they overflowed.
+__device__ __noinline__ int select_long_row(const DevArgs& a, int t, int which, Row r,
+                                            int32_t want, uint32_t* keys, uint32_t* scratch,
+                                            int32_t* out, Shared& sh) {
+  const bool blocks = which == 1;
+  int32_t written = 0;
+  // long row: its candidates (every entry in or above the threshold bin
+  // or digit) were compacted by lcompact_kernel
+  int32_t* cid = reinterpret_cast<int32_t*>(keys) + kLongCandCap;
+  int32_t* offs = reinterpret_cast<int32_t*>(scratch);
+  bool done = false;
+  if (a.lchunks > 0 && a.fhist != nullptr) {
+    int32_t pinned = -1;
+    if (blocks) {
+      const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
+      pinned = static_cast<int32_t>(
+          hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
+    }
+    const HistSel hs = hist_select(
+        a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins, pinned, want, sh);
+    if (hs.E > static_cast<uint32_t>(want) &&
+        load_candidates(a, t, which, r, keys, cid, offs, sh)) {
+      if (static_cast<uint32_t>(r.len) == hs.above + hs.cbin) {
+        uint32_t thr;
+        int32_t need_eq;
+        refine_threshold(keys, r.len, hs.sel, want - static_cast<int32_t>(hs.above),
+                         scratch + kHeadWords + kCandCap - 1024, sh, thr, need_eq);
+        written = ordered_output(r, thr, need_eq, out, sh);
+      } else {
+        written = select_ascending(r, want, out, sh, nullptr);
+      }
+      done = true;
+    }
+  } else if (a.lchunks > 0) {
+    (void)load_candidates(a, t, which, r, keys, cid, offs, sh);
+  }
+  if (!done) written = select_ascending(r, want, out, sh, nullptr);
+  return written;
+}
+
 // Dynamic shared memory: `region` words for the row's keys (or a long row's
 // candidates), then kHeadWords + kCandCap words for the sample and
-// histogram paths.
+// histogram paths. One instance per launch mode (score-stage histogram or
+// not, consumer rows or not), so each holds only the code its rows can take.
+template <bool kFused, bool kConsumerMode>
 __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key_cap,
                                                           int32_t region) {
   extern __shared__ uint32_t keys[];
@@ -1116,11 +1209,12 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
                         : a.idx_out + static_cast<int64_t>(t) * a.topk;
   // the row's histogram word is requested before the row's metadata, so the
   // two round trips overlap
-  const uint4 fh_word = a.fhist != nullptr
+  const uint4 fh_word = kFused
                             ? hist_word(a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins)
                             : make_uint4(0u, 0u, 0u, 0u);
   int32_t want;
   Row r = row_of(a, t, which, want);
+  r.consumer = kConsumerMode;      // a consumer launch has only consumer rows
   int32_t written = 0;
   if (blocks && r.len == 0) {
     // at most C visible blocks: all of them, in order
@@ -1129,38 +1223,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
     written = nb;
   } else {
     if (r.len > key_cap) {
-      // long row: its candidates (every entry in or above the threshold bin
-      // or digit) were compacted by lcompact_kernel
-      int32_t* cid = reinterpret_cast<int32_t*>(keys) + kLongCandCap;
-      int32_t* offs = reinterpret_cast<int32_t*>(scratch);
-      bool done = false;
-      if (a.lchunks > 0 && a.fhist != nullptr) {
-        int32_t pinned = -1;
-        if (blocks) {
-          const int32_t last = (r.V + kBlock - 1) / kBlock - 1;
-          pinned = static_cast<int32_t>(
-              hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
-        }
-        const HistSel hs = hist_select(
-            a.fhist + (2 * static_cast<int64_t>(t) + which) * kHistBins, pinned, want, sh);
-        if (hs.E > static_cast<uint32_t>(want) &&
-            load_candidates(a, t, which, r, keys, cid, offs, sh)) {
-          if (static_cast<uint32_t>(r.len) == hs.above + hs.cbin) {
-            uint32_t thr;
-            int32_t need_eq;
-            refine_threshold(keys, r.len, hs.sel, want - static_cast<int32_t>(hs.above),
-                             scratch + kHeadWords + kCandCap - 1024, sh, thr, need_eq);
-            written = ordered_output(r, thr, need_eq, out, sh);
-          } else {
-            written = select_ascending(r, want, out, sh, nullptr);
-          }
-          done = true;
-        }
-      } else if (a.lchunks > 0) {
-        (void)load_candidates(a, t, which, r, keys, cid, offs, sh);
-      }
-      if (!done) written = select_ascending(r, want, out, sh, nullptr);
-    } else if (a.fhist != nullptr) {
+      written = select_long_row(a, t, which, r, want, keys, scratch, out, sh);
+    } else if (kFused) {
       // the score stage's histogram gives the threshold bin up front: the
       // entries at or above it are compacted in row order in one pass over
       // the row and ranked exactly
@@ -1170,14 +1234,18 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
         pinned = static_cast<int32_t>(
             hist_bin(order_key(a.bscores[static_cast<int64_t>(t) * a.Brow + last])));
       }
-      const HistSel hs = hist_select_word(fh_word, pinned, want, sh);
       // candidates: a row of 2 to kShortChunks chunks of 4096 entries caches
-      // its keys in the key region and puts the candidates' keys and ids in
-      // the scratch area (kCandHalf words each); a one-chunk or a longer row
-      // puts keys in the key region and ids in the scratch area (one chunk
-      // needs a single barrier that way). The scratch area's last 1024 words
-      // hold the refine's digit histogram.
+      // its values in the key region and puts the candidates' keys and ids
+      // in the scratch area (kCandHalf words each); a one-chunk or a longer
+      // row puts keys in the key region and ids in the scratch area (one
+      // chunk needs a single barrier that way). The scratch area's last 1024
+      // words hold the refine's digit histogram. A short row's loads are in
+      // flight while the histogram picks the threshold bin.
       const bool short_row = r.len > 4 * kThreads && r.len <= kShortChunks * 4 * kThreads;
+      float4 f[kShortChunks];
+      int32_t blk[kShortChunks];
+      if (short_row) short_load<kConsumerMode>(r, f, blk);
+      const HistSel hs = hist_select_word(fh_word, pinned, want, sh);
       uint32_t* ckeys = short_row ? scratch : keys;
       int32_t* cid = reinterpret_cast<int32_t*>(short_row ? scratch + kCandHalf : scratch);
       const int cap = short_row ? kCandHalf : min(region, kHeadWords + kCandCap - 1024);
@@ -1190,12 +1258,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
         const uint32_t t_lo = hs.sel << (32 - kHistBits);
         int got;
         if (short_row) {
-          got = r.consumer ? compact_short<true>(r, t_lo, keys, ckeys, cid, cap, sh)
-                           : compact_short<false>(r, t_lo, keys, ckeys, cid, cap, sh);
+          got = compact_short_from<kConsumerMode>(r, t_lo, f, blk, keys, ckeys, cid, cap, sh);
         } else {
           const auto keep = [t_lo](uint32_t k) { return k >= t_lo; };
-          got = r.consumer ? compact_range<true>(r, 0, r.len, keep, ckeys, cid, cap, sh)
-                           : compact_range<false>(r, 0, r.len, keep, ckeys, cid, cap, sh);
+          got = compact_range<kConsumerMode>(r, 0, r.len, keep, ckeys, cid, cap, sh);
         }
         if (got == static_cast<int>(n)) {
           uint32_t thr;
@@ -1293,12 +1359,17 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   // candidate rows need room for kLongCandCap keys and ids
   const int32_t region = d.lchunks > 0 ? (cap > 2 * kLongCandCap ? cap : 2 * kLongCandCap) : cap;
   const int smem = 4 * (region + kHeadWords + kCandCap);
-  static std::atomic<uint64_t> done{0};
-  e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel),
-                        4 * (kSmemKeys + kHeadWords + kCandCap), done);
+  static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
+  void (*const kernels[4])(DevArgs, int32_t, int32_t) = {
+      select_kernel<false, false>, select_kernel<false, true>, select_kernel<true, false>,
+      select_kernel<true, true>};
+  const int which = (d.fhist != nullptr ? 2 : 0) + (d.mode == QLI_CAND_CONSUMER ? 1 : 0);
+  e = ensure_smem_limit(reinterpret_cast<const void*>(kernels[which]),
+                        4 * (kSmemKeys + kHeadWords + kCandCap), done[which]);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(d.T), d.mode == QLI_CAND_SOURCE ? 2u : 1u);
-  e = launch_pdl(select_kernel, grid, dim3(kThreads), static_cast<size_t>(smem), s, d, cap, region);
+  e = launch_pdl(kernels[which], grid, dim3(kThreads), static_cast<size_t>(smem), s, d, cap,
+                 region);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
