@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
 // (token, tile) list, so the token's queries stay in shared memory across
 // its tiles. Warp roles:
 //   warp 0      producer: TMA copies of the tile's INT8 K rows (128-byte
-//               swizzle) and FP16 scales into an 11-stage shared-memory ring
+//               swizzle) and FP16 scales into an 8-stage shared-memory ring
 //               (whole pages for dense tiles; 1 KB + 16 B per 8-position
 //               block in consumer mode); for dense tiles lane j resolves the
 //               page IDs of tile k0+j once per 32 tiles, so no block-table
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
 // slot still a phase behind, waiting on the other parity's MMA issuer.)
 namespace stream {
 
-constexpr int kKStages = 11;                         // shared-memory K ring
+constexpr int kKStages = 8;                          // shared-memory K ring
 // TMEM holds two rings: the MMA's A operands (the converted K tiles, 64
 // columns each), freed when the tensor core has read them, and the
 // accumulators (64 columns each), freed when the epilogue has loaded them.
