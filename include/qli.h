@@ -217,7 +217,7 @@ qli_status qli_write_index_k(const uint16_t *k, int64_t n, const int64_t *slot_m
                              int32_t rows_per_page, int64_t k_offset, int64_t scale_offset,
                              uint32_t *err_word, void *stream);
 
-/* Self-check of the quantisers' per-element division, which computes x / s
+/* Self-check of the quantisers' divisions, which compute x / s and amax / 127
  * from the row's reciprocal with one correction step instead of an IEEE
  * divide (Markstein, IBM J. Res. Dev. 34(1), 1990). Both operands come from
  * finite sets (x a BF16 value, s a positive finite FP16 scale), so one
@@ -226,7 +226,8 @@ qli_status qli_write_index_k(const uint16_t *k, int64_t n, const int64_t *slot_m
  * and every finite x for s = 65504. It leaves in the device array counts[2]
  * (8-byte aligned; zeroed by the call): counts[0] = pairs
  * whose code clamp(rint(x / s), -127, 127) differs from the one an IEEE FP32
- * division gives, counts[1] = pairs with |x| >= 2^-100 whose FP32 quotient
+ * division gives, plus the BF16 values amax >= 0 whose scale FP16(amax / 127)
+ * (computed the same way) differs from the IEEE one, counts[1] = pairs with |x| >= 2^-100 whose FP32 quotient
  * differs from the IEEE one (below that the correction's residual can
  * underflow; those quotients round to code 0 either way). Asynchronous. */
 qli_status qli_check_quant_rounding(unsigned long long *counts, void *stream);

@@ -40,7 +40,20 @@ __device__ __forceinline__ float quotient(float x, float sf, float y) {
 }
 
 __device__ __forceinline__ int code_of(float x, float sf, float y) {
-  return min(max(__float2int_rn(quotient(x, sf, y)), -127), 127);
+  // clamped before the conversion (same result as clamping the integer)
+  return __float2int_rn(fminf(fmaxf(quotient(x, sf, y), -127.0f), 127.0f));
+}
+
+// FP16(amax / 127) with the FP32 quotient rounded to nearest even, through
+// the same correction step from RN(1/127); capped at the largest finite
+// FP16. The check entry point compares it with IEEE division for every BF16
+// amax.
+__device__ __forceinline__ uint16_t scale_bits_of(float amax) {
+  const float kRcp127 = __uint_as_float(0x3c010204u);   // FP32 nearest 1/127
+  const float q = quotient(amax, 127.0f, kRcp127);
+  uint16_t sb = __half_as_ushort(__float2half_rn(q));
+  if (sb == 0x7c00u) sb = 0x7bffu;    // +inf: the largest finite FP16
+  return sb;
 }
 
 __device__ __forceinline__ uint32_t code_byte(float x, float sf, float y) {
@@ -62,8 +75,7 @@ __device__ __forceinline__ uint2 quant_half_row(const uint4 v, uint16_t& scale_b
   for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  uint16_t sb = __half_as_ushort(__float2half_rn(__fdiv_rn(m, 127.0f)));
-  if (sb == 0x7c00u) sb = 0x7bffu;    // +inf: the largest finite FP16
+  uint16_t sb = scale_bits_of(m);
   const float sf = __half2float(__ushort_as_half(sb));
   uint32_t lo = 0u, hi = 0u;
   if (sf != 0.0f) {
@@ -96,7 +108,7 @@ struct PagedOut {
   const int64_t* slot;
   uint8_t* cache;
   int64_t slots_total, page_stride, k_offset, scale_offset;
-  int32_t R;
+  int32_t R, log2R;                                // R is 64 or 128
   uint32_t* err;
   // the slot, loaded with the row (before any store of the warp)
   __device__ __forceinline__ int64_t key(int64_t r) const { return __ldg(slot + r); }
@@ -106,7 +118,7 @@ struct PagedOut {
       if (err != nullptr) atomicOr(err, QLI_DEVERR_PAGE);
       return false;
     }
-    const int64_t page = m / R, row = m - page * R;
+    const int64_t page = m >> log2R, row = m & (R - 1);
     uint8_t* p = cache + page * page_stride;
     codes = reinterpret_cast<uint2*>(p + k_offset + row * kRowValues);
     sc = reinterpret_cast<uint16_t*>(p + scale_offset + row * 2);
@@ -154,12 +166,27 @@ __global__ void __launch_bounds__(kQThreads) quant_kernel(const uint16_t* __rest
 // amax / s < 192 unless s is the 65504 cap (s = FP16(amax / 127): within
 // 2^-11 relative when normal, within 2^-25 when subnormal, s >= 2^-24), so
 // the pairs are |x| <= 256 s, and every finite x for s = 65504.
-// counts[0] += pairs whose code differs from clamp(rint(IEEE x / s));
+// counts[0] += pairs whose code differs from clamp(rint(IEEE x / s)), and
+// (the last block) BF16 values amax whose scale FP16(amax / 127) differs
+// from the one an IEEE division gives;
 // counts[1] += pairs with |x| >= 2^-100 whose FP32 quotient differs from the
 // IEEE one (below that the residual x - q0 s can fall under the FP32 range and
 // the correction step loses its exactness; those quotients are < 2^-85 and
 // their codes 0 either way, which counts[0] covers).
 __global__ void __launch_bounds__(256) rounding_check_kernel(unsigned long long* counts) {
+  if (blockIdx.x == 0x7bffu) {
+    // the scale: every non-negative finite BF16 amax
+    unsigned bad = 0;
+    for (uint32_t b = threadIdx.x; b < 0x7f80u; b += blockDim.x) {
+      const float m = __uint_as_float(b << 16);
+      uint16_t want = __half_as_ushort(__float2half_rn(__fdiv_rn(m, 127.0f)));
+      if (want == 0x7c00u) want = 0x7bffu;
+      bad += scale_bits_of(m) != want;
+    }
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+    if ((threadIdx.x & 31) == 0 && bad) atomicAdd(counts, bad);
+    return;
+  }
   const float sf = __half2float(__ushort_as_half(static_cast<uint16_t>(blockIdx.x + 1)));
   const float y = __frcp_rn(sf);
   const float xmax = sf == 65504.0f ? 3.4028235e38f : 256.0f * sf;
@@ -232,7 +259,7 @@ extern "C" qli_status qli_write_index_k(const uint16_t* k, int64_t n, const int6
   const qli_status st = device_sms(&sms);
   if (st != QLI_OK) return st;
   const PagedOut out{slot_mapping, cache, num_pages * rows_per_page, page_stride, k_offset,
-                     scale_offset, rows_per_page, err_word};
+                     scale_offset, rows_per_page, rows_per_page == 64 ? 6 : 7, err_word};
   quant_kernel<PagedOut><<<quant_grid(n, sms), kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       k, n, out);
   return cudaGetLastError() == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
@@ -245,6 +272,6 @@ extern "C" qli_status qli_check_quant_rounding(unsigned long long* counts, void*
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), st) != cudaSuccess)
     return QLI_ERR_CUDA;
-  rounding_check_kernel<<<0x7bff, 256, 0, st>>>(counts);
+  rounding_check_kernel<<<0x7bff + 1, 256, 0, st>>>(counts);
   return cudaGetLastError() == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
 }
