@@ -157,6 +157,8 @@ WsLayout workspace_layout(const qli_args& a) {
   const bool cons = a.cand_mode == QLI_CAND_CONSUMER;
   L.cand_list = take(cons ? 4 * T * C : 0);
   L.cand_cnt = take(cons ? 4 * T : 0);
+  L.cand_page = take(cons ? 4 * T * C : 0);
+  L.cand_sc = take(cons ? 16 * T * C : 0);
   const size_t kstride = round_up(static_cast<size_t>(cap), kTile);
   L.kf16 = take(L.stream_path ? 0 : 2 * kHeadDim * static_cast<size_t>(B) * kstride);
   L.ks32 = take(L.stream_path ? 0 : 4 * static_cast<size_t>(B) * kstride);
@@ -237,6 +239,8 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.kstride = static_cast<int64_t>(round_up(static_cast<size_t>(d.bt_stride) * a.rows_per_page, kTile));
   d.cand_list = reinterpret_cast<int32_t*>(w + L.cand_list);
   d.cand_cnt = reinterpret_cast<int32_t*>(w + L.cand_cnt);
+  d.cand_page = reinterpret_cast<int32_t*>(w + L.cand_page);
+  d.cand_sc = reinterpret_cast<uint4*>(w + L.cand_sc);
   d.scores = reinterpret_cast<float*>(w + L.scores);
   d.bscores = reinterpret_cast<float*>(w + L.bscores);
   d.Lrow = L.Lrow;

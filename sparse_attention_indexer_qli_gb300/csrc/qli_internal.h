@@ -61,6 +61,8 @@ struct DevArgs {
   int32_t* grp_cnt;    // [Gmax] tokens in the group (0 = unused)
   int32_t* cand_list;  // [T, C] consumer: sorted distinct usable block IDs
   int32_t* cand_cnt;   // [T] consumer: how many
+  int32_t* cand_page;  // [T, C] consumer: the page holding each listed block (checked)
+  uint4* cand_sc;      // [T, C] consumer: each listed block's eight FP16 K scales
   int32_t* unit_start; // [T+1] stream path: first score tile of token t
   uint32_t* counter;   // stream path: CTAs done in cand_prep (reset by plan)
   __half* kf16;        // group path: [B, kstride, 128] widened K
@@ -90,7 +92,8 @@ struct DevArgs {
 
 struct WsLayout {
   size_t err, counter, tok_V, tok_b, req_lk, req_res, req_q0, req_q1, req_g0;
-  size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, kf16, ks32, scores, bscores, total;
+  size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, cand_page, cand_sc, kf16, ks32, scores,
+      bscores, total;
   size_t lext, lhist, lcount, lkey, lid, long_bytes;   // long-row selection (zeroed region: lext..lcount)
   size_t fhist;
   int32_t lchunks;

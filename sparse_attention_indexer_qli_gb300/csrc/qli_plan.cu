@@ -214,6 +214,34 @@ __device__ void consumer_units(const DevArgs& a) {
   }
 }
 
+// The page of each of token t's n listed candidate blocks (its request's
+// block table at the block's first position) and the block's eight FP16 K
+// scales (16 bytes after the page's K rows), one coalesced pass after the
+// list is written; an entry outside the pool sets QLI_DEVERR_PAGE and reads
+// page 0 instead. The score kernel then needs one round trip per tile and
+// one copy per block.
+template <int NT>
+__device__ void cand_pages(const DevArgs& a, int t, int32_t n) {
+  __syncthreads();                       // the CTA's list writes are visible
+  const int32_t b = a.tok_b[t];
+  const int32_t* list = a.cand_list + static_cast<int64_t>(t) * a.C;
+  int32_t* pages = a.cand_page + static_cast<int64_t>(t) * a.C;
+  const int64_t bt_row = static_cast<int64_t>(b < 0 ? 0 : b) * a.bt_stride;
+  bool bad = false;
+  for (int32_t i = threadIdx.x; i < n; i += NT) {
+    const int64_t pos0 = static_cast<int64_t>(list[i]) * kBlock;
+    int32_t page = a.bt[bt_row + pos0 / a.R];
+    if (page < 0 || page >= a.num_pages) {
+      bad = true;
+      page = 0;
+    }
+    pages[i] = page;
+    a.cand_sc[static_cast<int64_t>(t) * a.C + i] = *reinterpret_cast<const uint4*>(
+        a.cache + static_cast<int64_t>(page) * a.page_stride + a.s_off + (pos0 % a.R) * 2);
+  }
+  if (bad) atomicOr(a.err, QLI_DEVERR_PAGE);
+}
+
 // Consumer mode, one CTA per token: keep the candidate IDs that name a block
 // with at least one visible position (0 <= id < ceil(V/8)), sort them
 // ascending and drop duplicates. The guide gives candidates as a padded list
@@ -275,6 +303,7 @@ __global__ void __launch_bounds__(kPrepThreads) cand_prep_kernel(DevArgs a, int3
   for (int k = lo; k < lo + per && k < pow2; ++k)
     if (keys[k] != INT_MAX && (k == 0 || keys[k] != keys[k - 1])) out[pos++] = keys[k];
   if (tid == 0) a.cand_cnt[t] = total;
+  cand_pages<kPrepThreads>(a, t, total);
 
   consumer_units<kPrepThreads>(a);
 }
@@ -329,6 +358,7 @@ __global__ void __launch_bounds__(kBitmapThreads) cand_bitmap_kernel(DevArgs a, 
     }
   }
   if (tid == 0) a.cand_cnt[t] = total;
+  cand_pages<kBitmapThreads>(a, t, total);
   consumer_units<kBitmapThreads>(a);
 }
 

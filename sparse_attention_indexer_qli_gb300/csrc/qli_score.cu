@@ -427,6 +427,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     c.init(a, u0);
     int issued = 0;
     int32_t pg0 = 0, pg1 = -1;     // dense: this lane's look-ahead tile's pages
+    // consumer: tile k's candidate count, this lane's block and its page,
+    // loaded while tile k-1 was issued (one round trip, off the critical path)
+    int32_t cn_nc = 0, cn_blk = 0, cn_page = 0;
+    uint4 cn_sc = make_uint4(0u, 0u, 0u, 0u);
+    const auto consumer_fetch = [&](const Cursor& at) {
+      const int32_t t = at.t;
+      const int64_t i = static_cast<int64_t>(t) * a.C + at.tile * (kTile / kBlock) + lane;
+      cn_nc = a.cand_cnt[t];
+      if (at.tile * (kTile / kBlock) + lane < a.C) {
+        cn_blk = a.cand_list[i];
+        cn_page = a.cand_page[i];
+        cn_sc = a.cand_sc[i];
+      }
+    };
+    if (consumer && nk > 0) consumer_fetch(c);
     for (int k = 0; k < nk && ok; ++k) {
       const int s = k % kKStages;
       const uint32_t ph = (k / kKStages) & 1;
@@ -491,28 +506,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           }
         }
       } else {
-        const int32_t t = c.t, b = a.tok_b[t];
-        const int64_t bt_row = static_cast<int64_t>(b) * a.bt_stride;
-        const int32_t nc = a.cand_cnt[t];
+        // pages were looked up (and range-checked) by the candidate kernel
         const int32_t first = c.tile * (kTile / kBlock);
-        const int32_t nblk = min(kTile / kBlock, nc - first);
-        if (lane == 0) mbar_arrive_expect_tx(&S.full[s], nblk * (kBlock * kHeadDim + kBlock * 2));
+        const int32_t nblk = min(kTile / kBlock, cn_nc - first);
+        const int32_t blk = cn_blk, page = cn_page;
+        // the block's scales (gathered by the candidate kernel) go to the
+        // stage by plain stores, ordered before lane 0's arrival on it
+        if (lane < nblk) *reinterpret_cast<uint4*>(&S.sc[s][lane * kBlock * 2]) = cn_sc;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[s], nblk * (kBlock * kHeadDim));
         __syncwarp();
         if (lane < nblk) {
-          const int32_t blk = a.cand_list[static_cast<int64_t>(t) * a.C + first + lane];
-          const int32_t pos0 = blk * kBlock;
-          int32_t page = a.bt[bt_row + pos0 / a.R];
-          if (page < 0 || page >= a.num_pages) {
-            atomicOr(a.err, QLI_DEVERR_PAGE);
-            page = 0;
-          }
-          const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
-          const int32_t row = pos0 % a.R;
+          const int32_t row = (blk * kBlock) % a.R;
           tma_load_3d_hint(&S.k[s][lane * kBlock * kHeadDim], &tm_blk, 0, row, page, &S.full[s], kpol);
-          bulk_g2s_hint(&S.sc[s][lane * kBlock * 2], pg + a.s_off + row * 2, kBlock * 2, &S.full[s],
-                        kpol);
         }
         c.next(a, u0 + k + 1);
+        if (k + 1 < nk) consumer_fetch(c);
       }
       __syncwarp();
       ++issued;
