@@ -36,6 +36,12 @@ UNIT = "pairs/s"
 L2_BYTES = 129 * 1024 * 1024
 ROTATE_SETS = {1: 1, 2: 3, 3: 1, 4: 8, 5: 1}   # input sets cycled so a step never hits L2
 SCORE_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_score.cu")
+PREFILL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_prefill.cu")
+# workload -> (committed ncu summary, the kernel source it was taken on)
+PROFILES = {
+    2: ("stream_kernel_decode_b64_ratio1.md", SCORE_SRC, "score_source_sha256"),
+    3: ("prefill_kernel_prefill_t4096_2x2048.md", PREFILL_SRC, "prefill_source_sha256"),
+}
 
 
 # ---------------------------------------------------------------- accounting
@@ -162,13 +168,13 @@ def roofline(idx, sets, args, score_ms_avg):
         achieved = flops / (score_ms_avg / 1e3) / 1e12
         peak, kind = tensor_peak()
         return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "kernel": "prefill_kernel",
+                "frac": achieved / peak, "traffic": profiled_traffic(idx), "kernel": "prefill_kernel",
                 "peak_source": kind, "kernel_ms": score_ms_avg, "algorithmic_flops": flops}
     alg = sum(score_algorithmic_bytes(c, p) for c, _, p in chosen) / len(chosen)
     achieved = alg / (score_ms_avg / 1e3) / 1e9
     peak, kind = peaks()
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(), "kernel": "stream_kernel",
+            "frac": achieved / peak, "traffic": profiled_traffic(idx), "kernel": "stream_kernel",
             "peak_source": kind, "kernel_ms": score_ms_avg, "algorithmic_bytes": alg}
 
 
@@ -181,18 +187,22 @@ def tensor_peak():
     return 1900.0, "fallback"
 
 
-def profiled_traffic():
-    """Per-launch DRAM traffic of the score kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "stream_kernel_decode_b64_ratio1.md")
+def profiled_traffic(idx):
+    """Per-launch DRAM traffic of the workload's score kernel from its
+    committed ncu summary, if there is one for this workload and it was taken
+    on the current kernel source; else None."""
+    if idx not in PROFILES:
+        return None
+    name, src, key = PROFILES[idx]
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
-    h = re.search(r"score_source_sha256:\s*([0-9a-f]{64})", txt)
+    h = re.search(key + r":\s*([0-9a-f]{64})", txt)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(SCORE_SRC, "rb").read()).hexdigest()
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
     return int(m.group(1)) if h.group(1) == cur else None
 
 
