@@ -10,12 +10,16 @@
 // [1, 2048], candidate blocks in [64, 2048].
 //
 // Ranking reading: higher score first, equal scores (with -0 == +0) by the
-// lower position / block ID. The selected entries are found with an exact
-// radix select over order-preserving 32-bit keys, digit by digit below the
-// bits that every eligible key of the row shares, then written in position
-// order by two warp-segmented sweeps, so no sort is needed. Rows that fit are
-// first copied into shared memory as keys, so the passes never go back to
-// L2; longer rows are read from L2 on every pass.
+// lower position / block ID. Scores are compared as order-preserving 32-bit
+// keys. A row's threshold bin comes from a 4096-bin histogram of the keys'
+// top 12 bits (built by the decode score stage, or counted here in shared
+// memory for prefill rows); one pass compacts the entries at or above that
+// bin in row order, an exact refine on the remaining 20 bits (10-bit digits)
+// finds the want-th key, and two warp-segmented sweeps write the IDs in
+// position order, so no sort is needed. Rows longer than one CTA's shared
+// memory are compacted chunk by chunk by lcompact_kernel first. When a bin
+// holds more candidates than the scratch space, the whole row is ranked by a
+// digit-by-digit radix select below the bits its eligible keys share.
 #include <cuda_fp16.h>
 
 #include "qli_internal.h"
