@@ -147,6 +147,18 @@ def test_consumer_all_blocks_equals_none_on_gpu():
     assert np.array_equal(g_cons["indices"], g_none["indices"])
 
 
+def test_consumer_beyond_the_bitmap_takes_the_sorting_path():
+    # a block table wide enough that a request could hold more blocks than
+    # the candidate kernel's shared-memory bitmap covers (66000 x 64
+    # positions > 16384 x 32 x 8): the candidates are sorted by the bitonic
+    # fallback, which also looks up their pages and scales
+    case = synth.make_case(11, [3000, 1700], [2, 1], N=32, ratio=2, topk=100,
+                           cand_mode="consumer", cand_blocks=128, bt_stride=66000,
+                           cand_policy="messy", name="consumer-wide-table")
+    assert case.bt_stride * case.rows_per_page > 16384 * 32 * 8
+    check(case)
+
+
 def test_device_checks_flag_bad_metadata():
     import torch
     case = synth.make_case(8, [500, 300], [1, 1], N=64, ratio=2, topk=16)
