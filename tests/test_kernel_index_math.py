@@ -1,0 +1,131 @@
+"""The index and bit arithmetic the score and selection kernels rely on,
+restated in Python from the kernels' algorithms and checked against plain
+definitions (the GPU parity tests check the kernels themselves):
+
+- keep test: order_key(x) >= t_lo is one unsigned compare on the raw FP32
+  bits, (u - lo) <= span, for every threshold that can occur (the start of
+  any of the 4096 top-12-bit bins);
+- unit search: a warp probing 32 tile prefixes per round trip finds the same
+  (token, tile) as a scalar binary search;
+- look-ahead: 32 consecutive tiles' tokens found from one load of the next
+  32 token boundaries and a shuffle search, with the batch-to-batch hand-off
+  the producer uses, including tokens with no tiles.
+"""
+import random
+
+import numpy as np
+
+M32 = 0xFFFFFFFF
+
+
+def order_key(u):
+    """Order-preserving key of the FP32 bit pattern u (-0 as +0)."""
+    u = np.asarray(u, dtype=np.uint64)
+    u = np.where((u << np.uint64(1)) & np.uint64(M32) == 0, np.uint64(0), u)
+    neg = (u & np.uint64(0x80000000)) != 0
+    return np.where(neg, (~u) & np.uint64(M32), u | np.uint64(0x80000000))
+
+
+def keep_range(t_lo):
+    if t_lo >= 0x80000000:
+        lo = t_lo - 0x80000000
+        span = 0x80000000 if lo == 0 else 0x7FFFFFFF - lo
+    else:
+        lo, span = 0, (~t_lo) & M32
+    return lo, span
+
+
+def test_keep_range_equals_the_key_compare():
+    rng = np.random.default_rng(0)
+    u = np.concatenate([rng.integers(0, 1 << 32, 200000, dtype=np.uint64),
+                        np.array([0, 0x80000000, 0x7F800000, 0xFF800000, 0x7FC00000, 0xFFFFFFFF,
+                                  1, 0x80000001, 0x7FFFFFFF], dtype=np.uint64)])
+    k = order_key(u)
+    for b in range(4096):
+        t_lo = b << 20
+        lo, span = keep_range(t_lo)
+        fast = ((u - np.uint64(lo)) & np.uint64(M32)) <= np.uint64(span)
+        assert np.array_equal(fast, k >= np.uint64(t_lo)), b
+
+
+def scalar_search(us, T, u):
+    lo, hi = 0, T - 1
+    while lo < hi:
+        mid = (lo + hi + 1) >> 1
+        if us[mid] <= u:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo, u - us[lo]
+
+
+def warp_search(us, T, u):
+    lo, hi = 0, T
+    while hi - lo > 1:
+        step = (hi - lo + 31) >> 5
+        n = sum(1 for lane in range(32)
+                if lo + (lane + 1) * step < hi and us[lo + (lane + 1) * step] <= u)
+        lo += n * step
+        hi = min(hi, lo + step)
+    return lo, u - us[lo]
+
+
+def shuffle_count(nb, uj):
+    n = 0
+    for w in (16, 8, 4, 2, 1):
+        if nb[n + w - 1] <= uj:
+            n += w
+    if nb[n] <= uj:
+        n += 1
+    return n
+
+
+def layouts(seed, count):
+    rng = random.Random(seed)
+    for _ in range(count):
+        T = rng.randint(1, 700)
+        tiles = [rng.randint(0, 5) if rng.random() < 0.5 else rng.randint(0, 300) for _ in range(T)]
+        if rng.random() < 0.3:
+            tiles = [t if rng.random() < 0.5 else 0 for t in tiles]
+        if sum(tiles) == 0:
+            tiles[rng.randrange(T)] = 1
+        us = [0]
+        for t in tiles:
+            us.append(us[-1] + t)
+        yield T, us, rng.randint(1, 160)
+
+
+def test_warp_search_equals_scalar_search():
+    for T, us, G in layouts(1, 300):
+        U = us[T]
+        for g in range(G):
+            u0 = U * g // G
+            if u0 < U:
+                assert warp_search(us, T, u0) == scalar_search(us, T, u0)
+
+
+def test_look_ahead_places_every_tile():
+    for T, us, G in layouts(2, 300):
+        U = us[T]
+        for g in range(G):
+            u0, u1 = U * g // G, U * (g + 1) // G
+            nk = u1 - u0
+            if nk <= 0:
+                continue
+            ct, ctile = warp_search(us, T, u0)
+            for k in range(0, nk, 32):
+                nb = [us[ct + 1 + l] if ct + 1 + l <= T else 0x7FFFFFFF for l in range(32)]
+                got = []
+                for lane in range(32):
+                    uj = u0 + k + lane
+                    cnt = shuffle_count(nb, uj)
+                    if k + lane >= nk:
+                        got.append((ct, 0))
+                    elif cnt < 32:
+                        below = nb[cnt - 1] if cnt > 0 else u0 + k - ctile
+                        got.append((ct + cnt, uj - below))
+                    else:
+                        got.append(scalar_search(us, T, uj))
+                for lane in range(min(32, nk - k)):
+                    assert got[lane] == scalar_search(us, T, u0 + k + lane)
+                ct, ctile = got[31][0], got[31][1] + 1
