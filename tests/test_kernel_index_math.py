@@ -129,3 +129,65 @@ def test_look_ahead_places_every_tile():
                 for lane in range(min(32, nk - k)):
                     assert got[lane] == scalar_search(us, T, u0 + k + lane)
                 ct, ctile = got[31][0], got[31][1] + 1
+
+
+def packed_offsets(keep):
+    """compact_short's placement: keep[t][c] is thread t's 4-bit keep mask in
+    chunk c (1024 threads, 8 chunks). Per-chunk counts travel as 8-bit fields
+    (chunks 0-3 and 4-7 in two words) through a warp inclusive scan, and as
+    16-bit fields (widened from each warp's total) through a scan across the
+    32 warps; a kept entry's output index is (entries of earlier chunks) +
+    (chunk c in earlier warps) + (chunk c in earlier lanes) + (earlier bits)."""
+    T, C = len(keep), len(keep[0])
+    mine = [[0, 0] for _ in range(T)]
+    for t in range(T):
+        for c in range(C):
+            mine[t][c >> 2] |= bin(keep[t][c]).count("1") << (8 * (c & 3))
+    incl = [[0, 0] for _ in range(T)]
+    for w in range(T // 32):
+        acc = [0, 0]
+        for l in range(32):
+            t = 32 * w + l
+            for h in range(2):
+                acc[h] = (acc[h] + mine[t][h]) & M32
+                assert all(((acc[h] >> (8 * f)) & 0xFF) <= 128 for f in range(4))
+                incl[t][h] = acc[h]
+    nw = T // 32
+    wide = []
+    for w in range(nw):
+        lo, hi = incl[32 * w + 31]
+        wide.append([(lo & 0xFF) | (((lo >> 8) & 0xFF) << 16), ((lo >> 16) & 0xFF) | ((lo >> 24) << 16),
+                     (hi & 0xFF) | (((hi >> 8) & 0xFF) << 16), ((hi >> 16) & 0xFF) | ((hi >> 24) << 16)])
+    wincl, acc = [], [0, 0, 0, 0]
+    for w in range(nw):
+        acc = [(acc[h] + wide[w][h]) & M32 for h in range(4)]
+        assert all(((acc[h] >> (16 * f)) & 0xFFFF) <= 4096 for h in range(4) for f in range(2))
+        wincl.append(list(acc))
+    out = {}
+    for t in range(T):
+        w = t // 32
+        total = 0
+        for c in range(C):
+            shift = 16 * (c & 1)
+            tot_c = (wincl[nw - 1][c >> 1] >> shift) & 0xFFFF
+            bw = ((wincl[w][c >> 1] - wide[w][c >> 1]) >> shift) & 0xFFFF
+            bt = ((incl[t][c >> 2] - mine[t][c >> 2]) >> (8 * (c & 3))) & 0xFF
+            at = total + bw + bt
+            total += tot_c
+            for j in range(4):
+                if keep[t][c] >> j & 1:
+                    out[(c, t, j)] = at
+                    at += 1
+    return out
+
+
+def test_packed_scans_place_entries_in_row_order():
+    rng = random.Random(5)
+    for trial in range(12):
+        dens = rng.choice([0.0, 0.02, 0.1, 0.5, 1.0])
+        keep = [[sum(1 << j for j in range(4) if rng.random() < dens) for _ in range(8)]
+                for _ in range(1024)]
+        got = packed_offsets(keep)
+        # row order: chunk c covers entries c*4096 + 4t + j
+        order = sorted(got, key=lambda e: e[0] * 4096 + 4 * e[1] + e[2])
+        assert [got[e] for e in order] == list(range(len(order)))
