@@ -34,6 +34,7 @@ class _In(ctypes.Structure):
         ("ratio", ctypes.c_int32), ("topk", ctypes.c_int32),
         ("cand_mode", ctypes.c_int32), ("cand_blocks", ctypes.c_int32),
         ("cand_in", ctypes.c_void_p),
+        ("quant_mode", ctypes.c_int32),
     ]
 
 
@@ -69,6 +70,12 @@ def lib():
         L.oracle_dot.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
         L.oracle_pair_score.restype = ctypes.c_float
         L.oracle_pair_score.argtypes = [ctypes.POINTER(_In), ctypes.c_int32, ctypes.c_int64]
+        L.oracle_e4m3_to_f64.restype = ctypes.c_double
+        L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_dot_e4m3.restype = ctypes.c_float
+        L.oracle_dot_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+        L.oracle_head_term_f8.restype = ctypes.c_float
+        L.oracle_head_term_f8.argtypes = [ctypes.c_float, ctypes.c_uint16, ctypes.c_uint16]
         _lib = L
     return _lib
 
@@ -93,7 +100,9 @@ class Prepared:
             self.keep.append(a)
             return a
 
-        q = c(case.q, np.int8)
+        # FP8 cases carry E4M3 bit patterns: the bytes are passed unchanged
+        q = c(np.asarray(case.q).view(np.int8) if np.asarray(case.q).dtype == np.uint8 else case.q,
+              np.int8)
         T, N, D = q.shape
         pages = np.ascontiguousarray(pages)
         self.keep.append(pages)
@@ -115,6 +124,7 @@ class Prepared:
         s.ratio = case.ratio; s.topk = case.topk
         s.cand_mode = MODES[mode]; s.cand_blocks = case.cand_blocks
         s.cand_in = _ptr(c(cin, np.int32))
+        s.quant_mode = int(getattr(case, "quant_mode", 2))
         self.s = s
         self.T = T
         self.topk = case.topk
@@ -184,6 +194,23 @@ def pair_score(prep: Prepared, t: int, j: int) -> float:
     return float(lib().oracle_pair_score(ctypes.byref(prep.s), int(t), int(j)))
 
 
+# ---- FP8 (quant mode 1): E4M3 codes ----------------------------------------
+
+def e4m3_to_f64(code: int) -> float:
+    return float(lib().oracle_e4m3_to_f64(int(code)))
+
+
+def dot_e4m3(q_codes: np.ndarray, k_codes: np.ndarray) -> float:
+    q = np.ascontiguousarray(q_codes, dtype=np.uint8)
+    k = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    assert q.size == k.size
+    return float(lib().oracle_dot_e4m3(_ptr(q), _ptr(k), q.size))
+
+
+def head_term_f8(s: float, w_bits: int, qs_bits: int) -> float:
+    return float(lib().oracle_head_term_f8(float(s), int(w_bits), int(qs_bits)))
+
+
 # ---- query quantiser and index-K writer (qli_quant_oracle.c) ---------------
 
 QUANT_ERRORS = {-1: "invalid argument", -2: "non-finite input", -5: "slot out of range"}
@@ -214,6 +241,27 @@ def quantize_rows(x_bf16: np.ndarray):
     if rc != 0:
         raise OracleError(QUANT_ERRORS.get(rc, str(rc)))
     return q, s
+
+
+def quantize_rows_e4m3(x_bf16: np.ndarray):
+    """FP8 variant: per-row E4M3 quantisation of BF16 rows (uint16 bit
+    patterns, shape [..., D]). Returns (codes uint8 [..., D] E4M3 bits,
+    scales uint16 [...] FP16 bits)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    D = x.shape[-1]
+    rows = x.size // D if D else 0
+    c = np.empty(x.shape, dtype=np.uint8)
+    s = np.empty(x.shape[:-1], dtype=np.uint16)
+    f = _quant_fn("oracle_quantize_rows_e4m3", ctypes.c_int,
+                  [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p])
+    rc = f(_ptr(x), rows, D, _ptr(c), _ptr(s))
+    if rc != 0:
+        raise OracleError(QUANT_ERRORS.get(rc, str(rc)))
+    return c, s
+
+
+def f32_to_e4m3(x: float) -> int:
+    return int(_quant_fn("oracle_f32_to_e4m3", ctypes.c_uint8, [ctypes.c_float])(float(x)))
 
 
 def write_index_k(k_bf16: np.ndarray, slot: np.ndarray, pages: np.ndarray, rows_per_page: int,

@@ -44,11 +44,14 @@
  * position, ties between blocks to the lower block ID; a source's position
  * TopK ranges over all visible positions; a consumer uses the given IDs as a
  * set (duplicates, order, -1 and IDs with no visible position are ignored)
- * and does not add the last block itself.
+ * and does not add the last block itself. Quant mode 1 (FP8, not in the A3
+ * contract): E4M3 codes, the exact dot rounded once to FP32, then the same
+ * chain (see the FP8 section below).
  *
  * FP16 arithmetic uses the C _Float16 type (IEEE binary16, round to nearest
  * even). Build with -ffp-contract=off and without -ffast-math.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -81,6 +84,7 @@ typedef struct oracle_in {
     const uint16_t *q_scale;      /* FP16 bits [T, N] */
     int32_t ratio, topk, cand_mode, cand_blocks;
     const int32_t *cand_in;     /* [T, 1, C] consumer input */
+    int32_t quant_mode;         /* 2: INT8 Q/K (the A3 contract); 1: FP8 E4M3 codes */
 } oracle_in;
 
 /* ---- FP16 helpers (IEEE binary16 through _Float16) ---------------------- */
@@ -147,12 +151,51 @@ int32_t oracle_dot(const int8_t *qh, const int8_t *k, int32_t D) {
     return s;
 }
 
-/* One head's FP16 term: fp16(relu(fp16(s / 1024)) * fp16(w * q_scale)). */
-float oracle_head_term(int32_t s, uint16_t w_bits, uint16_t qs_bits) {
-    float x = oracle_f16_to_f32(oracle_f32_to_f16((float)s / 1024.0f)); /* INT32/1024 -> FP16 */
+/* The chain after the FP16 rounding: fp16(relu(x) * fp16(w * q_scale)). */
+static float chain_from_x(float x, uint16_t w_bits, uint16_t qs_bits) {
     float r = x > 0.0f ? x : 0.0f;                                       /* FP16 ReLU */
     float wq = f16_mul(oracle_f16_to_f32(w_bits), oracle_f16_to_f32(qs_bits)); /* FP16 w*qs */
     return f16_mul(r, wq);                                               /* FP16 product */
+}
+
+/* One head's FP16 term: fp16(relu(fp16(s / 1024)) * fp16(w * q_scale)). */
+float oracle_head_term(int32_t s, uint16_t w_bits, uint16_t qs_bits) {
+    float x = oracle_f16_to_f32(oracle_f32_to_f16((float)s / 1024.0f)); /* INT32/1024 -> FP16 */
+    return chain_from_x(x, w_bits, qs_bits);
+}
+
+/* ---- FP8 variant (quant mode 1) ------------------------------------------
+ * [G/compile-scope] lists FP8 as quant mode 1 of the A5 build's dtype
+ * registration; the pages print no golden for it. Reading taken: the codes
+ * are OCP E4M3 ("fn": bias 7, no infinities, 0x7F / 0xFF are NaN, largest
+ * finite 448) in the same byte layout as the INT8 codes, with the same FP16
+ * per-head Q scale and per-position K scale, and the A3 chain from the
+ * division by 1024 on; the INT32 dot becomes the exact dot of the decoded
+ * codes rounded once to FP32. The exact dot needs no accumulation order:
+ * every product is a multiple of 2^-18 below 2^18, so any sum of 128 of them
+ * is an integer multiple of 2^-18 below 2^43, exact in double. */
+
+/* Value of an E4M3 code (NaN codes decode to NaN). */
+double oracle_e4m3_to_f64(uint8_t c) {
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);            /* subnormal: m/8 * 2^-6 */
+    else v = ldexp(8.0 + m, e - 10);                 /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* The exact dot of two rows of E4M3 codes, rounded once to FP32. */
+float oracle_dot_e4m3(const uint8_t *qh, const uint8_t *k, int32_t D) {
+    double s = 0.0;
+    for (int32_t d = 0; d < D; ++d) s += oracle_e4m3_to_f64(qh[d]) * oracle_e4m3_to_f64(k[d]);
+    return (float)s;
+}
+
+/* The FP8 head term: the A3 chain applied to the FP32 dot. */
+float oracle_head_term_f8(float s, uint16_t w_bits, uint16_t qs_bits) {
+    float x = oracle_f16_to_f32(oracle_f32_to_f16(s / 1024.0f));       /* /1024 exact, -> FP16 */
+    return chain_from_x(x, w_bits, qs_bits);
 }
 
 /* Score of (token t of request b, compressed position j). */
@@ -161,9 +204,13 @@ static float pair_score(const oracle_in *in, int32_t t, int32_t b, int64_t j) {
     float acc = 0.0f;                                 /* FP32 head reduction */
     for (int32_t h = 0; h < in->N; ++h) {
         const int8_t *qh = in->q + (int64_t)t * in->q_stride_t + (int64_t)h * in->q_stride_h;
-        int32_t s = oracle_dot(qh, k, in->D);
-        acc = acc + oracle_head_term(s, in->head_weights[(int64_t)t * in->N + h],
-                                     in->q_scale[(int64_t)t * in->N + h]);
+        const uint16_t w = in->head_weights[(int64_t)t * in->N + h];
+        const uint16_t qs = in->q_scale[(int64_t)t * in->N + h];
+        if (in->quant_mode == 1)
+            acc = acc + oracle_head_term_f8(
+                            oracle_dot_e4m3((const uint8_t *)qh, (const uint8_t *)k, in->D), w, qs);
+        else
+            acc = acc + oracle_head_term(oracle_dot(qh, k, in->D), w, qs);
     }
     return acc * oracle_f16_to_f32(k_scale(in, b, j)); /* then the K scale */
 }
@@ -217,6 +264,7 @@ int oracle_qli(const oracle_in *in, const int32_t *rows, int32_t nrows,
                int32_t *idx_out, int32_t *cand_out, float *scores,
                int64_t score_stride, int64_t *visible, int32_t nthreads) {
     if (!in || !rows || !idx_out || in->D <= 0 || in->N <= 0) return ORACLE_ERR_ARG;
+    if (in->quant_mode != 1 && in->quant_mode != 2) return ORACLE_ERR_ARG;
     if (in->ratio == 1 && in->residual) return ORACLE_ERR_RESIDUAL_WITH_RATIO1;
     if (in->cand_mode == 3 && !in->cand_in) return ORACLE_ERR_CONSUMER_WITHOUT_SOURCE;
     if (in->cand_mode == 2 && !cand_out) return ORACLE_ERR_ARG;

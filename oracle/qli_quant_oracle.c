@@ -64,9 +64,10 @@ static uint16_t f16_bits(_Float16 h) {
     return b;
 }
 
-/* One row: D BF16 values -> D INT8 codes and the FP16 scale bits. Returns 0,
- * or QORACLE_ENONFINITE for a row holding an Inf or NaN. */
-int oracle_quant_row(const uint16_t *x, int32_t D, int8_t *q, uint16_t *scale_bits) {
+/* A row's absmax and its FP16 scale s = FP16(amax / levels): FP32 quotient,
+ * then RN-even to binary16, capped at the largest finite FP16. Returns 0, or
+ * QORACLE_ENONFINITE for a row holding an Inf or NaN. */
+static int row_scale(const uint16_t *x, int32_t D, float levels, _Float16 *s_out) {
     float amax = 0.0f;
     for (int32_t d = 0; d < D; ++d) {
         const float v = oracle_bf16_to_f32(x[d]);
@@ -74,9 +75,19 @@ int oracle_quant_row(const uint16_t *x, int32_t D, int8_t *q, uint16_t *scale_bi
         const float a = fabsf(v);
         if (a > amax) amax = a;
     }
-    const float quotient = amax / 127.0f;
+    const float quotient = amax / levels;
     _Float16 s = (_Float16)quotient;                 /* RN-even to binary16 */
     if (isinf((float)s)) s = (_Float16)65504.0f;     /* largest finite FP16 */
+    *s_out = s;
+    return QORACLE_OK;
+}
+
+/* One row: D BF16 values -> D INT8 codes and the FP16 scale bits. Returns 0,
+ * or QORACLE_ENONFINITE for a row holding an Inf or NaN. */
+int oracle_quant_row(const uint16_t *x, int32_t D, int8_t *q, uint16_t *scale_bits) {
+    _Float16 s;
+    const int e = row_scale(x, D, 127.0f, &s);
+    if (e) return e;
     const float sf = (float)s;
     if (sf == 0.0f) {
         memset(q, 0, (size_t)D);
@@ -100,6 +111,71 @@ int oracle_quantize_rows(const uint16_t *x, int64_t rows, int32_t D, int8_t *q,
     if (rows < 0 || D <= 0 || (rows > 0 && (!x || !q || !scales))) return QORACLE_EINVAL;
     for (int64_t r = 0; r < rows; ++r) {
         const int e = oracle_quant_row(x + r * D, D, q + r * D, scales + r);
+        if (e) return e;
+    }
+    return QORACLE_OK;
+}
+
+/* ---- FP8 (E4M3) variant -------------------------------------------------
+ * Quant mode 1, which the pages only name (A5 dtype registration). Reading:
+ * the same symmetric absmax scheme with E4M3's largest finite value 448 in
+ * place of 127:
+ *     s   = FP16(amax / 448)            (FP32 quotient, then RN; capped at 65504)
+ *     c_d = E4M3(x_d / s)               (FP32 quotient, RN-even, saturated to +-448)
+ * s rounding to zero gives codes 0 (+0) and scale +0. */
+
+/* E4M3 code of a finite FP32 value: round to nearest even on the E4M3 grid
+ * (quantum 2^-9 below 2^-6, 2^(e-3) in binade [2^e, 2^(e+1))), magnitudes
+ * past 448 saturated to 448. */
+uint8_t oracle_f32_to_e4m3(float v) {
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;
+    int e;
+    (void)frexp(a, &e);                  /* a = f * 2^e, f in [0.5, 1): binade 2^(e-1) */
+    int binade = e - 1;
+    if (a == 0.0 || binade < -6) binade = -6;    /* subnormal range shares the quantum 2^-9 */
+    const double quantum = ldexp(1.0, binade - 3);
+    double n = nearbyint(a / quantum);   /* exact division; current mode: to even */
+    double r = n * quantum;
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    /* encode r, exactly on the grid */
+    int er;
+    (void)frexp(r, &er);
+    int b = er - 1;
+    uint8_t code;
+    if (b < -6) {
+        code = (uint8_t)(r / ldexp(1.0, -9));                 /* subnormal: m * 2^-9 */
+    } else {
+        const int m = (int)(r / ldexp(1.0, b - 3)) - 8;       /* (8 + m) * 2^(b-3) */
+        code = (uint8_t)(((b + 7) << 3) | m);
+    }
+    return sign | code;
+}
+
+/* One row: D BF16 values -> D E4M3 codes and the FP16 scale bits. Returns 0,
+ * or QORACLE_ENONFINITE for a row holding an Inf or NaN. */
+int oracle_quant_row_e4m3(const uint16_t *x, int32_t D, uint8_t *c, uint16_t *scale_bits) {
+    _Float16 s;
+    const int e = row_scale(x, D, 448.0f, &s);
+    if (e) return e;
+    const float s8 = (float)s;
+    if (s8 == 0.0f) {
+        memset(c, 0, (size_t)D);
+        *scale_bits = 0;
+        return QORACLE_OK;
+    }
+    for (int32_t d = 0; d < D; ++d) c[d] = oracle_f32_to_e4m3(oracle_bf16_to_f32(x[d]) / s8);
+    *scale_bits = f16_bits(s);
+    return QORACLE_OK;
+}
+
+int oracle_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int32_t D, uint8_t *c,
+                              uint16_t *scales) {
+    if (rows < 0 || D <= 0 || (rows > 0 && (!x || !c || !scales))) return QORACLE_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int e = oracle_quant_row_e4m3(x + r * D, D, c + r * D, scales + r);
         if (e) return e;
     }
     return QORACLE_OK;
