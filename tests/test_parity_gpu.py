@@ -12,12 +12,11 @@ import numpy as np
 import pytest
 
 import oracle
+from parity_rules import REL_TIE_TOL, assert_selection  # noqa: F401
 from sparse_attention_indexer_qli_gb300 import build as libbuild
 from sparse_attention_indexer_qli_gb300 import qli, synth
 
 pytestmark = pytest.mark.gpu
-
-REL_TIE_TOL = 1e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,16 +48,8 @@ def consumer_slots(case, t, V):
     return ids[(ids >= 0) & (ids < nb)]
 
 
-def assert_selection(gpu_row, ora_row, score_of, what):
-    if np.array_equal(gpu_row, ora_row):
-        return
-    g = set(gpu_row[gpu_row >= 0].tolist())
-    o = set(ora_row[ora_row >= 0].tolist())
-    assert len(g) == len(o), (what, len(g), len(o))
-    assert np.all(np.diff(gpu_row[gpu_row >= 0]) > 0), what
-    bound = min(score_of(j) for j in o)
-    for j in g ^ o:
-        assert abs(score_of(j) - bound) <= REL_TIE_TOL * abs(bound), (what, j, score_of(j), bound)
+def cand_width(case):
+    return case.cand_blocks
 
 
 def check(case, rows=None, scores=True):
@@ -73,17 +64,29 @@ def check(case, rows=None, scores=True):
         V = int(ora["visible"][r])
         osc = ora["scores"][r]
 
+        nb = (V + 7) // 8
+        if case.cand_mode == "consumer":
+            in_set = set(consumer_slots(case, t, V).tolist())
+        else:
+            in_set = None
+
         def score_of(j):
             return float(osc[j])
 
-        assert_selection(gpu["indices"][t], ora["indices"][r], score_of, ("indices", int(t)))
-        if case.cand_mode == "source":
-            nb = (V + 7) // 8
+        def eligible(j):
+            return 0 <= j < V and (in_set is None or j // 8 in in_set)
 
+        assert_selection(gpu["indices"][t], ora["indices"][r], score_of, eligible,
+                         ("indices", int(t)))
+        if case.cand_mode == "source":
             def bscore(k):
                 return float(osc[8 * k:min(8 * k + 8, V)].max())
 
-            assert_selection(gpu["cand"][t], ora["cand"][r], bscore, ("cand", int(t)))
+            def block_eligible(k):
+                return 0 <= k < nb
+
+            assert_selection(gpu["cand"][t], ora["cand"][r], bscore, block_eligible,
+                             ("cand", int(t)), pinned=nb - 1 if nb > cand_width(case) else None)
             if nb:
                 assert nb - 1 in gpu["cand"][t]
         if not scores or V == 0:
