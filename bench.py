@@ -34,7 +34,9 @@ from sparse_attention_indexer_qli_gb300 import synth  # noqa: E402
 METRIC = "QLI scored (query,position) pairs/s; % of HBM (decode) / INT8 (prefill) roof"
 UNIT = "pairs/s"
 L2_BYTES = 129 * 1024 * 1024
-ROTATE_SETS = {1: 1, 2: 3, 3: 1, 4: 8, 5: 1}   # input sets cycled so a step never hits L2
+# input sets cycled so that a step never finds its index K in L2 (the
+# prefill workload's K is 8.4 MB per set: 16 sets exceed the 129 MB L2)
+ROTATE_SETS = {1: 1, 2: 3, 3: 16, 4: 8, 5: 1}
 SCORE_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_score.cu")
 PREFILL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_prefill.cu")
 # workload -> (committed ncu summary, the kernel source it was taken on)
@@ -248,6 +250,14 @@ def aggregate(ms: float, pairs: float, ws: int, device: str = "cuda"):
     return total / (ms_max / 1e3), ms_max, total
 
 
+def repeats_for(first_ms: float, min_seconds: float, ws: int, cap: int = 500) -> int:
+    """How many times to run the K-step timed region so that about
+    `min_seconds` of GPU time pass in total (the same count on every rank)."""
+    want = 1 if first_ms <= 0 else int(np.ceil(1e3 * min_seconds / first_ms))
+    want = max(1, min(cap, want))
+    return int(reduce_max(float(want), ws))
+
+
 def barrier(ws: int):
     import torch
     torch.cuda.synchronize()
@@ -391,17 +401,46 @@ def run_ours(args):
 
     for k in range(args.warmup):
         whole[k % nsets].replay()
-    # timed region: K whole-call steps
+    # timed region: K whole-call steps, bracketed by a barrier and a
+    # synchronize; the region is repeated (K steps each time) until about
+    # `--min-seconds` of GPU time has run, so that the clock sampler sees the
+    # GPU under load, and the median repeat is reported
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    kbytes = 130 * int(sets[0][0].k_lens.sum())
+    flush = None
+    if nsets * kbytes <= L2_BYTES:
+        # the input sets fit in L2 together: every step is timed on its own
+        # (events around it) after a 256 MB write that evicts the previous
+        # steps' data, outside the events
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+
+    def timed_region():
+        barrier(world)
+        if flush is not None:
+            for k in range(args.steps):
+                flush.fill_(k & 255)
+                step_ev[k][0].record(stream)
+                whole[(args.warmup + k) % nsets].replay()
+                step_ev[k][1].record(stream)
+            torch.cuda.synchronize()
+            barrier(world)
+            return sum(a.elapsed_time(b) for a, b in step_ev)
         start.record(stream)
         for k in range(args.steps):
             whole[(args.warmup + k) % nsets].replay()
         stop.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
-    ms = start.elapsed_time(stop)
+        barrier(world)
+        return start.elapsed_time(stop)
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        region_ms = [timed_region()]
+        repeats = repeats_for(region_ms[0], args.min_seconds, world)
+        for _ in range(repeats - 1):
+            region_ms.append(timed_region())
+    ms = statistics.median(region_ms)
     my_pairs = sum(sets[(args.warmup + k) % nsets][2] for k in range(args.steps))
     value, ms_max, all_pairs = aggregate(ms, my_pairs, world)
 
@@ -451,11 +490,17 @@ def run_ours(args):
             "query_tokens": case0.T, "heads": case0.N, "ratio": case0.ratio,
             "topk": case0.topk, "cand_mode": case0.cand_mode,
             "pairs_per_step": my_pairs / args.steps,
-            "l2": "inputs rotate over %d independent sets, %.0f MB of index K each (L2 129 MB)"
-                  % (nsets, 128 * sets[0][2] / 1e6),
+            "l2": ("inputs larger than L2: the steps rotate over %d independent input sets, "
+                   "%.1f MB of index K (rows and scales) each, %.0f MB in all (L2 129 MB)"
+                   % (nsets, kbytes / 1e6, nsets * kbytes / 1e6)) if flush is None else
+                  ("L2 flushed between steps: a 256 MB write before each step, outside the "
+                   "events that time the step (%.2f MB of index K per step)" % (kbytes / 1e6)),
             "parallelism": "replicas" if world > 1 else "single",
             "launch": "one CUDA graph per input set holding the whole call",
+            "timing": "median of %d repeats of the %d-step timed region (%.0f ms of steps in all)"
+                      % (len(region_ms), args.steps, sum(region_ms)),
         },
+        "repeats": len(region_ms),
         "roofline": roof,
         "stage_ms": stage_ms,
         "cpu_baseline": cpu,
@@ -710,7 +755,10 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5],
+                    help="workload (default 3: the prefill chunk, the largest single-GPU one)")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the timed region until this much GPU time has run")
     ap.add_argument("--op", default="index", choices=["index", "quantize_q", "write_index_k"],
                     help="index: the indexer (default); the others time the query quantiser "
                          "or the index-K cache writer alone")

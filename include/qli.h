@@ -168,8 +168,15 @@ qli_status qli_read_device_error(const void *workspace, uint32_t *host_word, voi
  * QLI_ERR_WORKSPACE_TOO_SMALL without launching anything. All calls share the
  * array and it keeps the previous call's contents (none of them has to start
  * at zero); calls that overlap on the GPU race on it, so issue them in order
- * on one stream. Inputs, outputs, stream and errors are as for qli_run. */
+ * on one stream. Inputs, outputs, stream and host-side errors are as for
+ * qli_run; the device error word is read with qli_read_static_device_error. */
 qli_status qli_run_static(const qli_args *a, void *stream);
+
+/* The device error word (QLI_DEVERR_* bits) of the last qli_run_static call
+ * on the current device, copied to *host_word after waiting for `stream`.
+ * Synchronous; allocates nothing. The next qli_run_static call on the device
+ * resets the word, so read it before issuing another. */
+qli_status qli_read_static_device_error(uint32_t *host_word, void *stream);
 
 /* ---- Query quantiser and index-K cache writer -------------------------------
  * The two steps either side of the indexer's paged gather. The guide's

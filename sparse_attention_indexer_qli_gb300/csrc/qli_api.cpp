@@ -115,12 +115,7 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, std::atomic<uint64_t>
 // every consumer call take the streaming kernel; prefill-shaped calls take
 // the group kernel, which shares each K tile between up to 256/N tokens.
 bool use_stream_path(const qli_args& a) {
-#ifdef QLI_TILE_KERNEL_ONLY
-  (void)a;
-  return false;
-#else
   return a.cand_mode == QLI_CAND_CONSUMER || static_cast<int64_t>(a.T) <= 2 * static_cast<int64_t>(a.B);
-#endif
 }
 
 WsLayout workspace_layout(const qli_args& a) {
@@ -221,11 +216,6 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.unit_start = reinterpret_cast<int32_t*>(w + L.unit_start);
   d.counter = reinterpret_cast<uint32_t*>(w + L.counter);
   d.stream_path = L.stream_path;
-#ifdef QLI_TILE_KERNEL_ONLY
-  d.use_prefill_kernel = 0;   // diagnostic build: one CTA per (tile, group)
-#else
-  d.use_prefill_kernel = 1;
-#endif
   d.lext = reinterpret_cast<uint32_t*>(w + L.lext);
   d.lhist = reinterpret_cast<uint32_t*>(w + L.lhist);
   d.lcount = reinterpret_cast<int32_t*>(w + L.lcount);

@@ -87,7 +87,6 @@ struct DevArgs {
   int64_t cap;         // bt_stride * R: most positions a request can hold
   int32_t stream_path; // 1: one token per tile, persistent streaming kernel
   int32_t num_sms;     // SMs of the device (persistent grids)
-  int32_t use_prefill_kernel;  // group path: persistent prefill kernel (else one CTA per tile)
 };
 
 struct WsLayout {

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     }
     if (lane == 0) {
       for (int j = max(0, k - kStages); j < k; ++j)
-        (void)mbar_wait_bounded(&S.full[j % kStages], (j / kStages) & 1);
+        (void)mbar_wait_drain(&S.full[j % kStages], (j / kStages) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
         mma_commit(&S.bempty);   // the unit's queries are no longer read
       }
-      if (k > 0) (void)mbar_wait_bounded(&S.dfull[(k - 1) & 1], ((k - 1) >> 1) & 1);
+      if (k > 0) (void)mbar_wait_drain(&S.dfull[(k - 1) & 1], ((k - 1) >> 1) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else {

@@ -10,8 +10,17 @@
 
 namespace qli {
 
-// Give up an on-chip wait after this long (ns of %globaltimer).
-constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
+// Give up an on-chip pipeline wait after this long (ns of %globaltimer).
+// A test build lowers it (QLI_WAIT_LIMIT_NS) to check the give-up path.
+#ifndef QLI_WAIT_LIMIT_NS
+#define QLI_WAIT_LIMIT_NS (200ull * 1000ull * 1000ull)
+#endif
+constexpr uint64_t kWaitLimitNs = QLI_WAIT_LIMIT_NS;
+// Waits for a thread's own asynchronous work (TMA copies it issued, MMAs it
+// committed) before teardown. That work completes by itself, so this limit
+// stays long in every build: a role that gave up on its pipeline still
+// drains what it started before the CTA frees TMEM or exits.
+constexpr uint64_t kDrainLimitNs = 200ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -49,14 +58,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false once
+// `limit_ns` have passed without it.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The same for the drain of a thread's own copies or MMAs at teardown.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_bounded(bar, parity, kDrainLimitNs);
 }
 
 // Same, for a whole warp waiting on one barrier: lane 0 probes, the result

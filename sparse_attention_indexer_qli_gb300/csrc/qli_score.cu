@@ -31,13 +31,6 @@
 namespace qli {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 256;
-constexpr int kSmemA = kTile * kHeadDim * 2;        // 32 KB
-constexpr int kSmemB = kMaxMmaN * kHeadDim * 2;     // 64 KB
-constexpr int kSmemWq = kMaxMmaN * 2;
-constexpr int kSmemBytes = 1024 + kSmemA + kSmemB + kSmemWq + 64;
-
 // Byte offset of 16-byte chunk c (8 FP16 values, c in 0..15) of row n in a
 // K-major tile with the 128-byte swizzle: two 64-element K halves of
 // rows*128 bytes each; rows grouped by 8 (1024 B); the chunk index XORed with
@@ -78,156 +71,6 @@ __device__ __forceinline__ uint4 i8x8_to_f16x8_div1024(uint2 v) {
     o[k] = *reinterpret_cast<uint32_t*>(&x);
   }
   return r;
-}
-
-// One CTA scores one tile of 128 positions against one token group.
-//   grid.x = tile, grid.y = token group (none/source) or token (consumer).
-__global__ void __launch_bounds__(kThreads) score_tile_kernel(DevArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kSmemA;
-  __half* s_wq = reinterpret_cast<__half*>(sB + kSmemB);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kSmemB + kSmemWq);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
-
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int tile = blockIdx.x, g = blockIdx.y;
-  const bool consumer = a.mode == QLI_CAND_CONSUMER;
-
-  int32_t t0, cnt, ncand = 0, vmax;
-  if (consumer) {
-    t0 = g;
-    cnt = 1;
-    ncand = a.cand_cnt[t0];
-    vmax = a.tok_V[t0];
-    if (tile * (kTile / kBlock) >= ncand) return;
-  } else {
-    cnt = a.grp_cnt[g];
-    if (cnt == 0) return;
-    t0 = a.grp_t0[g];
-    vmax = a.tok_V[t0 + cnt - 1];   // V grows with the token index
-    if (tile * kTile >= vmax) return;
-  }
-  const int32_t b = a.tok_b[t0];
-  if (b < 0) return;
-  const int n_mma = cnt * a.N;
-
-  if (warp == 0) tmem_alloc(tslot, kTmemCols);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-
-  // B operand: the group's query heads, times 2^-10, and wq = fp16(w * qs)
-  for (int idx = tid; idx < n_mma * 16; idx += kThreads) {
-    const int n = idx >> 4, c = idx & 15;
-    const int gi = n / a.N, h = n % a.N;
-    const int8_t* src = a.q + static_cast<int64_t>(t0 + gi) * a.q_st +
-                        static_cast<int64_t>(h) * a.q_sh + c * 8;
-    const uint2 v = *reinterpret_cast<const uint2*>(src);
-    *reinterpret_cast<uint4*>(sB + sw128_off(n_mma, n, c)) = i8x8_to_f16x8_div1024(v);
-  }
-  for (int n = tid; n < n_mma; n += kThreads) {
-    const int gi = n / a.N, h = n % a.N;
-    const int64_t o = static_cast<int64_t>(t0 + gi) * a.N + h;
-    s_wq[n] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
-  }
-
-  // A operand: row `tid` of the tile is one position
-  const int i = tid;
-  int32_t pos, slot = 0;
-  bool row_ok;
-  if (consumer) {
-    slot = tile * kTile + i;
-    row_ok = slot < ncand * kBlock;
-    const int32_t blk = row_ok ? a.cand_list[static_cast<int64_t>(t0) * a.C + slot / kBlock] : 0;
-    pos = blk * kBlock + (slot & (kBlock - 1));
-    row_ok = row_ok && pos < vmax;
-  } else {
-    pos = tile * kTile + i;
-    row_ok = pos < vmax;
-  }
-  uint4 kv[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) kv[c] = make_uint4(0, 0, 0, 0);
-  __half ks = __ushort_as_half(0);
-  if (row_ok) {
-    const int32_t page = a.bt[static_cast<int64_t>(b) * a.bt_stride + pos / a.R];
-    if (page < 0 || page >= a.num_pages) {
-      atomicOr(a.err, QLI_DEVERR_PAGE);
-      row_ok = false;
-    } else {
-      const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
-      const int r = pos % a.R;
-      const uint4* kr = reinterpret_cast<const uint4*>(pg + a.k_off + r * kHeadDim);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) kv[c] = __ldg(kr + c);
-      ks = __ushort_as_half(*reinterpret_cast<const uint16_t*>(pg + a.s_off + r * 2));
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    *reinterpret_cast<uint4*>(sA + sw128_off(kTile, i, 2 * c)) =
-        i8x8_to_f16x8(make_uint2(kv[c].x, kv[c].y));
-    *reinterpret_cast<uint4*>(sA + sw128_off(kTile, i, 2 * c + 1)) =
-        i8x8_to_f16x8(make_uint2(kv[c].z, kv[c].w));
-  }
-
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-
-  if (tid == 0) {
-    const uint32_t idesc = idesc_f16_m128(static_cast<uint32_t>(n_mma));
-    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-#pragma unroll
-    for (int s = 0; s < kHeadDim / 16; ++s) {
-      const uint32_t kb = s >> 2, koff = (s & 3) * 32;
-      mma_f16_ss(tmem, sdesc_k_sw128(a0 + kb * (kTile * 128) + koff),
-                 sdesc_k_sw128(b0 + kb * (n_mma * 128) + koff), idesc, s > 0 ? 1u : 0u);
-    }
-    mma_commit(bar);
-  }
-  __syncwarp();
-  const bool done = mbar_wait_bounded(bar, 0);
-  tc_fence_after();
-  if (!done) {
-    if (tid == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
-  } else {
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    for (int gi = 0; gi < cnt; ++gi) {
-      const int32_t t = t0 + gi;
-      const int32_t V = a.tok_V[t];
-      float acc = 0.0f;
-      for (int hc = 0; hc < a.N; hc += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(gi * a.N + hc), r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc = head_term_acc(acc, __uint_as_float(r[k]), s_wq[gi * a.N + hc + k]);
-      }
-      const float score = __fmul_rn(acc, __half2float(ks));
-      const bool elig = row_ok && pos < V;
-      float* srow = a.scores + static_cast<int64_t>(t) * a.Lrow;
-      if (elig) srow[consumer ? slot : pos] = score;
-      if (a.mode == QLI_CAND_SOURCE) {
-        // max over the 8 positions of the block (8 consecutive lanes)
-        float m = elig ? score : -INFINITY;
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        if ((i & (kBlock - 1)) == 0 && pos < V)
-          a.bscores[static_cast<int64_t>(t) * a.Brow + pos / kBlock] = m;
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -306,6 +149,9 @@ struct Smem {
   uint64_t full[kKStages], empty[kKStages];
   uint64_t afull[kASlots], afree[kASlots], dfull[kDSlots], dfree[kDSlots];
   uint64_t kready[kSlots];                           // wq / ks of the slot's tile written
+#ifdef QLI_TEST_STALL_EPILOGUE
+  uint64_t never;                                    // test build: nothing arrives here
+#endif
   uint32_t tmem_base;
 };
 constexpr int kSmemBytes = static_cast<int>(sizeof(Smem)) + 1024;
@@ -400,6 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       mbar_init(&S.dfree[s], 4);      // the epilogue group's four warps
     }
     for (int s = 0; s < kSlots; ++s) mbar_init(&S.kready[s], 4);   // converter warps
+#ifdef QLI_TEST_STALL_EPILOGUE
+    mbar_init(&S.never, 1);
+#endif
     fence_mbar_init();
   }
   tc_fence_before();
@@ -529,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     // never leave a copy in flight: wait for the last stages issued
     if (lane == 0) {
       for (int k = max(0, issued - kKStages); k < issued; ++k)
-        (void)mbar_wait_bounded(&S.full[k % kKStages], (k / kKStages) & 1);
+        (void)mbar_wait_drain(&S.full[k % kKStages], (k / kKStages) & 1);
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
   } else if (warp < kConvWarp0) {
@@ -556,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         last = k;
       }
       // this thread's MMAs are complete before the block tears down TMEM
-      if (last >= 0) (void)mbar_wait_bounded(&S.dfull[last % kDSlots], (last / kDSlots) & 1);
+      if (last >= 0) (void)mbar_wait_drain(&S.dfull[last % kDSlots], (last / kDSlots) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else if (warp < kEpiWarp0) {
@@ -659,7 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     c.init(a, u0);
     if (grp == 1) c.next(a, u0 + 1);
     int32_t vt = -1, V = 0;          // V of the current token, loaded once per token
-    for (int k = grp; k < nk; k += 2) {
+#ifdef QLI_TEST_STALL_EPILOGUE
+    // test build only: the group waits on a barrier nothing arrives on, gives
+    // up, and every role that depends on it gives up in turn
+    if (!mbar_wait_warp(&S.never, 0)) ok = false;
+#endif
+    const int k_end = ok ? nk : 0;
+    for (int k = grp; k < k_end; k += 2) {
       const int sd = k % kDSlots;
       if (c.t != vt) {
         vt = c.t;
@@ -794,8 +649,6 @@ bool encode_k_map(const DevArgs& d, int box_rows, CUtensorMap* m) {
 
 std::atomic<uint64_t> g_smem_stream_stream_kernel{0};
 
-std::atomic<uint64_t> g_smem_score_tile_kernel{0};
-
 cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
   if (d.stream_path) {
@@ -808,22 +661,12 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
                    stream::kSmemBytes, s, tm_page, tm_blk, d);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
-  if (d.use_prefill_kernel) return launch_prefill(d, s);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_tile_kernel), kSmemBytes, g_smem_score_tile_kernel);
-  if (e != cudaSuccess) return e;
-  dim3 grid;
-  if (d.mode == QLI_CAND_CONSUMER) {
-    grid = dim3(static_cast<unsigned>(d.C * kBlock / kTile), static_cast<unsigned>(d.T));
-  } else {
-    grid = dim3(static_cast<unsigned>((d.cap + kTile - 1) / kTile), static_cast<unsigned>(d.Gmax));
-  }
-  score_tile_kernel<<<grid, kThreads, kSmemBytes, s>>>(d);
-  return cudaGetLastError();
+  return launch_prefill(d, s);
 }
 
 int score_launches(const DevArgs& d) {
   if (d.T == 0) return 0;
-  return (!d.stream_path && d.use_prefill_kernel) ? prefill_launches(d) : 1;
+  return d.stream_path ? 1 : prefill_launches(d);
 }
 
 }  // namespace qli

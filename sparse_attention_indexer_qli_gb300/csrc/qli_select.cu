@@ -246,9 +246,13 @@ __device__ void radix_threshold(const Row& r, int32_t k, const Stats& st, uint32
 // Writes, in row order, the ids of the entries with key > thr and of the
 // first need_eq entries with key == thr; returns how many. Warp w owns a
 // contiguous segment: one sweep counts, one block prefix places the warps,
-// a second sweep writes.
+// a second sweep writes. At most `cap` ids are written (the room the caller
+// has): the threshold always admits at most that many when it was derived
+// from the row itself, and the bound keeps a row whose score-stage
+// histogram disagrees with its scores (a score stage that gave up a wait)
+// inside its output.
 __device__ int ordered_output(const Row& r, uint32_t thr, int32_t need_eq, int32_t* out,
-                              Shared& sh) {
+                              int32_t cap, Shared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t seg = ((r.len + kWarps - 1) / kWarps + 31) & ~31;
   const int32_t lo = warp * seg, hi = min(r.len, lo + seg);
@@ -279,12 +283,13 @@ __device__ int ordered_output(const Row& r, uint32_t thr, int32_t need_eq, int32
     const unsigned eqm = __ballot_sync(0xffffffffu, eq);
     const bool take = gt || (eq && eq_seen + __popc(eqm & below) < need_eq);
     const unsigned tm = __ballot_sync(0xffffffffu, take);
-    if (take) out[at + __popc(tm & below)] = r.id(s);
+    const int o = at + __popc(tm & below);
+    if (take && o < cap) out[o] = r.id(s);
     at += __popc(tm);
     eq_seen += __popc(eqm);
   }
   __syncthreads();
-  return total_gt + min(need_eq, total_eq);
+  return min(total_gt + min(need_eq, total_eq), cap);
 }
 
 // Indices s (in row order) of the entries with key >= t_lo, into idx[];
@@ -825,7 +830,7 @@ __device__ void refine_threshold(const uint32_t* ckeys, int n, uint32_t sel, int
 __device__ __noinline__ int select_ascending(const Row& r, int32_t want, int32_t* out, Shared& sh,
                                          uint32_t* scratch, const Stats* known = nullptr) {
   const Stats st = known ? *known : row_stats(r, sh);
-  if (st.E <= static_cast<uint32_t>(want)) return ordered_output(r, 0u, 0, out, sh);
+  if (st.E <= static_cast<uint32_t>(want)) return ordered_output(r, 0u, 0, out, want, sh);
   if (scratch != nullptr && r.cached != nullptr && r.idx == nullptr && r.ids == nullptr &&
       r.len >= 4 * want && r.len > 2 * kSampleKeys) {
     // sample of kSampleKeys evenly spaced keys (one per thread)
@@ -856,14 +861,14 @@ __device__ __noinline__ int select_ascending(const Row& r, int32_t want, int32_t
         uint32_t thr;
         int32_t need_eq;
         radix_threshold(cr, want, cs, thr, need_eq, sh);
-        return ordered_output(cr, thr, need_eq, out, sh);
+        return ordered_output(cr, thr, need_eq, out, want, sh);
       }
     }
   }
   uint32_t thr;
   int32_t need_eq;
   radix_threshold(r, want, st, thr, need_eq, sh);
-  return ordered_output(r, thr, need_eq, out, sh);
+  return ordered_output(r, thr, need_eq, out, want, sh);
 }
 
 // ---------------------------------------------------------------------------
@@ -1182,7 +1187,7 @@ __device__ __noinline__ int select_long_row(const DevArgs& a, int t, int which, 
         int32_t need_eq;
         refine_threshold(keys, r.len, hs.sel, want - static_cast<int32_t>(hs.above),
                          scratch + kHeadWords + kCandCap - 1024, sh, thr, need_eq);
-        written = ordered_output(r, thr, need_eq, out, sh);
+        written = ordered_output(r, thr, need_eq, out, want, sh);
       } else {
         written = select_ascending(r, want, out, sh, nullptr);
       }
@@ -1256,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
       const uint32_t n = hs.above + hs.cbin;
       bool done = false;
       if (hs.E <= static_cast<uint32_t>(want)) {
-        written = ordered_output(r, 0u, 0, out, sh);        // every eligible entry, in order
+        written = ordered_output(r, 0u, 0, out, want, sh);        // every eligible entry, in order
         done = true;
       } else if (n <= static_cast<uint32_t>(cap)) {
         const uint32_t t_lo = hs.sel << (32 - kHistBits);
@@ -1278,7 +1283,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
           cr.idx = nullptr;
           cr.len = got;
           cr.consumer = false;
-          written = ordered_output(cr, thr, need_eq, out, sh);
+          written = ordered_output(cr, thr, need_eq, out, want, sh);
           done = true;
         }
       }
@@ -1313,7 +1318,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
             cr.ids = cid;
             cr.idx = nullptr;
             cr.len = got;
-            written = ordered_output(cr, thr, need_eq, out, sh);
+            written = ordered_output(cr, thr, need_eq, out, want, sh);
             done = true;
           }
         }

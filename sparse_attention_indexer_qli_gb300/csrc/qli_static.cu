@@ -60,8 +60,26 @@ extern "C" qli_status qli_run_static(const qli_args* a, void* stream) {
   if (st != QLI_OK) return st;
   if (need > QLI_STATIC_SCRATCH_BYTES) return QLI_ERR_WORKSPACE_TOO_SMALL;
   if (a->T == 0) return QLI_OK;
+  // the device check comes first, as in qli_run: on a GPU this library was
+  // not built for, the symbol lookup would fail and leave a sticky error
+  int sms = 0;
+  st = qli::device_sms(&sms);
+  if (st != QLI_OK) return st;
   void* scratch = nullptr;
   st = qli::static_scratch(&scratch);
   if (st != QLI_OK) return st;
   return qli_run(a, scratch, QLI_STATIC_SCRATCH_BYTES, stream);
+}
+
+// The error word sits at the start of the scratch, where every call's
+// planning kernel resets it and later kernels OR their flags in.
+extern "C" qli_status qli_read_static_device_error(uint32_t* host_word, void* stream) {
+  if (host_word == nullptr) return QLI_ERR_INVALID_ARG;
+  int sms = 0;
+  qli_status st = qli::device_sms(&sms);
+  if (st != QLI_OK) return st;
+  void* scratch = nullptr;
+  st = qli::static_scratch(&scratch);
+  if (st != QLI_OK) return st;
+  return qli_read_device_error(scratch, host_word, stream);
 }

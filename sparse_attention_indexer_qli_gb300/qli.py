@@ -55,8 +55,8 @@ class Args(ctypes.Structure):
 
 EXPORTS = ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage", "qli_launch_count",
            "qli_scores_layout", "qli_read_device_error", "qli_status_string", "qli_abi_version",
-           "qli_args_size", "qli_run_static", "qli_quantize_q", "qli_write_index_k",
-           "qli_check_quant_rounding"]
+           "qli_args_size", "qli_run_static", "qli_read_static_device_error",
+           "qli_quantize_q", "qli_write_index_k", "qli_check_quant_rounding"]
 
 _lib = None
 
@@ -82,6 +82,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.qli_read_device_error.argtypes = [c_void_p, ctypes.POINTER(c_uint32), c_void_p]
     L.qli_run_static.argtypes = [P, c_void_p]
     L.qli_run_static.restype = c_int32
+    L.qli_read_static_device_error.argtypes = [ctypes.POINTER(c_uint32), c_void_p]
+    L.qli_read_static_device_error.restype = c_int32
     L.qli_status_string.argtypes = [c_int32]
     L.qli_status_string.restype = ctypes.c_char_p
     L.qli_abi_version.restype = c_int32
@@ -200,6 +202,13 @@ class Call:
         (for callers that cannot allocate a workspace)."""
         _check(lib().qli_run_static(ctypes.byref(self.args), _stream(stream)), "qli_run_static")
         return self.indices, self.cand
+
+    def static_device_error(self, stream=None) -> int:
+        """The device error word of the last run_static call on this device."""
+        w = c_uint32(0)
+        _check(lib().qli_read_static_device_error(ctypes.byref(w), _stream(stream)),
+               "qli_read_static_device_error")
+        return int(w.value)
 
     def run_stage(self, stage: int, workspace, stream=None):
         _check(lib().qli_run_stage(ctypes.byref(self.args), _ptr(workspace), workspace.numel(),

@@ -138,10 +138,19 @@ def test_contract_rejects(L, mode, over, want):
     assert status(L, _with(mode, **over)) == want
 
 
+@pytest.mark.parametrize("mode,over,want", REJECT)
+def test_static_entry_rejects_like_the_workspace_entry(L, mode, over, want):
+    # host validation runs before either entry point touches the device
+    a = _with(mode, **over)
+    assert L.qli_run_static(ctypes.byref(a), None) == want
+    assert L.qli_run(ctypes.byref(a), 0x100000, 1 << 40, None) == want
+
+
 def test_residual_with_ratio_one_is_rejected(L):
     a = good_args(ratio=1)
     a.residual = 0x100000
     assert status(L, a) == 4          # "residual must be absent when ratio is 1"
+    assert L.qli_run_static(ctypes.byref(a), None) == 4
 
 
 def test_candidate_extent_is_tokens_times_blocks(L):

@@ -74,3 +74,23 @@ def test_static_entry_rejects_calls_beyond_its_scratch():
     with pytest.raises(qli.QLIError) as e:
         call.run_static()
     assert e.value.status == 5                 # QLI_ERR_WORKSPACE_TOO_SMALL, nothing launched
+
+
+def test_static_entry_reports_device_side_errors():
+    # a k_len past the block table's capacity is clamped on the device and
+    # flagged in the error word, which the static caller reads back without a
+    # workspace of its own
+    import torch
+    case = synth.make_case(75, [500, 300], [1, 1], N=64, ratio=2, topk=16)
+    kw = synth.upload(case, "cuda")
+    kw["k_lens"] = torch.tensor([250, 10 ** 6], dtype=torch.int32, device="cuda")
+    call = qli.Call(**kw)
+    call.run_static()
+    assert call.static_device_error() & 2          # QLI_DEVERR_KLEN
+    idx = call.indices.cpu().numpy()[:, 0, :]
+    assert np.all(idx[idx >= 0] < case.bt_stride * case.rows_per_page)
+    # the next call resets the word
+    good = qli.Call(**synth.upload(case, "cuda"))
+    good.run_static()
+    assert good.static_device_error() == 0
+
