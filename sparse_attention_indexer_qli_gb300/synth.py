@@ -29,6 +29,7 @@ import numpy as np
 
 D = 128                      # index head dimension
 KV_ROW_BYTES = 1024          # KV bytes per row that precede the index K in a page
+ATTN_D = KV_ROW_BYTES // 2   # BF16 values of one KV row (the attention consumer's head dim)
 BLOCK = 8                    # compressed positions per candidate block
 GEOMETRY = {2: (64, 131072), 1: (128, 147712)}   # ratio -> (rows per page, page stride)
 CAND_MODES = {"none": 1, "source": 2, "consumer": 3}
@@ -79,6 +80,10 @@ class Case:
     cand_blocks: int
     cand_in: Optional[np.ndarray]  # int32 [T, 1, C] (consumer only)
     notes: dict = field(default_factory=dict)
+    # attention consumer inputs (add_attention): BF16 bit patterns
+    kv_rows: Optional[np.ndarray] = None      # uint16 [sum(k_lens), ATTN_D], like k_rows
+    q_attn: Optional[np.ndarray] = None       # uint16 [T, H, ATTN_D]
+    attn_indices: Optional[np.ndarray] = None  # int32 [T, 1, K_attn], ascending, -1 tail
 
     @property
     def T(self) -> int:
@@ -124,6 +129,7 @@ class Case:
             L = int(self.k_lens[b])
             rows = self.k_rows[self.k_row_start[b]:self.k_row_start[b] + L]
             scl = self.k_scale[self.k_row_start[b]:self.k_row_start[b] + L]
+            kvr = None if self.kv_rows is None else self.kv_of(b)
             for p in range(self.request_pages(b)):
                 pid = int(self.block_table[b, p])
                 n = min(R, L - p * R)
@@ -131,6 +137,9 @@ class Case:
                 pages[pid, k_off:k_off + kb.size] = kb
                 sb = scl[p * R:p * R + n].view(np.uint8)
                 pages[pid, s_off:s_off + sb.size] = sb
+                if kvr is not None and stride >= R * KV_ROW_BYTES:
+                    vb = kvr[p * R:p * R + n].view(np.uint8).reshape(-1)
+                    pages[pid, 0:vb.size] = vb
         return pages
 
     def pack_pages_torch(self, device, filler: bool = True):
@@ -150,6 +159,9 @@ class Case:
             pages.zero_()
         krows = torch.from_numpy(self.k_rows.view(np.uint8)).to(device)
         kscl = torch.from_numpy(self.k_scale.view(np.uint8).reshape(-1, 2)).to(device)
+        kvrows = (None if self.kv_rows is None else
+                  torch.from_numpy(self.kv_rows.view(np.uint8)).to(device))
+        KVB = KV_ROW_BYTES
         bt = torch.from_numpy(self.block_table.astype(np.int64)).to(device)
         ko, so = self.k_offset, self.scale_offset
         for b in range(self.B):
@@ -164,18 +176,51 @@ class Case:
                 pages[ids, ko:ko + R * D] = src
                 ssrc = kscl[base:base + full * R].reshape(full, R * 2)
                 pages[ids, so:so + R * 2] = ssrc
+                if kvrows is not None:
+                    pages[ids, 0:R * KVB] = kvrows[base:base + full * R].reshape(full, R * KVB)
             tail = L - full * R
             if tail:
                 pid = int(self.block_table[b, full])
                 pages[pid, ko:ko + tail * D] = krows[base + full * R:base + L].reshape(-1)
                 pages[pid, so:so + tail * 2] = kscl[base + full * R:base + L].reshape(-1)
+                if kvrows is not None:
+                    pages[pid, 0:tail * KVB] = kvrows[base + full * R:base + L].reshape(-1)
         return pages
+
+    def kv_of(self, b: int) -> np.ndarray:
+        return self.kv_rows[self.k_row_start[b]:self.k_row_start[b + 1]]
 
     def k_rows_of(self, b: int) -> np.ndarray:
         return self.k_rows[self.k_row_start[b]:self.k_row_start[b + 1]]
 
     def k_scale_of(self, b: int) -> np.ndarray:
         return self.k_scale[self.k_row_start[b]:self.k_row_start[b + 1]]
+
+
+def add_attention(case: Case, H: int, topk: int, count: Optional[tuple] = None,
+                  sigma: float = 1.0, stream: int = 50) -> Case:
+    """Adds the attention consumer's inputs to `case` (in place) and returns it:
+    BF16 KV rows N(0, sigma) for every compressed position (1024 bytes each,
+    at the start of their page row, before the index K), BF16 queries
+    [T, H, 512] N(0, 1), and per token a list of `topk` compressed positions
+    shaped like the indexer's output: distinct positions of the token's
+    request below its compressed length, ascending, -1 at the end, the count
+    drawn from `count` (default: min(topk, k_len))."""
+    rng = _rng(case.seed, stream)
+    total = int(case.k_lens.sum())
+    case.kv_rows = bf16_rows(case.seed, (total, ATTN_D), sigma=sigma, stream=stream + 1)
+    case.q_attn = bf16_rows(case.seed, (case.T, H, ATTN_D), sigma=1.0, stream=stream + 2)
+    idx = np.full((case.T, 1, topk), -1, dtype=np.int32)
+    for b in range(case.B):
+        lk = int(case.k_lens[b])
+        for t in range(int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])):
+            n = min(topk, lk)
+            if count is not None:
+                n = min(n, int(rng.integers(count[0], count[1], endpoint=True)))
+            if n > 0:
+                idx[t, 0, :n] = np.sort(rng.choice(lk, size=n, replace=False))
+    case.attn_indices = idx
+    return case
 
 
 def bf16_rows(seed: int, shape, sigma: float = 1.0, stream: int = 40) -> np.ndarray:
