@@ -749,6 +749,141 @@ def run_op(args):
     print(json.dumps(line))
 
 
+# ------------------------------------------------- attention over the indices
+
+ATTN_SCALE = 1.0 / np.sqrt(512.0)
+
+
+def attn_algorithmic_bytes(case) -> int:
+    """Bytes the attention kernel must move: each listed position's KV row
+    (1024 B) once per token, the token's queries and outputs (H x 512 BF16
+    each), its LSE (4 B per head), its index list (4 B per entry) and one
+    4-byte block-table entry per listed position."""
+    listed = int((case.attn_indices >= 0).sum())
+    T, H = case.q_attn.shape[:2]
+    return 1024 * listed + 2 * (T * H * 512 * 2) + 4 * T * H + 4 * case.attn_indices.size + 4 * listed
+
+
+def run_attn(args):
+    import torch
+
+    from sparse_attention_indexer_qli_gb300 import qli
+    world, rank, local = dist_setup()
+    qli.lib()
+    case = synth.attention_workload(seed=21 + 100 * rank)
+    dev = "cuda"
+    cache = case.pack_pages_torch(dev)
+    q = torch.from_numpy(case.q_attn.view(np.int16)).to(dev).view(torch.bfloat16)
+    cu = torch.from_numpy(case.cu_seqlens_q).to(dev)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    idx = torch.from_numpy(case.attn_indices).to(dev)
+    T, H = q.shape[:2]
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    pairs = int((case.attn_indices >= 0).sum())
+
+    def launch():
+        qli.sparse_attention(q, cu, cache, bt, idx, rows_per_page=case.rows_per_page,
+                             page_stride=case.page_stride, scale=ATTN_SCALE, out=out, lse=lse,
+                             err_word=err)
+    # one step reads 134 MB of KV rows, about the size of L2: every step is
+    # timed on its own after a 256 MB write that evicts the previous one
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        launch()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+
+    def region():
+        barrier(world)
+        for k in range(args.steps):
+            flush.fill_(k & 255)
+            evs[k][0].record(stream)
+            g.replay()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        times = [region()]
+        for _ in range(repeats_for(times[0], args.min_seconds, world) - 1):
+            times.append(region())
+    ms = statistics.median(times)
+    value, ms_max, _ = aggregate(ms, pairs * args.steps, world)
+    if int(err.item()) != 0:
+        sys.stderr.write("device error word %d: not a valid run\n" % int(err.item()))
+        sys.exit(3)
+    per_ms = ms / args.steps
+    alg = attn_algorithmic_bytes(case)
+    peak, kind = peaks()
+    roof = {"bound": "hbm", "achieved": alg / (per_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": alg / (per_ms / 1e3) / 1e9 / peak, "traffic": profiled_traffic("attn"),
+            "kernel": "attn_kernel", "peak_source": kind, "kernel_ms": per_ms,
+            "algorithmic_bytes": alg}
+    # e2e: the public call from pinned host buffers, outputs back to the host
+    h_q = torch.from_numpy(case.q_attn.view(np.int16)).pin_memory()
+    h_idx = torch.from_numpy(case.attn_indices).pin_memory()
+    h_out = torch.empty((T, H, 512), dtype=torch.bfloat16, pin_memory=True)
+    h_lse = torch.empty((T, H), dtype=torch.float32, pin_memory=True)
+    qv = q.view(torch.int16)
+
+    def e2e_step():
+        qv.copy_(h_q, non_blocking=True)
+        idx.copy_(h_idx, non_blocking=True)
+        launch()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e_step()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    t0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(t0.elapsed_time(t1), world)
+    e2e = {"value": reduce_sum(pairs * args.steps, world) / (e2e_ms / 1e3), "unit": "pairs/s",
+           "h2d_bytes_per_step": h_q.numel() * 2 + h_idx.numel() * 4,
+           "d2h_bytes_per_step": h_out.numel() * 2 + h_lse.numel() * 4}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import csa
+        rows = csa.rows_from_logical(case)
+        done, spent, tok = 0, 0.0, 0
+        while spent < min(args.cpu_seconds, 10.0) and tok < T:
+            t_0 = time.perf_counter()
+            csa.attention(case, ATTN_SCALE, tokens=[tok], rows=rows)
+            spent += time.perf_counter() - t_0
+            done += int((case.attn_indices[tok] >= 0).sum())
+            tok += 1
+        cpu = {"value": done / spent, "unit": "pairs/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle", "sample": "%d of %d tokens (%.1f s, numpy float64)" % (tok, T, spent)}
+    if rank != 0:
+        return
+    print(json.dumps({
+        "metric": "sparse attention over the selected positions: (token, listed position) pairs/s "
+                  "(% of HBM roof)",
+        "value": value, "unit": "pairs/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": synth.ATTN_WORKLOAD, "query_tokens": T, "heads": H,
+                   "listed_per_token": case.attn_indices.shape[-1],
+                   "l2": "a 256 MB write before each step, outside the events that time it",
+                   "timing": "median of %d repeats of the %d-step region" % (len(times), args.steps),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+        "clocks": clk.summary()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -759,9 +894,10 @@ def main():
                     help="workload (default 3: the prefill chunk, the largest single-GPU one)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="repeat the timed region until this much GPU time has run")
-    ap.add_argument("--op", default="index", choices=["index", "quantize_q", "write_index_k"],
-                    help="index: the indexer (default); the others time the query quantiser "
-                         "or the index-K cache writer alone")
+    ap.add_argument("--op", default="index",
+                    choices=["index", "quantize_q", "write_index_k", "sparse_attention"],
+                    help="index: the indexer (default); the others time the query quantiser, "
+                         "the index-K cache writer or the attention over the indices alone")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -775,7 +911,7 @@ def main():
             print(json.dumps({"impl": "reference", "op": args.op,
                               "unavailable": "the reference arm times the indexer only"}))
             return
-        run_op(args)
+        run_attn(args) if args.op == "sparse_attention" else run_op(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

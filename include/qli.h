@@ -239,6 +239,64 @@ qli_status qli_write_index_k(const uint16_t *k, int64_t n, const int64_t *slot_m
  * underflow; those quotients round to code 0 either way). Asynchronous. */
 qli_status qli_check_quant_rounding(unsigned long long *counts, void *stream);
 
+/* ---- Sparse attention over the selected positions ---------------------------
+ * The stage that consumes the indexer's output: blog "DeepSeek V4.1-Flash
+ * 登陆昇腾 · 需求故事（PR 16925）", section 四 (the attention forward passes the
+ * compressed indices to the sparse attention, then inverse-rotates the output
+ * tail in place); guide "DeepSeek V4.1 QLI V2 与候选集成", section 编译范围
+ * (BF16 TND queries over the PA_BBND paged cache, one KV head); section 数据流
+ * (each page row holds the KV row first, then the index K and its scale).
+ * Readings where the pages are silent: the KV row of a compressed position is
+ * 512 BF16 values (1024 bytes) at kv_offset + row * 1024 of its page and is
+ * both key and value; the softmax scale is an argument; the sliding-window
+ * stage and the sinks are not described on the pages and are not part of
+ * this call (the LSE output is what combining with another stage needs).
+ * For token t of request b (cu_seqlens_q), head h, and the listed positions
+ * J = { indices[t, 0, k] >= 0 } (a position listed twice counts twice):
+ *     s_j = scale * sum_d q[t, h, d] * kv_j[d]
+ *     out[t, h, :] = BF16( sum_j exp(s_j - m) kv_j / sum_j exp(s_j - m) ),
+ *     lse[t, h] = m + ln(sum_j exp(s_j - m)),    m = max_j s_j;
+ * an empty J gives out = 0 and lse = -inf. BF16 products are exact; sums are
+ * FP32 on the tensor cores, the weights are rounded to BF16 for the value
+ * product, so results agree with the exact definition to about 2^-8
+ * relative to the largest selected value. */
+typedef struct qli_attn_args {
+    const uint16_t *q;           /* BF16 [T, H, 512]: (t, h, d) at q[t*q_stride_t + h*q_stride_h + d]
+                                    (strides in elements, multiples of 8; d contiguous) */
+    int64_t q_stride_t, q_stride_h;
+    int32_t T;                   /* query tokens */
+    int32_t H;                   /* query heads: 32, 64, 96 or 128 */
+    int32_t D;                   /* values per KV row: 512 */
+    const int32_t *cu_seqlens_q; /* [B+1] raw query boundaries (token t belongs to the
+                                    last request b with cu_seqlens_q[b] <= t) */
+    int32_t B;
+    const uint8_t *cache;        /* the page pool of the indexer (qli_args.cache) */
+    int64_t page_stride;         /* bytes, multiple of 16 */
+    int64_t num_pages;
+    int32_t rows_per_page;       /* 64 or 128 */
+    int64_t kv_offset;           /* bytes from a page's start to row 0's KV values (multiple of 16) */
+    const int32_t *block_table;  /* [B, bt_stride] page IDs */
+    int32_t bt_stride;
+    const int32_t *indices;      /* [T, 1, K] compressed positions (the indexer's output); -1 skipped */
+    int32_t K;                   /* entries per token: 1..2048 */
+    float scale;                 /* softmax scale (finite) */
+    uint16_t *out;               /* BF16 [T, H, 512]: (t, h, d) at out[t*out_stride_t + h*out_stride_h + d] */
+    int64_t out_stride_t, out_stride_h;
+    float *lse;                  /* [T, H] natural-log LSE, or NULL */
+    uint32_t *err_word;          /* device word: QLI_DEVERR_PAGE is OR'ed in when a listed
+                                    position lies past the block table or names a page outside
+                                    the pool (that entry is skipped), QLI_DEVERR_TIMEOUT when an
+                                    on-chip wait gives up; may be NULL; the caller clears it */
+} qli_attn_args;
+
+/* Queues the sparse attention on `stream` (one kernel; no workspace: every
+ * intermediate stays on chip). Device pointers; asynchronous. Host-side
+ * checks as for qli_run (nothing is launched on a non-OK status). */
+qli_status qli_sparse_attention(const qli_attn_args *a, void *stream);
+
+/* sizeof(qli_attn_args) the library was built with. */
+int64_t qli_attn_args_size(void);
+
 /* Human-readable name of a status. Never NULL. */
 const char *qli_status_string(qli_status s);
 

@@ -53,10 +53,26 @@ class Args(ctypes.Structure):
     ]
 
 
+class AttnArgs(ctypes.Structure):
+    """Mirror of `qli_attn_args` (field order and types as in include/qli.h)."""
+    _fields_ = [
+        ("q", c_void_p), ("q_stride_t", c_int64), ("q_stride_h", c_int64),
+        ("T", c_int32), ("H", c_int32), ("D", c_int32),
+        ("cu_seqlens_q", c_void_p), ("B", c_int32),
+        ("cache", c_void_p), ("page_stride", c_int64), ("num_pages", c_int64),
+        ("rows_per_page", c_int32), ("kv_offset", c_int64),
+        ("block_table", c_void_p), ("bt_stride", c_int32),
+        ("indices", c_void_p), ("K", c_int32), ("scale", ctypes.c_float),
+        ("out", c_void_p), ("out_stride_t", c_int64), ("out_stride_h", c_int64),
+        ("lse", c_void_p), ("err_word", c_void_p),
+    ]
+
+
 EXPORTS = ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage", "qli_launch_count",
            "qli_scores_layout", "qli_read_device_error", "qli_status_string", "qli_abi_version",
            "qli_args_size", "qli_run_static", "qli_read_static_device_error",
-           "qli_quantize_q", "qli_write_index_k", "qli_check_quant_rounding"]
+           "qli_quantize_q", "qli_write_index_k", "qli_check_quant_rounding",
+           "qli_sparse_attention", "qli_attn_args_size"]
 
 _lib = None
 
@@ -95,6 +111,11 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.qli_write_index_k.restype = c_int32
     L.qli_check_quant_rounding.argtypes = [c_void_p, c_void_p]
     L.qli_check_quant_rounding.restype = c_int32
+    L.qli_sparse_attention.argtypes = [ctypes.POINTER(AttnArgs), c_void_p]
+    L.qli_sparse_attention.restype = c_int32
+    L.qli_attn_args_size.restype = c_int64
+    if L.qli_attn_args_size() != ctypes.sizeof(AttnArgs):
+        raise ImportError("qli_attn_args layout mismatch")
     for name in ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage",
                  "qli_launch_count", "qli_scores_layout", "qli_read_device_error"]:
         getattr(L, name).restype = c_int32
@@ -300,3 +321,47 @@ def write_index_k(k, slot_mapping, cache, *, rows_per_page: int, page_stride: in
     _check(lib().qli_write_index_k(_ptr(k), k.shape[0], _ptr(slot_mapping), _ptr(cache),
                                    num_pages, page_stride, rows_per_page, k_offset, scale_offset,
                                    _ptr(err_word), _stream(stream)), "qli_write_index_k")
+
+
+def sparse_attention(q, cu_seqlens_q, cache, block_table, indices, *, rows_per_page: int,
+                     page_stride: int, scale: float, kv_offset: int = 0, out=None, lse=None,
+                     err_word=None, stream=None):
+    """qli_sparse_attention: softmax attention of q [T, H, 512] (BF16, CUDA)
+    over the KV rows of the positions in indices [T, 1, K] (int32, -1
+    skipped), read through block_table from the page pool `cache`. Returns
+    (out [T, H, 512] BF16, lse [T, H] float32)."""
+    import torch
+    _require_cuda("q", q, torch.bfloat16)
+    _require_cuda("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _require_cuda("cache", cache, torch.uint8)
+    _require_cuda("block_table", block_table, torch.int32)
+    _require_cuda("indices", indices, torch.int32)
+    _require_cuda("err_word", err_word, torch.int32)
+    if q.dim() != 3 or q.stride(2) != 1:
+        raise ValueError("q must be [T, H, 512] with unit stride in the last dim")
+    if not indices.is_contiguous() or indices.dim() != 3:
+        raise ValueError("indices must be a contiguous [T, 1, K] tensor")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, bt_stride] row-major")
+    T, H, D = q.shape
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    _require_cuda("out", out, torch.bfloat16)
+    _require_cuda("lse", lse, torch.float32)
+    if out.stride(2) != 1 or not lse.is_contiguous():
+        raise ValueError("out must have unit stride in the last dim and lse be contiguous")
+    a = AttnArgs()
+    a.q = _ptr(q); a.q_stride_t = q.stride(0); a.q_stride_h = q.stride(1)
+    a.T, a.H, a.D = T, H, D
+    a.cu_seqlens_q = _ptr(cu_seqlens_q); a.B = cu_seqlens_q.numel() - 1
+    a.cache = _ptr(cache); a.page_stride = page_stride; a.num_pages = cache.numel() // page_stride
+    a.rows_per_page = rows_per_page; a.kv_offset = kv_offset
+    a.block_table = _ptr(block_table); a.bt_stride = block_table.stride(0)
+    a.indices = _ptr(indices); a.K = indices.shape[-1]; a.scale = float(scale)
+    a.out = _ptr(out); a.out_stride_t = out.stride(0); a.out_stride_h = out.stride(1)
+    a.lse = _ptr(lse); a.err_word = _ptr(err_word)
+    _check(lib().qli_sparse_attention(ctypes.byref(a), _stream(stream)), "qli_sparse_attention")
+    return out, lse
+

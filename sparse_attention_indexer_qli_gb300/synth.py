@@ -198,18 +198,18 @@ class Case:
 
 
 def add_attention(case: Case, H: int, topk: int, count: Optional[tuple] = None,
-                  sigma: float = 1.0, stream: int = 50) -> Case:
+                  stream: int = 50) -> Case:
     """Adds the attention consumer's inputs to `case` (in place) and returns it:
-    BF16 KV rows N(0, sigma) for every compressed position (1024 bytes each,
-    at the start of their page row, before the index K), BF16 queries
-    [T, H, 512] N(0, 1), and per token a list of `topk` compressed positions
+    BF16 KV rows for every compressed position (1024 bytes each, at the start
+    of their page row, before the index K) and BF16 queries [T, H, 512], both
+    drawn by bf16_spread, and per token a list of `topk` compressed positions
     shaped like the indexer's output: distinct positions of the token's
     request below its compressed length, ascending, -1 at the end, the count
     drawn from `count` (default: min(topk, k_len))."""
     rng = _rng(case.seed, stream)
     total = int(case.k_lens.sum())
-    case.kv_rows = bf16_rows(case.seed, (total, ATTN_D), sigma=sigma, stream=stream + 1)
-    case.q_attn = bf16_rows(case.seed, (case.T, H, ATTN_D), sigma=1.0, stream=stream + 2)
+    case.kv_rows = bf16_spread(case.seed, (total, ATTN_D), stream=stream + 1)
+    case.q_attn = bf16_spread(case.seed, (case.T, H, ATTN_D), stream=stream + 2)
     idx = np.full((case.T, 1, topk), -1, dtype=np.int32)
     for b in range(case.B):
         lk = int(case.k_lens[b])
@@ -221,6 +221,34 @@ def add_attention(case: Case, H: int, topk: int, count: Optional[tuple] = None,
                 idx[t, 0, :n] = np.sort(rng.choice(lk, size=n, replace=False))
     case.attn_indices = idx
     return case
+
+
+def bf16_spread(seed: int, shape, stream: int = 60) -> np.ndarray:
+    """Seeded BF16 values (uint16 bit patterns) with a random sign, an
+    exponent uniform over 2^-7 .. 2^0 and a random 7-bit mantissa: magnitudes
+    spread over [2^-7, 2), drawn straight as bits (fast for large tensors)."""
+    r = _rng(seed, stream).integers(0, 1 << 16, size=shape, dtype=np.uint16)
+    e = r >> 7                    # three random bits pick the exponent
+    e &= 7
+    e += 120
+    e <<= 7
+    r &= 0x807F                   # sign and mantissa
+    r |= e
+    return r
+
+
+def attention_workload(seed: int = 1, H: int = 64, topk: int = 2048) -> Case:
+    """The attention consumer's decode workload: the ratio-1 decode batch of
+    64 requests (contexts U(8K, 32K), 128-row pages, shuffled block table)
+    with 64 query heads of 512 values and `topk` listed positions per token,
+    shaped like the indexer's TopK output."""
+    raw = _rng(seed, 0).integers(8192, 32768, size=64, endpoint=True)
+    case = make_case(seed, raw, [1] * 64, N=64, ratio=1, topk=topk, cand_mode="none",
+                     name=ATTN_WORKLOAD)
+    return add_attention(case, H=H, topk=topk)
+
+
+ATTN_WORKLOAD = "attn-decode-b64-r1-ctxU8K..32K-h64-d512-topk2048"
 
 
 def bf16_rows(seed: int, shape, sigma: float = 1.0, stream: int = 40) -> np.ndarray:

@@ -251,3 +251,61 @@ def test_write_index_k_validation(L):
     assert _w(L, s_off=65536 + 8192 + 1) == 6
     assert _w(L, slot=A16 + 4) == 6
     assert _w(L, err=A16 + 2) == 6
+
+
+# ---- attention over the selected positions: layout and host validation ------
+
+def test_attn_struct_layout_matches_header(tmp_path):
+    fields = [f for f, _ in qli.AttnArgs._fields_]
+    src = ['#include <stddef.h>', '#include <stdio.h>', '#include "qli.h"', 'int main(void){',
+           'printf("%zu\\n", sizeof(qli_attn_args));']
+    src += ['printf("%%zu\\n", offsetof(qli_attn_args, %s));' % f for f in fields]
+    src += ['return 0;}']
+    c = tmp_path / "probe.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(c), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(qli.AttnArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(qli.AttnArgs, f).offset == off, f
+
+
+def good_attn(T=4, B=2, H=64, K=256):
+    a = qli.AttnArgs()
+    p = 0x100000
+    a.q = p; a.q_stride_t = H * 512; a.q_stride_h = 512
+    a.T, a.H, a.D = T, H, 512
+    a.cu_seqlens_q = p; a.B = B
+    a.cache = p; a.page_stride = 147712; a.num_pages = 100; a.rows_per_page = 128
+    a.kv_offset = 0; a.block_table = p; a.bt_stride = 8
+    a.indices = p; a.K = K; a.scale = 0.044
+    a.out = p; a.out_stride_t = H * 512; a.out_stride_h = 512
+    a.lse = p; a.err_word = None
+    return a
+
+
+ATTN_REJECT = [
+    (dict(D=576), 2), (dict(H=16), 2), (dict(H=48), 2), (dict(H=160), 2),
+    (dict(rows_per_page=32), 2), (dict(K=0), 1), (dict(K=2049), 1),
+    (dict(scale=float("inf")), 1), (dict(scale=float("nan")), 1),
+    (dict(q=None), 1), (dict(indices=None), 1), (dict(out=None), 1),
+    (dict(kv_offset=147712 - 128 * 1024 + 16), 1),     # KV rows past the page end
+    (dict(q=0x100008), 6), (dict(q_stride_h=500), 1), (dict(q_stride_h=524), 6),
+    (dict(page_stride=147720), 6), (dict(kv_offset=8), 6), (dict(out=0x100001), 6),
+    (dict(B=0), 1), (dict(num_pages=0), 1),
+]
+
+
+@pytest.mark.parametrize("over,want", ATTN_REJECT)
+def test_attention_contract_rejects(L, over, want):
+    a = good_attn()
+    for k, v in over.items():
+        setattr(a, k, v)
+    assert L.qli_sparse_attention(ctypes.byref(a), None) == want
+
+
+def test_attention_nothing_to_do(L):
+    a = good_attn(T=0)
+    assert L.qli_sparse_attention(ctypes.byref(a), None) == qli.OK
