@@ -12,21 +12,29 @@
 // for token t, head h and the listed positions J (-1 skipped):
 //   s_j = scale * q[t,h,:] . kv_j,  o = softmax(s) . kv,  lse = log sum exp s.
 //
-// One CTA per (token, group of 32 heads); 7 warps:
-//   warps 0-1  gather: the group's queries and, tile by tile, the KV rows of
-//              128 listed positions, with 16-byte cp.async copies (each row
-//              lives in its own page, so no tensor map fits) into 128-byte-
-//              swizzled 32 KB chunks of 128 rows x 128 values (5-chunk ring)
-//   warp 2     TMEM allocation and the MMA issuer (tcgen05, BF16, FP32
-//              accumulators): S^T = KV_tile . Q^T (M = 128 positions, N = 32
-//              heads, K = 512), then O^T += KV_tile^T . P^T (M = 128 values
-//              per chunk, N = 64 (32 heads, zero padded), K = 128 positions),
-//              reading the same swizzled chunks K-major and MN-major
-//   warps 3-6  softmax: thread = position (TMEM lane); per-head tile maxima
-//              by a transpose-reduction across lanes, an online softmax that
-//              rescales O^T only when a head's maximum grows by more than
-//              kRescale (the stale maximum keeps every weight below e^kRescale),
-//              P^T as BF16 into shared memory; at the end O / l and the LSE.
+// One CTA per (token, group of 32 heads); 7 warps. The listed positions are
+// taken 32 at a time (a chunk: 32 rows of 1 KB), five chunks in flight:
+//   warps 0-1  gather: the group's queries, then each chunk's KV rows with
+//              16-byte cp.async copies (every row lives in its own page, so no
+//              tensor map fits), coalesced 512 bytes per warp instruction,
+//              into a 128-byte-swizzled layout whose 128 rows are the pairs
+//              (quarter of the 512 values, position)
+//   warp 2     TMEM allocation and the MMA issuer (tcgen05, BF16, FP32 in
+//              TMEM). Scores: M = 128 rows (quarter e, position p) x N = 128
+//              (quarter e', head) x K = 128 values of the quarter, against
+//              the queries stacked by quarter, so the block e = e' holds the
+//              quarter's partial dot products; the four blocks sum to S.
+//              Values: O^T[e] += V^T . P^T per quarter (M = 128 values,
+//              N = 64: 32 heads and 32 zero columns, K = 32 positions), from
+//              the same chunk read MN-major. Scores of chunk n+1 run while
+//              chunk n's softmax does
+//   warps 3-6  softmax: warp e loads quarter e's block (lane = position),
+//              the blocks are summed in shared memory, warp w then owns heads
+//              8w..8w+7 for the chunk's 32 positions: maxima by warp
+//              shuffles, an online softmax that rescales O^T only when a
+//              head's maximum grows by more than kRescale (the stale maximum
+//              keeps every weight below e^kRescale), P^T as BF16; at the end
+//              O / l and the LSE
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,31 +50,31 @@ namespace {
 constexpr int kD = 512;                    // values per KV row
 constexpr int kRowBytes = kD * 2;
 constexpr int kHeads = 32;                 // heads per CTA
-constexpr int kTileRows = 128;             // positions per tile (MMA M of S^T)
-constexpr int kChunkD = 128;               // values per chunk
-constexpr int kChunks = kD / kChunkD;      // 4 chunks per tile
-constexpr int kChunkBytes = kTileRows * kChunkD * 2;   // 32 KB
-constexpr int kRegionBytes = kTileRows * 128;          // 64 values x 128 rows
+constexpr int kCP = 32;                    // positions per chunk
+constexpr int kChunkBytes = kCP * kRowBytes;       // 32 KB
+constexpr int kRegionBytes = 128 * 128;    // 128 rows x 64 values (BF16)
 constexpr int kSlots = 5;                  // chunk ring
-constexpr int kQRegion = kHeads * 128;     // 64 values x 32 heads
-constexpr int kQBytes = kHeads * kD * 2;   // 32 KB
-constexpr int kPBytes = kTileRows * 128;   // 128 positions x 64 heads (BF16)
+constexpr int kQBytes = 2 * kRegionBytes;  // 128 rows (quarter, head) x 128 values
+constexpr int kPBytes = kCP * 128;         // 32 positions x 64 heads (BF16)
 constexpr int kThreads = 224;
 constexpr int kGatherThreads = 64;
 constexpr int kEpiWarp0 = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 0;              // S^T: 32 columns
-constexpr uint32_t kOCol = 64;             // O^T: 4 chunks x 64 columns
+constexpr uint32_t kSCol = 0;              // two score buffers of 128 columns
+constexpr uint32_t kOCol = 256;            // O^T: 4 quarters x 64 columns
 constexpr float kRescale = 8.0f;           // natural-log slack before O is rescaled
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Smem {
   uint8_t kv[kSlots][kChunkBytes];         // 1024-aligned
   uint8_t q[kQBytes];                      // 1024-aligned
-  uint8_t p[kPBytes];                      // 1024-aligned
-  const uint8_t* rowptr[kTileRows];        // this tile's row addresses (nullptr: zero row)
-  float red[4][32];
-  uint64_t full[kSlots], empty[kSlots], qfull, sfull, pready, ofull;
+  uint8_t p[2][kPBytes];                   // 1024-aligned, by chunk parity
+  float xs[4][kCP][33];                    // quarter blocks of the scores (padded rows)
+  float alpha[kHeads];
+  float mfin[kHeads], lfin[kHeads];
+  int32_t chflag[4];
+  int32_t slot[qli::kMaxTopK];             // listed entry -> page * R + row, -1: skipped
+  uint64_t full[kSlots], empty[kSlots], qfull, tfull, sfull[2], pready[2], pvdone, ofull;
   uint32_t tmem_base;
 };
 constexpr int kSmemBytes = static_cast<int>(sizeof(Smem)) + 1024;
@@ -118,6 +126,13 @@ __device__ __forceinline__ uint32_t sw(uint32_t r, uint32_t u) {
   return (r >> 3) * 1024u + (r & 7u) * 128u + ((u ^ (r & 7u)) << 4);
 }
 
+// 2^x by the SFU's approximation (ex2.approx.ftz: a few ulp; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void cp16(void* dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                "r"(src_bytes)
@@ -131,40 +146,21 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// v[0..31] of each lane -> lane L returns op over the warp's lanes of v[L].
-// Five exchange rounds: each lane keeps half of its values and combines them
-// with the partner's copy of that half.
-template <class Op>
-__device__ __forceinline__ float transpose_reduce(float (&v)[32], Op op) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool upper = (lane & w) != 0;
-#pragma unroll
-    for (int j = 0; j < w; ++j) {
-      const float send = upper ? v[j] : v[j + w];
-      const float keep = upper ? v[j + w] : v[j];
-      v[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, w));
-    }
-  }
-  return v[0];
-}
-
-// The address of position j's KV row for request b, or nullptr when j lies
-// outside the block table or names a page outside the pool (flagged).
-__device__ __forceinline__ const uint8_t* row_of(const Args& a, int32_t b, int32_t j, bool& bad) {
-  if (j < 0) return nullptr;
+// Position j of request b as page * R + row, or -1 when j is negative, lies
+// outside the block table or names a page outside the pool (the last two
+// flagged).
+__device__ __forceinline__ int32_t slot_of(const Args& a, int32_t b, int32_t j, bool& bad) {
+  if (j < 0) return -1;
   if (static_cast<int64_t>(j) >= static_cast<int64_t>(a.bt_stride) * a.R) {
     bad = true;
-    return nullptr;
+    return -1;
   }
   const int32_t page = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + j / a.R);
   if (page < 0 || page >= a.num_pages) {
     bad = true;
-    return nullptr;
+    return -1;
   }
-  return a.cache + static_cast<int64_t>(page) * a.page_stride + a.kv_off +
-         static_cast<int64_t>(j % a.R) * kRowBytes;
+  return page * a.R + j % a.R;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(Args a) {
@@ -173,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(Args a) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.y, h0 = blockIdx.x * kHeads;
-  const int ntiles = (a.K + kTileRows - 1) / kTileRows;
+  const int nchunks = (a.K + kCP - 1) / kCP;
 
   if (warp == 2) tmem_alloc(&S.tmem_base, kTmemCols);
   if (tid == 0) {
@@ -182,16 +178,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(Args a) {
       mbar_init(&S.empty[s], 1);
     }
     mbar_init(&S.qfull, kGatherThreads);
-    mbar_init(&S.sfull, 1);
-    mbar_init(&S.pready, 4);
+    mbar_init(&S.tfull, kGatherThreads);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.sfull[s], 1);
+      mbar_init(&S.pready[s], 4);
+    }
+    mbar_init(&S.pvdone, 1);
     mbar_init(&S.ofull, 1);
     fence_mbar_init();
   }
   // P^T columns 32..63 (padding heads) stay zero for the whole call
-  if (warp >= kEpiWarp0) {
-    const int p = tid - 32 * kEpiWarp0;
+  if (warp >= kEpiWarp0 && tid - 32 * kEpiWarp0 < 2 * kCP) {
+    const int r = tid - 32 * kEpiWarp0;
 #pragma unroll
-    for (int u = 4; u < 8; ++u) *reinterpret_cast<uint4*>(&S.p[sw(p, u)]) = make_uint4(0, 0, 0, 0);
+    for (int u = 4; u < 8; ++u)
+      *reinterpret_cast<uint4*>(&S.p[r >> 5][sw(r & 31, u)]) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -217,83 +218,103 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(Args a) {
     const int g = tid;                                   // 0..63
     const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(
         a.q + static_cast<int64_t>(t) * a.q_st + static_cast<int64_t>(h0) * a.q_sh);
+    // queries: row (quarter e, head h) of the stacked operand holds values
+    // 128e .. 128e+127 of head h
     for (int u = g; u < kHeads * (kD / 8); u += kGatherThreads) {
       const int h = u / (kD / 8), du = u % (kD / 8);
-      cp16(&S.q[(du >> 3) * kQRegion + sw(h, du & 7)],
+      const int e = du >> 4, kq = du & 15;
+      cp16(&S.q[(kq >> 3) * kRegionBytes + sw(e * 32 + h, kq & 7)],
            qsrc + static_cast<int64_t>(h) * a.q_sh * 2 + du * 16, 16);
     }
     cp_arrive(&S.qfull);
-    // lanes 0-15 and 16-31 of a warp copy two rows' 256-byte chunk pieces
-    // per instruction (coalesced); warp w copies rows 4k + 2w + half, whose
-    // addresses its own lanes look up (lane k: rows 4k + 2w and 4k + 2w + 1),
-    // so the two gather warps never wait on each other
-    const int half = lane >> 4, u = lane & 15;
+    // the slot of every listed entry, once: all index loads first, then all
+    // block-table loads, so the dependent round trips are paid once per call
     bool bad = false;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      __syncwarp();                                      // the last tile's copies are issued
+    {
+      constexpr int kPer = qli::kMaxTopK / kGatherThreads;   // 32
+      int32_t j[kPer];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int p = 4 * lane + 2 * warp + hh;
-        const int e = i * kTileRows + p;
-        S.rowptr[p] = e < a.K ? row_of(a, b, __ldg(idx_row + e), bad) : nullptr;
+      for (int i = 0; i < kPer; ++i) {
+        const int e = g + i * kGatherThreads;
+        j[i] = e < a.K ? __ldg(idx_row + e) : -1;
       }
-      __syncwarp();
-      for (int c = 0; c < kChunks; ++c) {
-        const int n = i * kChunks + c, s = n % kSlots;
-        if (lane == 0) ok = mbar_wait_bounded(&S.empty[s], ((n / kSlots) & 1) ^ 1);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        uint8_t* dst = S.kv[s];
-#pragma unroll 4
-        for (int k = 0; k < kTileRows / 4; ++k) {
-          const int p = 4 * k + 2 * warp + half;
-          const uint8_t* src = S.rowptr[p];
-          cp16(dst + (u >> 3) * kRegionBytes + sw(p, u & 7),
-               src ? src + c * (kChunkD * 2) + u * 16 : a.cache, src ? 16u : 0u);
-        }
-        cp_arrive(&S.full[s]);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = g + i * kGatherThreads;
+        if (e < a.K) S.slot[e] = slot_of(a, b, j[i], bad);
       }
+    }
+    mbar_arrive(&S.tfull);
+    if (lane == 0) ok = mbar_wait_bounded(&S.tfull, 0);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    // lane l resolves row l of each chunk; a warp instruction copies 512
+    // contiguous bytes of one row (units 32w .. 32w+31 of its 64)
+    const auto row_addr = [&](int n) -> const uint8_t* {
+      const int e = n * kCP + lane;
+      const int32_t sl = (n < nchunks && e < a.K) ? S.slot[e] : -1;
+      if (sl < 0) return nullptr;
+      return a.cache + static_cast<int64_t>(sl / a.R) * a.page_stride + a.kv_off +
+             static_cast<int64_t>(sl % a.R) * kRowBytes;
+    };
+    const int ur = warp * 32 + lane;                     // this lane's 16-byte unit of a row
+    const int ue = ur >> 4, ukq = ur & 15;               // quarter, unit within the quarter
+    const uint32_t dst_col = (ukq >> 3) * kRegionBytes;
+    for (int n = 0; n < nchunks && ok; ++n) {
+      const uint8_t* ptr = row_addr(n);
+      const int s = n % kSlots;
+      if (lane == 0) ok = mbar_wait_bounded(&S.empty[s], ((n / kSlots) & 1) ^ 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      uint8_t* dst = S.kv[s] + dst_col;
+#pragma unroll 8
+      for (int p = 0; p < kCP; ++p) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(ptr), p));
+        cp16(dst + sw(ue * 32 + p, ukq & 7), src ? src + ur * 16 : a.cache, src ? 16u : 0u);
+      }
+      cp_arrive(&S.full[s]);
     }
     if (bad && a.err) atomicOr(a.err, QLI_DEVERR_PAGE);
     cp_wait_all();                                       // nothing in flight at exit
     if (!ok && lane == 0 && a.err) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
   } else if (warp == 2) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: scores of chunk n, then values of chunk n-1
     if (lane == 0) {
-      const uint32_t id_qk = idesc_bf16(kHeads, false, false);
+      const uint32_t id_qk = idesc_bf16(128, false, false);
       const uint32_t id_pv = idesc_bf16(64, true, true);
-      const uint32_t qb = smem_u32(S.q), pb = smem_u32(S.p);
+      const uint32_t qb = smem_u32(S.q);
       ok = mbar_wait_bounded(&S.qfull, 0);
-      for (int i = 0; i < ntiles && ok; ++i) {
-        // S^T = KV_tile . Q^T over the four chunks
-        for (int c = 0; c < kChunks && ok; ++c) {
-          const int n = i * kChunks + c, s = n % kSlots;
+      for (int n = 0; n <= nchunks && ok; ++n) {
+        if (n < nchunks) {
+          const int s = n % kSlots;
           if (!mbar_wait_bounded(&S.full[s], (n / kSlots) & 1)) { ok = false; break; }
           fence_proxy_async_smem();                      // cp.async writes -> tensor core
           tc_fence_after();
           const uint32_t kvb = smem_u32(S.kv[s]);
 #pragma unroll
-          for (int kk = 0; kk < kChunkD / 16; ++kk) {
+          for (int kk = 0; kk < 8; ++kk) {
             const uint32_t r = kk >> 2, koff = (kk & 3) * 32;
-            mma_f16_ss(tmem + kSCol, sdesc_sw128(kvb + r * kRegionBytes + koff, 16, 1024),
-                       sdesc_sw128(qb + (2 * c + r) * kQRegion + koff, 16, 1024), id_qk,
-                       (c | kk) != 0 ? 1u : 0u);
+            mma_f16_ss(tmem + kSCol + (n & 1) * 128,
+                       sdesc_sw128(kvb + r * kRegionBytes + koff, 16, 1024),
+                       sdesc_sw128(qb + r * kRegionBytes + koff, 16, 1024), id_qk, kk ? 1u : 0u);
           }
+          mma_commit(&S.sfull[n & 1]);
         }
-        if (!ok) break;
-        mma_commit(&S.sfull);
-        // O^T += KV_tile^T . P^T, chunk by chunk; each chunk's slot is
-        // returned to the gather when its MMAs are done
-        if (!mbar_wait_bounded(&S.pready, i & 1)) { ok = false; break; }
-        tc_fence_after();
-        for (int c = 0; c < kChunks; ++c) {
-          const int n = i * kChunks + c, s = n % kSlots;
-          const uint32_t kvb = smem_u32(S.kv[s]);
+        if (n >= 1) {
+          const int m = n - 1, s = m % kSlots;
+          if (!mbar_wait_bounded(&S.pready[m & 1], (m >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kvb = smem_u32(S.kv[s]), pb = smem_u32(S.p[m & 1]);
 #pragma unroll
-          for (int kk = 0; kk < kTileRows / 16; ++kk)
-            mma_f16_ss(tmem + kOCol + c * 64, sdesc_sw128(kvb + kk * 2048, kRegionBytes, 1024),
-                       sdesc_sw128(pb + kk * 2048, 1024, 1024), id_pv, (i | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kCP / 16; ++kk) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              mma_f16_ss(tmem + kOCol + e * 64,
+                         sdesc_sw128(kvb + e * 4096 + kk * 2048, kRegionBytes, 1024),
+                         sdesc_sw128(pb + kk * 2048, 1024, 1024), id_pv, (m | kk) ? 1u : 0u);
+          }
           mma_commit(&S.empty[s]);
+          mma_commit(&S.pvdone);
         }
       }
       mma_commit(&S.ofull);                              // every MMA of the CTA is done
@@ -301,111 +322,141 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(Args a) {
       if (!ok && a.err) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
     }
   } else {
-    // ---------------- softmax and output: thread = TMEM lane
-    const int quarter = warp & 3;
-    const int pos = 32 * quarter + lane;                 // position within a tile / value within a chunk
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
-    const int ew = warp - kEpiWarp0;                     // 0..3
-    float m_own = -INFINITY;                             // lane L: head L's reference maximum
-    float l_part[kHeads];                                // this position's running sums
-#pragma unroll
-    for (int h = 0; h < kHeads; ++h) l_part[h] = 0.0f;
-    const float sl2 = a.scale * kLog2e;
-    // every epilogue warp runs the same sequence of named barriers whatever
+    // ---------------- softmax and output
+    // Every epilogue warp runs the same sequence of named barriers whatever
     // happens: a wait that gives up clears `ok`, later waits are skipped and
-    // the remaining tiles are run through on whatever TMEM holds (the call
-    // then reports QLI_DEVERR_TIMEOUT and its outputs are not written)
-    for (int i = 0; i < ntiles; ++i) {
-      const int e = i * kTileRows + pos;
-      bool bad = false;
-      const bool valid = e < a.K && row_of(a, b, __ldg(idx_row + e), bad) != nullptr;
-      if (ok && !mbar_wait_warp(&S.sfull, i & 1)) ok = false;
+    // the remaining chunks are run through on whatever TMEM holds (the call
+    // then reports QLI_DEVERR_TIMEOUT and its outputs are not written).
+    const int qw = warp & 3;                             // TMEM lane quarter / quarter of values
+    const int ew = warp - kEpiWarp0;                     // 0..3: heads 8ew .. 8ew+7
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * qw) << 16;
+    float m_used[8], l_part[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      m_used[j] = -INFINITY;
+      l_part[j] = 0.0f;
+    }
+    const float sl2 = a.scale * kLog2e;
+    if (!mbar_wait_warp(&S.tfull, 0)) ok = false;       // the slot table is written
+    for (int n = 0; n < nchunks; ++n) {
+      const int e_idx = n * kCP + lane;
+      const bool valid = e_idx < a.K && S.slot[e_idx] >= 0;
+      if (ok && !mbar_wait_warp(&S.sfull[n & 1], (n >> 1) & 1)) ok = false;
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem + lane_addr + kSCol, r);
-      tmem_ld_wait();
-      // scores in log2 units: x = s * scale * log2(e)
-      float x[kHeads];
+      {
+        // block (quarter qw, quarter qw): this position's partial dots of 32 heads
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + lane_addr + kSCol + (n & 1) * 128 + 32 * qw, r);
+        tmem_ld_wait();
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) x[h] = valid ? __uint_as_float(r[h]) * sl2 : -INFINITY;
-      float v[kHeads];
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h) v[h] = x[h];
-      S.red[ew][lane] = transpose_reduce(v, [](float p, float q) { return fmaxf(p, q); });
-      named_bar(1, 128);
-      const float mt = fmaxf(fmaxf(S.red[0][lane], S.red[1][lane]), fmaxf(S.red[2][lane], S.red[3][lane]));
-      named_bar(1, 128);                                 // red is reused next tile
-      // lane L decides head L's reference maximum (log2 units)
-      float m_new = m_own;
-      if (mt > -INFINITY && (m_own == -INFINITY || mt > m_own + kRescale * kLog2e)) m_new = mt;
-      const float alpha = (m_new == m_own) ? 1.0f : (m_own == -INFINITY ? 0.0f : exp2f(m_own - m_new));
-      const bool changed = __any_sync(0xffffffffu, m_new != m_own);
-      m_own = m_new;
-      // P for this position, all 32 heads; running sums
-      uint32_t pk[kHeads / 2];
-#pragma unroll
-      for (int h = 0; h < kHeads; h += 2) {
-        const float ma = __shfl_sync(0xffffffffu, m_own, h), mb = __shfl_sync(0xffffffffu, m_own, h + 1);
-        const float pa = (x[h] == -INFINITY) ? 0.0f : exp2f(x[h] - ma);
-        const float pb = (x[h + 1] == -INFINITY) ? 0.0f : exp2f(x[h + 1] - mb);
-        if (changed) {
-          l_part[h] *= __shfl_sync(0xffffffffu, alpha, h);
-          l_part[h + 1] *= __shfl_sync(0xffffffffu, alpha, h + 1);
-        }
-        l_part[h] += pa;
-        l_part[h + 1] += pb;
-        const __nv_bfloat162 pp = __floats2bfloat162_rn(pa, pb);
-        pk[h / 2] = *reinterpret_cast<const uint32_t*>(&pp);
+        for (int h = 0; h < 32; ++h) S.xs[qw][lane][h] = __uint_as_float(r[h]);
       }
+      named_bar(1, 128);
+      float x[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(&S.p[sw(pos, u)]) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      if (changed && i > 0) {
-        // O^T (lane = value, column = head) times alpha of each head; the
-        // MMAs of the previous tile are complete (S^T of this tile is)
+      for (int j = 0; j < 8; ++j) {
+        const int h = 8 * ew + j;
+        const float sc = (S.xs[0][lane][h] + S.xs[1][lane][h]) + (S.xs[2][lane][h] + S.xs[3][lane][h]);
+        x[j] = valid ? sc * sl2 : -INFINITY;
+      }
+      // per-head maxima over the chunk's 32 positions (the eight shuffle
+      // chains side by side), then each head's decision, branch-free: the
+      // reference maximum moves only when the chunk's exceeds it by more
+      // than kRescale (or on the first positions the head sees)
+      float mt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mt[j] = x[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mt[j] = fmaxf(mt[j], __shfl_xor_sync(0xffffffffu, mt[j], o));
+      }
+      bool changed = false;
+      float alpha[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool up = mt[j] > m_used[j] + kRescale * kLog2e;   // false while mt is -inf
+        alpha[j] = up ? ex2(m_used[j] - mt[j]) : 1.0f;           // 0 when m_used was -inf
+        m_used[j] = up ? mt[j] : m_used[j];
+        changed |= up;
+      }
+      if (lane < 8) {
+        float al = alpha[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) al = lane == j ? alpha[j] : al;
+        S.alpha[8 * ew + lane] = al;
+      }
+      if (lane == 0) S.chflag[ew] = changed ? 1 : 0;
+      named_bar(1, 128);                                 // scores read, alphas published
+      const bool rescale = n > 0 && (S.chflag[0] | S.chflag[1] | S.chflag[2] | S.chflag[3]) != 0;
+      uint32_t pk[4];
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        const float pa = x[j] == -INFINITY ? 0.0f : ex2(x[j] - m_used[j]);
+        const float pb = x[j + 1] == -INFINITY ? 0.0f : ex2(x[j + 1] - m_used[j + 1]);
+        l_part[j] = l_part[j] * alpha[j] + pa;
+        l_part[j + 1] = l_part[j + 1] * alpha[j + 1] + pb;
+        const __nv_bfloat162 pp = __floats2bfloat162_rn(pa, pb);
+        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pp);
+      }
+      *reinterpret_cast<uint4*>(&S.p[n & 1][sw(lane, ew)]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      if (rescale) {
+        // O^T (lane = value, column = head) times each head's alpha, once the
+        // values of the previous chunk are accumulated
+        if (ok && !mbar_wait_warp(&S.pvdone, (n - 1) & 1)) ok = false;
+        tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
+        for (int e = 0; e < 4; ++e) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + kOCol + c * 64, o);
+          tmem_ld_32x32b_x32(tmem + lane_addr + kOCol + e * 64, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int h = 0; h < kHeads; ++h)
-            o[h] = __float_as_uint(__uint_as_float(o[h]) * __shfl_sync(0xffffffffu, alpha, h));
-          tmem_st_32x32b_x32(tmem + lane_addr + kOCol + c * 64, o);
+          for (int h = 0; h < 32; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * S.alpha[h]);
+          tmem_st_32x32b_x32(tmem + lane_addr + kOCol + e * 64, o);
         }
         tmem_st_wait();
       }
       fence_proxy_async_smem();                          // P^T -> tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.pready);
+      if (lane == 0) mbar_arrive(&S.pready[n & 1]);
     }
-    // totals: l of head L in lane L, the same in every epilogue warp
-    const float lw = transpose_reduce(l_part, [](float p, float q) { return p + q; });
+    // totals of this warp's heads (sum over the 32 positions of each chunk)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        S.lfin[8 * ew + j] = l_part[j];
+        S.mfin[8 * ew + j] = m_used[j];
+      }
+    }
     named_bar(1, 128);
-    S.red[ew][lane] = lw;
-    named_bar(1, 128);
-    const float l = (S.red[0][lane] + S.red[1][lane]) + (S.red[2][lane] + S.red[3][lane]);
-    const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
     if (ok && !mbar_wait_warp(&S.ofull, 0)) ok = false;
     tc_fence_after();
     if (ok) {
-      if (ew == 0 && a.lse)
+      if (ew == 0 && a.lse) {
+        const float l = S.lfin[lane];
         a.lse[static_cast<int64_t>(t) * a.H + h0 + lane] =
-            l > 0.0f ? (m_own + log2f(l)) * (1.0f / kLog2e) : -INFINITY;
+            l > 0.0f ? (S.mfin[lane] + log2f(l)) * (1.0f / kLog2e) : -INFINITY;
+      }
+      float inv_l[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) inv_l[h] = S.lfin[h] > 0.0f ? 1.0f / S.lfin[h] : 0.0f;
       uint16_t* orow = a.out + static_cast<int64_t>(t) * a.o_st + static_cast<int64_t>(h0) * a.o_sh;
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c) {
+      for (int e = 0; e < 4; ++e) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + lane_addr + kOCol + c * 64, o);
+        tmem_ld_32x32b_x32(tmem + lane_addr + kOCol + e * 64, o);
         tmem_ld_wait();
+        const int v = e * 128 + 32 * qw + lane;          // value of this TMEM lane
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) {
-          const float val = __uint_as_float(o[h]) * __shfl_sync(0xffffffffu, inv_l, h);
-          const __nv_bfloat16 bv = __float2bfloat16_rn(val);
-          orow[static_cast<int64_t>(h) * a.o_sh + c * kChunkD + pos] =
-              *reinterpret_cast<const uint16_t*>(&bv);
+        for (int h = 0; h < 32; ++h) {
+          const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(o[h]) * inv_l[h]);
+          orow[static_cast<int64_t>(h) * a.o_sh + v] = *reinterpret_cast<const uint16_t*>(&bv);
         }
       }
     }
@@ -438,6 +489,7 @@ extern "C" qli_status qli_sparse_attention(const qli_attn_args* a, void* stream)
   if (a->q == nullptr || a->cu_seqlens_q == nullptr || a->cache == nullptr ||
       a->block_table == nullptr || a->indices == nullptr || a->out == nullptr)
     return QLI_ERR_INVALID_ARG;
+  if (a->num_pages > (int64_t{1} << 24)) return QLI_ERR_UNSUPPORTED;   // page * R fits 31 bits
   if (a->bt_stride < 1 || a->num_pages < 1 || a->page_stride <= 0 || a->kv_offset < 0 ||
       a->kv_offset + static_cast<int64_t>(a->rows_per_page) * kRowBytes > a->page_stride)
     return QLI_ERR_INVALID_ARG;
