@@ -60,6 +60,16 @@ enum { QLI_CAND_NONE = 1, QLI_CAND_SOURCE = 2, QLI_CAND_CONSUMER = 3 };
 /* Layouts, quantisation and mask modes the contract compiles. */
 enum { QLI_LAYOUT_TND = 1, QLI_LAYOUT_PA_BBND = 2 };
 enum { QLI_QUANT_INT8 = 2 };          /* quant mode 2: INT8 Q/K, FP16 weights/scales */
+/* Quant mode 1: FP8. The guide's section "编译范围" names FP8 as quant mode 1
+ * of the A5 build and prints no FP8 golden; this library reads it as the
+ * same layout and chain with E4M3 codes ("fn": bias 7, largest 448, no
+ * infinities) in place of the INT8 values: q and the index-K rows hold one
+ * code per byte, the dot of the decoded codes (rounded to FP32) takes the
+ * INT32 dot's place, and the chain from the division by 1024 on is
+ * unchanged. The sums are the tensor core's FP32 ones, so a score can differ
+ * from the exactly rounded dot's by the rounding of those sums (a few FP32
+ * ulps of each head's dot before its FP16 rounding). */
+enum { QLI_QUANT_FP8 = 1 };
 enum { QLI_MASK_CAUSAL = 3 };         /* causal mask mode 3 */
 /* Stages of one call, for timing them separately (qli_run_stage). */
 enum { QLI_STAGE_PLAN = 1, QLI_STAGE_SCORE = 2, QLI_STAGE_SELECT = 3 };
@@ -74,7 +84,8 @@ enum {
 
 typedef struct qli_args {
     /* Queries, TND: element (t, h, d) at q[t*q_stride_t + h*q_stride_h + d],
-     * INT8, strides in bytes, each a multiple of 16 with q_stride_h >= D. */
+     * INT8 (E4M3 codes in quant mode 1), strides in bytes, each a multiple
+     * of 16 with q_stride_h >= D. */
     const int8_t *q;
     int64_t q_stride_t, q_stride_h;
     int32_t T;                        /* query tokens (all requests)            */
@@ -103,7 +114,7 @@ typedef struct qli_args {
     const uint16_t *q_scale;
     int32_t ratio;                    /* compression ratio: 1 or 2              */
     int32_t mask_mode;                /* QLI_MASK_CAUSAL                        */
-    int32_t quant_mode;               /* QLI_QUANT_INT8                         */
+    int32_t quant_mode;               /* QLI_QUANT_INT8 or QLI_QUANT_FP8        */
     int32_t layout_q;                 /* QLI_LAYOUT_TND                         */
     int32_t layout_k;                 /* QLI_LAYOUT_PA_BBND                     */
     int32_t topk;                     /* K in [1, 2048]                         */

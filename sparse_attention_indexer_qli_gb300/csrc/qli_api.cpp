@@ -6,7 +6,8 @@
 //  section 数据流 — TND queries and PA_BBND paged index K only (other layouts
 //    are rejected by host validation); residual absent when ratio is 1;
 //    a consumer without a source raises;
-//  section 当前 A3 契约 — INT8 Q/K with FP16 weights and scales (quant mode 2),
+//  section 当前 A3 契约 — INT8 Q/K with FP16 weights and scales (quant mode 2);
+//    section 编译范围 — FP8 (quant mode 1) as the A5 build registers it,
 //    32 or 64 heads of dim 128, ratio 1 or 2, causal mask mode 3, TopK in
 //    [1, 2048], candidate blocks in [64, 2048] and a multiple of 64, block
 //    size exactly 8;
@@ -29,7 +30,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 qli_status validate(const qli_args* a) {
   if (a == nullptr) return QLI_ERR_INVALID_ARG;
   if (a->layout_q != QLI_LAYOUT_TND || a->layout_k != QLI_LAYOUT_PA_BBND) return QLI_ERR_UNSUPPORTED;
-  if (a->quant_mode != QLI_QUANT_INT8 || a->mask_mode != QLI_MASK_CAUSAL) return QLI_ERR_UNSUPPORTED;
+  if ((a->quant_mode != QLI_QUANT_INT8 && a->quant_mode != QLI_QUANT_FP8) ||
+      a->mask_mode != QLI_MASK_CAUSAL)
+    return QLI_ERR_UNSUPPORTED;
   if (a->N != 32 && a->N != 64) return QLI_ERR_UNSUPPORTED;
   if (a->D != kHeadDim) return QLI_ERR_UNSUPPORTED;
   if (a->ratio != 1 && a->ratio != 2) return QLI_ERR_UNSUPPORTED;
@@ -200,6 +203,7 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.topk = a.topk;
   d.mode = a.cand_mode;
   d.C = a.cand_blocks;
+  d.fp8 = a.quant_mode == QLI_QUANT_FP8 ? 1 : 0;
   d.cand_in = a.cand_in;
   d.cand_out = a.cand_out;
   d.idx_out = a.indices_out;

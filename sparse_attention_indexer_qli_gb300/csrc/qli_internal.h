@@ -45,6 +45,7 @@ struct DevArgs {
   const uint16_t* w;
   const uint16_t* qs;
   int32_t ratio, topk, mode, C;
+  int32_t fp8;         // 1: q and the index K hold E4M3 codes (quant mode 1), 0: INT8
   const int32_t* cand_in;
   int32_t* cand_out;
   int32_t* idx_out;

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kConvThreads) kconv_kernel(DevArgs a) {
   const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
   const int r = row % a.R;
   const uint2 v = __ldg(reinterpret_cast<const uint2*>(pg + a.k_off + r * kHeadDim) + ch);
-  *dst = widen8(v, false);
+  *dst = a.fp8 ? e4m3x8_to_f16x8(v, false) : widen8(v, false);
   if (ch == 0)
     a.ks32[static_cast<int64_t>(b) * a.kstride + row] =
         __half2float(*reinterpret_cast<const __half*>(pg + a.s_off + r * 2));
@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           const int idx = etid + 512 * i;
           const int nn = idx >> 4, ch = idx & 15;
           if (idx < nrows * 16)
-            *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) = widen8(v[i], true);
+            *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) =
+                a.fp8 ? e4m3x8_to_f16x8(v[i], true) : widen8(v[i], true);
         }
       }
       for (int nn = etid; nn < nrows; nn += 512) {

@@ -299,6 +299,42 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---- FP8 (E4M3) codes -------------------------------------------------------
+// Every E4M3 value (largest 448, smallest 2^-9) is an FP16 value, so these
+// widenings are exact; so is the product by 2^-10 (the results stay FP16
+// values, subnormals included: the smallest is 2^-19).
+// Two codes (the low byte is the lower K index) -> two FP16 values.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(r)
+      : "r"(two_codes));
+  return r;
+}
+// 8 codes -> 8 FP16 values, optionally times 2^-10.
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v, bool div1024) {
+  uint32_t o[4] = {e4m3x2_to_f16x2(v.x & 0xFFFFu), e4m3x2_to_f16x2(v.x >> 16),
+                   e4m3x2_to_f16x2(v.y & 0xFFFFu), e4m3x2_to_f16x2(v.y >> 16)};
+  if (div1024) {
+    const __half2 s = __floats2half2_rn(1.0f / 1024.0f, 1.0f / 1024.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 x = __hmul2(*reinterpret_cast<__half2*>(&o[k]), s);
+      o[k] = *reinterpret_cast<uint32_t*>(&x);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+// 16 codes -> 16 FP16 values as 8 words (lower K index in the low half).
+__device__ __forceinline__ void e4m3x16_to_f16x16(const uint4 v, uint32_t* out8) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    out8[2 * k] = e4m3x2_to_f16x2(w[k] & 0xFFFFu);
+    out8[2 * k + 1] = e4m3x2_to_f16x2(w[k] >> 16);
+  }
+}
+
 // ---- selection keys -------------------------------------------------------
 // Order-preserving map of a finite FP32 score to a non-zero uint32 key
 // (larger score -> larger key; -0 and +0 map to the same key). Key 0 is kept

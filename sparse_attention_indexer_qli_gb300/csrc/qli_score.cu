@@ -7,7 +7,10 @@
 //
 // sm_103a has no INT8 tensor-core MMA (tcgen05 kind::i8 is not available on
 // this target), so the INT8 operands are widened to FP16 and contracted with
-// kind::f16 into FP32. This is exact: every INT8 value is an FP16 integer,
+// kind::f16 into FP32. The FP8 variant (quant mode 1, E4M3 codes) widens its
+// codes to FP16 the same way (exactly); there the FP32 sums are the tensor
+// core's, no longer exact, so its scores match the exact dot to within the
+// rounding of those sums. This is exact: every INT8 value is an FP16 integer,
 // every product is an integer below 2^15, and every partial sum of the 128
 // terms is an integer of magnitude <= 128*128*128 = 2^21 < 2^24. The queries
 // are pre-multiplied by 2^-10 (exact in FP16 for |q| <= 128), so the FP32
@@ -218,6 +221,7 @@ __device__ __forceinline__ void cvt_row16(const uint4 v, uint32_t* out8) {
 // 19 warps: the four SM sub-partitions hold 5, 5, 5 and 4 of them in 16K
 // registers each, which caps a thread at 96 registers (allocated in steps of
 // 8): a larger per-thread budget would make the launch fail
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_blk,
     DevArgs a) {
@@ -460,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
           const int idx = ctid + 128 * i;
           const int n = idx >> 4, ch = idx & 15;
           if (idx < a.N * 16)
-            *reinterpret_cast<uint4*>(&S.b[grp][sw128_off(a.N, n, ch)]) = i8x8_to_f16x8_div1024(v[i]);
+            *reinterpret_cast<uint4*>(&S.b[grp][sw128_off(a.N, n, ch)]) =
+                kFp8 ? e4m3x8_to_f16x8(v[i], true) : i8x8_to_f16x8_div1024(v[i]);
         }
         btok = t;
       }
@@ -487,7 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       for (int half = 0; half < 2; ++half) {
         uint32_t regs[32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cvt_row16(raw[4 * half + j], &regs[8 * j]);
+        for (int j = 0; j < 4; ++j) {
+          if constexpr (kFp8) {
+            e4m3x16_to_f16x16(raw[4 * half + j], &regs[8 * j]);
+          } else {
+            cvt_row16(raw[4 * half + j], &regs[8 * j]);
+          }
+        }
         tmem_st_32x32b_x32(tmem + lane_addr + sa * kSlotCols + 32 * half, regs);
       }
       tmem_st_wait();
@@ -647,7 +658,7 @@ bool encode_k_map(const DevArgs& d, int box_rows, CUtensorMap* m) {
 
 }  // namespace
 
-std::atomic<uint64_t> g_smem_stream_stream_kernel{0};
+std::atomic<uint64_t> g_smem_stream_kernel[2] = {{0}, {0}};
 
 cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
@@ -655,10 +666,13 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
     CUtensorMap tm_page, tm_blk;
     if (!encode_k_map(d, d.R, &tm_page) || !encode_k_map(d, kBlock, &tm_blk))
       return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(stream::stream_kernel), stream::kSmemBytes, g_smem_stream_stream_kernel);
+    // one instance per code type: INT8 (quant mode 2) or E4M3 (quant mode 1)
+    auto* kern = d.fp8 ? stream::stream_kernel<true> : stream::stream_kernel<false>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), stream::kSmemBytes,
+                                      g_smem_stream_kernel[d.fp8 ? 1 : 0]);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(stream::stream_kernel, dim3(d.num_sms), dim3(stream::kThreads),
-                   stream::kSmemBytes, s, tm_page, tm_blk, d);
+    e = launch_pdl(kern, dim3(d.num_sms), dim3(stream::kThreads), stream::kSmemBytes, s, tm_page,
+                   tm_blk, d);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   return launch_prefill(d, s);

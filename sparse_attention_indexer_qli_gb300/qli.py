@@ -23,6 +23,7 @@ STATUS = {
 CAND_MODES = {"none": 1, "source": 2, "consumer": 3}
 STAGE_PLAN, STAGE_SCORE, STAGE_SELECT = 1, 2, 3
 LAYOUT_TND, LAYOUT_PA_BBND, QUANT_INT8, MASK_CAUSAL = 1, 2, 2, 3
+QUANT_FP8 = 1            # q and the index K hold E4M3 codes (passed as int8 bytes)
 DEVERR = {1: "cu_seqlens", 2: "k_lens", 4: "residual", 8: "block table page", 16: "wait timeout"}
 
 
@@ -153,7 +154,7 @@ class Call:
     def __init__(self, q, cu_seqlens_q, k_lens, residual, cache, block_table, head_weights,
                  q_scale, *, ratio: int, rows_per_page: int, page_stride: int, k_offset: int,
                  scale_offset: int, topk: int, cand_mode: str = "none", cand_blocks: int = 0,
-                 cand_in=None, indices_out=None, cand_out=None):
+                 cand_in=None, indices_out=None, cand_out=None, quant_mode: int = QUANT_INT8):
         import torch
         _require_cuda("q", q, torch.int8)
         for n, t in (("cu_seqlens_q", cu_seqlens_q), ("k_lens", k_lens), ("residual", residual),
@@ -189,7 +190,7 @@ class Call:
         a.num_pages = cache.numel() // page_stride
         a.block_table = _ptr(block_table); a.bt_stride = block_table.stride(0)
         a.head_weights = _ptr(head_weights); a.q_scale = _ptr(q_scale)
-        a.ratio = ratio; a.mask_mode = MASK_CAUSAL; a.quant_mode = QUANT_INT8
+        a.ratio = ratio; a.mask_mode = MASK_CAUSAL; a.quant_mode = quant_mode
         a.layout_q = LAYOUT_TND; a.layout_k = LAYOUT_PA_BBND
         a.topk = topk; a.cand_mode = mode; a.cand_blocks = cand_blocks; a.block_size = 8
         a.cand_in = _ptr(cand_in); a.cand_in_numel = 0 if cand_in is None else cand_in.numel()

@@ -416,6 +416,19 @@ def config(idx: int, seed: Optional[int] = None) -> Case:
     raise ValueError(idx)
 
 
+def to_fp8(case: Case, stream: int = 70) -> Case:
+    """The same batch with E4M3 codes (quant mode 1) in place of the INT8
+    queries and index-K rows: every finite code (both zeros, no NaN 0x7F /
+    0xFF) equally likely, so the decoded values span 2^-9 .. 448 with both
+    signs. Scales, weights, pages and metadata are unchanged. In place."""
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    rng = _rng(case.seed, stream)
+    case.q = finite[rng.integers(0, finite.size, size=case.q.shape)]
+    case.k_rows = finite[rng.integers(0, finite.size, size=case.k_rows.shape)]
+    case.quant_mode = 1
+    return case
+
+
 def workload_pairs_upper(case: Case) -> int:
     """Sum over requests of q_len * k_len: an upper bound on scored pairs that
     needs no knowledge of the causal rule (used only to size samples)."""
@@ -436,7 +449,8 @@ def upload(case: Case, device="cuda", filler: bool = True, cache=None) -> dict:
         return x.to(device)
 
     return dict(
-        q=t(case.q), cu_seqlens_q=t(case.cu_seqlens_q), k_lens=t(case.k_lens),
+        q=t(np.asarray(case.q).view(np.int8)), cu_seqlens_q=t(case.cu_seqlens_q),
+        k_lens=t(case.k_lens), quant_mode=int(getattr(case, "quant_mode", 2)),
         residual=None if case.residual is None else t(case.residual),
         cache=case.pack_pages_torch(device, filler) if cache is None else cache,
         block_table=t(case.block_table),

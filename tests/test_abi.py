@@ -95,6 +95,12 @@ def test_contract_accepts(L, mode, ratio, N):
     assert status(L, good_args(mode, ratio=ratio, N=N)) == 0
 
 
+def test_fp8_quant_mode_is_accepted(L):
+    a = good_args("source")
+    a.quant_mode = qli.QUANT_FP8
+    assert status(L, a) == 0
+
+
 def _with(mode="none", **kw):
     a = good_args(mode, **{k: v for k, v in kw.items() if k in ("T", "B", "N", "ratio", "K", "C")})
     for k, v in kw.items():
@@ -107,7 +113,8 @@ REJECT = [
     # (mode, overrides, expected status) — contract of section 当前 A3 契约
     ("none", dict(layout_q=3), 2),                     # BSND query rejected
     ("none", dict(layout_k=3), 2),                     # non-paged key rejected
-    ("none", dict(quant_mode=1), 2),                   # FP8 quant mode not in this build
+    ("none", dict(quant_mode=3), 2),                   # quant modes other than 1 (FP8) and 2 (INT8)
+    ("none", dict(quant_mode=4), 2),
     ("none", dict(mask_mode=1), 2),
     ("none", dict(N=16), 2),
     ("none", dict(D=64), 2),
