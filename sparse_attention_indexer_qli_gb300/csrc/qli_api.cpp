@@ -171,6 +171,7 @@ WsLayout workspace_layout(const qli_args& a) {
   L.lkey = take(L.lchunks ? 4 * rows2 * L.lchunks * kLongChunkCap : 0);
   L.lid = take(L.lchunks ? 4 * rows2 * L.lchunks * kLongChunkCap : 0);
   L.fhist = take(L.stream_path ? 4 * 4096 * rows2 : 0);
+  L.flist = take(L.stream_path ? 0 : 4 * rows2);
   L.scores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Lrow));
   L.bscores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Brow));
   L.total = off;
@@ -227,6 +228,7 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.lid = reinterpret_cast<int32_t*>(w + L.lid);
   d.lchunks = L.lchunks;
   d.fhist = L.stream_path ? reinterpret_cast<uint32_t*>(w + L.fhist) : nullptr;
+  d.flist = reinterpret_cast<int32_t*>(w + L.flist);
   d.long_zero_bytes = L.long_bytes;
   d.kf16 = reinterpret_cast<__half*>(w + L.kf16);
   d.ks32 = reinterpret_cast<float*>(w + L.ks32);

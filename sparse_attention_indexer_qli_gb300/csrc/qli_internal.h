@@ -65,7 +65,9 @@ struct DevArgs {
   int32_t* cand_page;  // [T, C] consumer: the page holding each listed block (checked)
   uint4* cand_sc;      // [T, C] consumer: each listed block's eight FP16 K scales
   int32_t* unit_start; // [T+1] stream path: first score tile of token t
-  uint32_t* counter;   // stream path: CTAs done in cand_prep (reset by plan)
+  uint32_t* counter;   // consumer: CTAs done in the candidate kernel; group path: rows
+                       // listed in flist (reset by plan)
+  int32_t* flist;      // group path: [2T] rows (2t + which) left to the general selection
   __half* kf16;        // group path: [B, kstride, 128] widened K
   float* ks32;         // group path: [B, kstride] K scales as FP32
   int64_t kstride;     // group path: rows per request (cap rounded up to 128)
@@ -93,7 +95,7 @@ struct DevArgs {
 struct WsLayout {
   size_t err, counter, tok_V, tok_b, req_lk, req_res, req_q0, req_q1, req_g0;
   size_t grp_t0, grp_cnt, unit_start, cand_list, cand_cnt, cand_page, cand_sc, kf16, ks32, scores,
-      bscores, total;
+      bscores, flist, total;
   size_t lext, lhist, lcount, lkey, lid, long_bytes;   // long-row selection (zeroed region: lext..lcount)
   size_t fhist;
   int32_t lchunks;

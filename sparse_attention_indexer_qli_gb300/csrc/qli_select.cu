@@ -1205,13 +1205,10 @@ __device__ __noinline__ int select_long_row(const DevArgs& a, int t, int which, 
 // histogram paths. One instance per launch mode (score-stage histogram or
 // not, consumer rows or not), so each holds only the code its rows can take.
 template <bool kFused, bool kConsumerMode>
-__global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key_cap,
-                                                          int32_t region) {
-  extern __shared__ uint32_t keys[];
+__device__ __forceinline__ void select_one(const DevArgs& a, int t, int which, int32_t key_cap,
+                                           int32_t region, uint32_t* keys, Shared& sh) {
   uint32_t* scratch = keys + region;
-  pdl_wait();
-  __shared__ Shared sh;
-  const int t = blockIdx.x, which = blockIdx.y, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const bool blocks = which == 1;
   const int32_t width = blocks ? a.C : a.topk;
   int32_t* out = blocks ? a.cand_out + static_cast<int64_t>(t) * a.C
@@ -1337,11 +1334,353 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
   for (int k = written + tid; k < width; k += kThreads) out[k] = -1;
 }
 
+template <bool kFused, bool kConsumerMode>
+__global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key_cap,
+                                                          int32_t region) {
+  extern __shared__ uint32_t keys[];
+  pdl_wait();
+  __shared__ Shared sh;
+  select_one<kFused, kConsumerMode>(a, blockIdx.x, blockIdx.y, key_cap, region, keys, sh);
+}
+
+// ---------------------------------------------------------------------------
+// Rows without a score-stage histogram (the prefill path): one CTA of 256
+// threads per row, several rows in flight on each SM. One pass over the row
+// (from HBM) counts the top 12 key bits in a shared-memory histogram, which
+// gives the threshold bin; a second pass (from L2) keeps the entries at or
+// above that bin in row order (a count sweep and a write sweep per warp
+// segment); an exact refine on the remaining 20 bits finds the threshold
+// key; one ordered pass writes the ids. A row this path cannot finish (longer
+// than kSmemKeys entries, or more than kFCap entries at or above the
+// threshold bin, as with heavy ties) is appended to a list for the general
+// selection (select_list_kernel), which ranks it exactly.
+constexpr int kFT = 256;
+constexpr int kFW = kFT / 32;
+constexpr int kFCap = 4096;
+
+struct FastSmem {
+  uint32_t hist[kHistBins];    // top-12-bit histogram, then the refine's 10-bit digits
+  uint32_t ckey[kFCap];        // candidates in row order
+  int32_t cid[kFCap];
+  uint32_t wtot[kFW];
+  uint32_t sel[4];
+};
+
+// Inclusive block scan over the 256 threads of one value each; `total` gets
+// the block sum. Two barriers.
+__device__ __forceinline__ uint32_t fast_scan(uint32_t v, uint32_t& total, FastSmem& F) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) F.wtot[warp] = incl;
+  __syncthreads();
+  uint32_t w = lane < kFW ? F.wtot[lane] : 0u, wincl = w;
+#pragma unroll
+  for (int o = 1; o < kFW; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  total = __shfl_sync(0xffffffffu, wincl, kFW - 1);
+  const uint32_t before = __shfl_sync(0xffffffffu, wincl - w, warp);
+  __syncthreads();                                   // wtot is reused by the next scan
+  return incl + before;
+}
+
+__device__ __forceinline__ void enlist(const DevArgs& a, int t, int which) {
+  if (threadIdx.x == 0) {
+    const uint32_t i = atomicAdd(a.counter, 1u);
+    a.flist[i] = 2 * t + which;
+  }
+}
+
+__global__ void __launch_bounds__(kFT) fast_select_kernel(DevArgs a) {
+  extern __shared__ __align__(16) uint8_t fs_raw[];
+  FastSmem& F = *reinterpret_cast<FastSmem*>(fs_raw);
+  pdl_wait();
+  const int t = blockIdx.x, which = blockIdx.y, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const bool blocks = which == 1;
+  const int32_t width = blocks ? a.C : a.topk;
+  int32_t* out = blocks ? a.cand_out + static_cast<int64_t>(t) * a.C
+                        : a.idx_out + static_cast<int64_t>(t) * a.topk;
+  int32_t want;
+  const Row r = row_of(a, t, which, want);
+  const int32_t nb = (r.V + kBlock - 1) / kBlock;
+  const int32_t len = r.len;
+  int32_t written = 0;
+  if (len > kSmemKeys) {
+    enlist(a, t, which);
+    return;
+  }
+  if (blocks && len == 0) {
+    // at most C visible blocks: all of them, in order
+    for (int c = tid; c < nb; c += kFT) out[c] = c;
+    written = nb;
+  } else if (len <= want) {
+    // every entry is selected (all entries of these rows are eligible)
+    for (int s = tid; s < len; s += kFT) out[s] = s;
+    written = len;
+    if (blocks) {
+      if (tid == 0) out[written] = nb - 1;            // the pinned last visible block
+      written += 1;
+    }
+  } else {
+    // ---- pass 1: top-12-bit histogram
+    for (int i = tid; i < kHistBins; i += kFT) F.hist[i] = 0u;
+    __syncthreads();
+    const float4* v4 = reinterpret_cast<const float4*>(r.vals);
+    const int32_t n4 = (len + 3) >> 2;
+    for (int32_t base = 0; base < n4; base += 8 * kFT) {
+      float4 f[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int32_t i4 = base + u * kFT + tid;
+        f[u] = i4 < n4 ? __ldcg(v4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int32_t s0 = 4 * (base + u * kFT + tid);
+        const float fv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (s0 + j < len) atomicAdd(&F.hist[hist_bin(order_key(fv[j]))], 1u);
+      }
+    }
+    __syncthreads();
+    // ---- threshold bin: thread i holds bins 4095-16i .. 4080-16i
+    uint32_t c[16], mine = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      c[j] = F.hist[kHistBins - 1 - 16 * tid - j];
+      mine += c[j];
+    }
+    uint32_t E;
+    const uint32_t incl = fast_scan(mine, E, F);
+    {
+      const uint32_t k = static_cast<uint32_t>(want);
+      uint32_t above = incl - mine;
+      if (above < k && k <= incl) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (above + c[j] >= k) {
+            F.sel[0] = static_cast<uint32_t>(kHistBins - 1 - 16 * tid - j);
+            F.sel[1] = above;
+            F.sel[2] = c[j];
+            break;
+          }
+          above += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t sel = F.sel[0], abv = F.sel[1], cbin = F.sel[2];
+    const uint32_t n_want = abv + cbin;
+    if (n_want > static_cast<uint32_t>(kFCap)) {       // block-uniform
+      enlist(a, t, which);
+      return;
+    }
+    // ---- pass 2: entries with key >= the bin's lowest key, in row order;
+    // warp w owns a contiguous segment, 128 entries (a float4 per lane) per step
+    const uint32_t t_lo = sel << (32 - kHistBits);
+    const int32_t seg = ((len + kFW - 1) / kFW + 127) & ~127;
+    const int32_t lo = warp * seg, hi = min(len, lo + seg);
+    // eight steps' loads are issued before any is used (one L2 round trip
+    // per 1024 entries of the segment instead of one per 128)
+    constexpr int kB = 8;
+    const auto load8 = [&](int32_t b, float4 (&f)[kB]) {
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int32_t s0 = b + 128 * u + 4 * lane;
+        f[u] = s0 < hi ? __ldcg(v4 + (s0 >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    };
+    const auto keep_bits = [&](int32_t s0, const float4& f, uint32_t (&k)[4]) {
+      k[0] = order_key(f.x); k[1] = order_key(f.y); k[2] = order_key(f.z); k[3] = order_key(f.w);
+      uint32_t m = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m |= (s0 + j < hi && k[j] >= t_lo) ? (1u << j) : 0u;
+      return m;
+    };
+    uint32_t wcount = 0u;
+    for (int32_t b = lo; b < hi; b += 128 * kB) {
+      float4 f[kB];
+      load8(b, f);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        uint32_t k[4];
+        const uint32_t m = keep_bits(b + 128 * u + 4 * lane, f[u], k);
+        wcount += __popc(m);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wcount += __shfl_xor_sync(0xffffffffu, wcount, o);
+    if (lane == 0) F.wtot[warp] = wcount;
+    __syncthreads();
+    uint32_t at = 0u, total = 0u;
+#pragma unroll
+    for (int w = 0; w < kFW; ++w) {
+      const uint32_t x = F.wtot[w];
+      at += w < warp ? x : 0u;
+      total += x;
+    }
+    __syncthreads();
+    if (total != n_want) {                            // block-uniform
+      enlist(a, t, which);
+      return;
+    }
+    for (int32_t b = lo; b < hi; b += 128 * kB) {
+      float4 f[kB];
+      load8(b, f);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        uint32_t k[4];
+        const int32_t s0 = b + 128 * u + 4 * lane;
+        const uint32_t m = keep_bits(s0, f[u], k);
+        const uint32_t cnt = __popc(m);
+        uint32_t pre = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, pre, o);
+          if (lane >= o) pre += y;
+        }
+        uint32_t pos = at + pre - cnt;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if ((m >> j) & 1u) {
+            F.ckey[pos] = k[j];
+            F.cid[pos] = s0 + j;
+            ++pos;
+          }
+        }
+        at += __shfl_sync(0xffffffffu, pre, 31);
+      }
+    }
+    __syncthreads();
+    // ---- exact threshold inside bin `sel`: the k-th largest of its keys,
+    // two 10-bit digits below the top 12 bits
+    int32_t k2 = want - static_cast<int32_t>(abv);     // 1 .. cbin
+    uint32_t prefix = sel << (32 - kHistBits), mask = ~0u << (32 - kHistBits);
+    uint32_t thr = 0u;
+    int32_t need_eq = 0;
+    bool settled = false;
+    const int32_t n = static_cast<int32_t>(total);
+    for (int shift = 32 - kHistBits - 10; shift >= 0 && !settled; shift -= 10) {
+      for (int i = tid; i < 1024; i += kFT) F.hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < n; i += kFT) {
+        const uint32_t key = F.ckey[i];
+        if ((key & mask) == prefix) atomicAdd(&F.hist[(key >> shift) & 1023u], 1u);
+      }
+      __syncthreads();
+      // thread i holds digits 1023-4i .. 1020-4i
+      uint32_t d[4], dm = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        d[j] = F.hist[1023 - 4 * tid - j];
+        dm += d[j];
+      }
+      uint32_t dtot;
+      const uint32_t dincl = fast_scan(dm, dtot, F);
+      {
+        const uint32_t kk = static_cast<uint32_t>(k2);
+        uint32_t above = dincl - dm;
+        if (above < kk && kk <= dincl) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (above + d[j] >= kk) {
+              F.sel[0] = static_cast<uint32_t>(1023 - 4 * tid - j);
+              F.sel[1] = above;
+              F.sel[2] = d[j];
+              break;
+            }
+            above += d[j];
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t dsel = F.sel[0];
+      k2 -= static_cast<int32_t>(F.sel[1]);
+      const uint32_t in_digit = F.sel[2];
+      __syncthreads();
+      prefix |= dsel << shift;
+      mask |= 1023u << shift;
+      if (in_digit == static_cast<uint32_t>(k2)) {
+        thr = prefix - 1u;                             // every key of this digit and above
+        need_eq = 0;
+        settled = true;
+      }
+    }
+    if (!settled) {
+      thr = prefix;
+      need_eq = k2;
+    }
+    // ---- ordered output: thread i takes candidates [i*per, (i+1)*per)
+    const int32_t per = (n + kFT - 1) / kFT;
+    const int32_t i0 = min(n, tid * per), i1 = min(n, i0 + per);
+    uint32_t gt = 0u, eq = 0u;
+    for (int32_t i = i0; i < i1; ++i) {
+      const uint32_t key = F.ckey[i];
+      gt += key > thr ? 1u : 0u;
+      eq += key == thr ? 1u : 0u;
+    }
+    uint32_t gt_tot, eq_tot;
+    const uint32_t gt_incl = fast_scan(gt, gt_tot, F);
+    const uint32_t eq_incl = fast_scan(eq, eq_tot, F);
+    const uint32_t ne = static_cast<uint32_t>(need_eq);
+    uint32_t eq_seen = eq_incl - eq;
+    uint32_t o = (gt_incl - gt) + min(eq_seen, ne);
+    for (int32_t i = i0; i < i1; ++i) {
+      const uint32_t key = F.ckey[i];
+      const bool take = key > thr || (key == thr && eq_seen < ne);
+      if (key == thr) ++eq_seen;
+      if (take) {
+        if (o < static_cast<uint32_t>(want)) out[o] = F.cid[i];
+        ++o;
+      }
+    }
+    written = min(static_cast<int32_t>(gt_tot + min(eq_tot, ne)), want);
+    if (blocks) {
+      if (tid == 0) out[written] = nb - 1;            // the pinned last visible block
+      written += 1;
+    }
+  }
+  for (int k = written + tid; k < width; k += kFT) out[k] = -1;
+}
+
+// The general selection for the rows fast_select_kernel listed, a
+// persistent grid walking the list.
+__global__ void __launch_bounds__(kThreads) select_list_kernel(DevArgs a, int32_t key_cap,
+                                                               int32_t region) {
+  extern __shared__ uint32_t keys[];
+  pdl_wait();
+  __shared__ Shared sh;
+  const uint32_t n = __ldcg(a.counter);
+  for (uint32_t i = blockIdx.x; i < n; i += gridDim.x) {
+    const int32_t item = __ldcg(a.flist + i);
+    select_one<false, false>(a, item >> 1, item & 1, key_cap, region, keys, sh);
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
   cudaError_t e;
+  if (d.fhist == nullptr && d.mode != QLI_CAND_CONSUMER) {
+    static std::atomic<uint64_t> done_fast{0};
+    e = ensure_smem_limit(reinterpret_cast<const void*>(fast_select_kernel),
+                          static_cast<int>(sizeof(FastSmem)), done_fast);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(fast_select_kernel,
+                   dim3(static_cast<unsigned>(d.T), d.mode == QLI_CAND_SOURCE ? 2u : 1u),
+                   dim3(kFT), sizeof(FastSmem), s, d);
+    if (e != cudaSuccess) return e;
+  }
   if (d.lchunks > 0) {
     const dim3 g(static_cast<unsigned>(d.lchunks), static_cast<unsigned>(d.T),
                  d.mode == QLI_CAND_SOURCE ? 2u : 1u);
@@ -1368,6 +1707,17 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
   // candidate rows need room for kLongCandCap keys and ids
   const int32_t region = d.lchunks > 0 ? (cap > 2 * kLongCandCap ? cap : 2 * kLongCandCap) : cap;
   const int smem = 4 * (region + kHeadWords + kCandCap);
+  if (d.fhist == nullptr && d.mode != QLI_CAND_CONSUMER) {
+    // rows without a score-stage histogram: the many-rows-per-SM pass, then
+    // the general selection for the rows it listed
+    static std::atomic<uint64_t> done_list{0};
+    e = ensure_smem_limit(reinterpret_cast<const void*>(select_list_kernel),
+                          4 * (kSmemKeys + kHeadWords + kCandCap), done_list);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(select_list_kernel, dim3(static_cast<unsigned>(d.num_sms)), dim3(kThreads),
+                   static_cast<size_t>(smem), s, d, cap, region);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
   void (*const kernels[4])(DevArgs, int32_t, int32_t) = {
       select_kernel<false, false>, select_kernel<false, true>, select_kernel<true, false>,
@@ -1384,8 +1734,9 @@ cudaError_t launch_select(const DevArgs& d, cudaStream_t s) {
 
 int select_launches(const DevArgs& d) {
   if (d.T == 0) return 0;
-  if (d.lchunks == 0) return 1;
-  return d.fhist != nullptr ? 2 : 4;
+  const int fast = (d.fhist == nullptr && d.mode != QLI_CAND_CONSUMER) ? 1 : 0;
+  if (d.lchunks == 0) return 1 + fast;
+  return (d.fhist != nullptr ? 2 : 4) + fast;
 }
 
 }  // namespace qli
