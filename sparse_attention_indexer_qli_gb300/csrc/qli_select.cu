@@ -1345,24 +1345,33 @@ __global__ void __launch_bounds__(kThreads) select_kernel(DevArgs a, int32_t key
 
 // ---------------------------------------------------------------------------
 // Rows without a score-stage histogram (the prefill path): one CTA of 256
-// threads per row, several rows in flight on each SM. One pass over the row
-// (from HBM) counts the top 12 key bits in a shared-memory histogram, which
-// gives the threshold bin; a second pass (from L2) keeps the entries at or
-// above that bin in row order (a count sweep and a write sweep per warp
-// segment); an exact refine on the remaining 20 bits finds the threshold
-// key; one ordered pass writes the ids. A row this path cannot finish (longer
-// than kSmemKeys entries, or more than kFCap entries at or above the
-// threshold bin, as with heavy ties) is appended to a list for the general
-// selection (select_list_kernel), which ranks it exactly.
+// threads per row, five rows in flight on each SM, each row read from HBM
+// once. A row longer than the candidate space first draws a sample of 1024
+// entries (16 evenly spread runs of 64); the key of a rank a little past the
+// expected rank of the want-th best in the sample gives a provisional
+// threshold. One pass over the row keeps every entry at or above it (slots
+// claimed per warp step, in no particular order); an exact radix select on
+// the candidates (digits of 12, 10 and 10 bits) finds the want-th best key;
+// the winners are marked in position bitmaps, and one ordered scan of the
+// bitmaps writes them in ascending order (equal keys at the threshold by
+// lower position). A row this path cannot finish (longer than kSmemKeys
+// entries, a sample that misjudged: fewer than `want` or more than kFCap
+// candidates) is appended to a list for the general selection
+// (select_list_kernel), which ranks it exactly.
 constexpr int kFT = 256;
 constexpr int kFW = kFT / 32;
-constexpr int kFCap = 4096;
+constexpr int kFCap = 4608;                        // candidates a row may keep
+constexpr int kBitWords = (kSmemKeys + 31) / 32;   // one bit per position of a row
+constexpr int kSample = 1024;
+static_assert(2 * kBitWords <= kHistBins, "the two bitmaps fit the histogram space");
+static_assert(kSmemKeys <= 65536, "candidate positions are 16-bit");
 
 struct FastSmem {
-  uint32_t hist[kHistBins];    // top-12-bit histogram, then the refine's 10-bit digits
-  uint32_t ckey[kFCap];        // candidates in row order
-  int32_t cid[kFCap];
+  uint32_t hist[kHistBins];    // the sample's histogram, the radix digits, then the bitmaps
+  uint32_t ckey[kFCap];        // candidates (any order)
+  uint16_t cid[kFCap];
   uint32_t wtot[kFW];
+  uint32_t cnt;                // candidates claimed
   uint32_t sel[4];
 };
 
@@ -1388,6 +1397,38 @@ __device__ __forceinline__ uint32_t fast_scan(uint32_t v, uint32_t& total, FastS
   const uint32_t before = __shfl_sync(0xffffffffu, wincl - w, warp);
   __syncthreads();                                   // wtot is reused by the next scan
   return incl + before;
+}
+
+// The digit (from the top) of a histogram of nbins = 256 * per bins at which
+// the running count reaches k: its value, the count above it and its own
+// count, left in F.sel[0..2] for every thread. Thread i holds bins
+// nbins-1-per*i .. nbins-per*(i+1).
+template <int kPer>
+__device__ __forceinline__ void fast_pick(const uint32_t* hist, uint32_t k, FastSmem& F) {
+  const int tid = threadIdx.x;
+  constexpr int nbins = kPer * kFT;
+  uint32_t c[kPer], mine = 0u;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    c[j] = hist[nbins - 1 - kPer * tid - j];
+    mine += c[j];
+  }
+  uint32_t tot;
+  const uint32_t incl = fast_scan(mine, tot, F);
+  uint32_t above = incl - mine;
+  if (above < k && k <= incl) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (above + c[j] >= k) {
+        F.sel[0] = static_cast<uint32_t>(nbins - 1 - kPer * tid - j);
+        F.sel[1] = above;
+        F.sel[2] = c[j];
+        break;
+      }
+      above += c[j];
+    }
+  }
+  __syncthreads();
 }
 
 __device__ __forceinline__ void enlist(const DevArgs& a, int t, int which) {
@@ -1429,185 +1470,109 @@ __global__ void __launch_bounds__(kFT) fast_select_kernel(DevArgs a) {
       written += 1;
     }
   } else {
-    // ---- pass 1: top-12-bit histogram
-    for (int i = tid; i < kHistBins; i += kFT) F.hist[i] = 0u;
-    __syncthreads();
     const float4* v4 = reinterpret_cast<const float4*>(r.vals);
-    const int32_t n4 = (len + 3) >> 2;
-    for (int32_t base = 0; base < n4; base += 8 * kFT) {
-      float4 f[8];
+    // ---- provisional threshold (keep everything when the row fits)
+    uint32_t t_p = 0u;
+    if (len > kFCap) {
+      for (int i = tid; i < kHistBins; i += kFT) F.hist[i] = 0u;
+      __syncthreads();
+      // thread i: entries 4(i%16) .. of run i/16, the runs starting at
+      // (len * run / 16) rounded down to a multiple of 4
+      const int32_t s0 = static_cast<int32_t>((static_cast<int64_t>(len) * (tid >> 4) / 16) & ~3LL) +
+                         4 * (tid & 15);
+      const float4 f = __ldcg(v4 + (s0 >> 2));
+      const float fv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int32_t i4 = base + u * kFT + tid;
-        f[u] = i4 < n4 ? __ldcg(v4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < 4; ++j)
+        if (s0 + j < len) atomicAdd(&F.hist[hist_bin(order_key(fv[j]))], 1u);
+      __syncthreads();
+      // a rank 10% past the want-th best's expected sample rank, plus 24
+      const uint32_t rank = static_cast<uint32_t>(
+          (static_cast<int64_t>(want) * kSample * 11) / (10 * static_cast<int64_t>(len))) + 24u;
+      if (rank >= static_cast<uint32_t>(kSample) - 64u) {   // block-uniform
+        enlist(a, t, which);
+        return;
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int32_t s0 = 4 * (base + u * kFT + tid);
-        const float fv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (s0 + j < len) atomicAdd(&F.hist[hist_bin(order_key(fv[j]))], 1u);
-      }
+      fast_pick<kHistBins / kFT>(F.hist, rank, F);
+      t_p = F.sel[0] << (32 - kHistBits);
     }
+    // ---- one pass over the row: every entry with key >= t_p; warp w owns
+    // a contiguous segment, eight 128-entry steps per batch of loads
+    if (tid == 0) F.cnt = 0u;
     __syncthreads();
-    // ---- threshold bin: thread i holds bins 4095-16i .. 4080-16i
-    uint32_t c[16], mine = 0u;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      c[j] = F.hist[kHistBins - 1 - 16 * tid - j];
-      mine += c[j];
-    }
-    uint32_t E;
-    const uint32_t incl = fast_scan(mine, E, F);
     {
-      const uint32_t k = static_cast<uint32_t>(want);
-      uint32_t above = incl - mine;
-      if (above < k && k <= incl) {
+      const int32_t seg = ((len + kFW - 1) / kFW + 127) & ~127;
+      const int32_t lo = warp * seg, hi = min(len, lo + seg);
+      const unsigned below = (1u << lane) - 1u;
+      constexpr int kB = 8;
+      for (int32_t b = lo; b < hi; b += 128 * kB) {
+        float4 f[kB];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (above + c[j] >= k) {
-            F.sel[0] = static_cast<uint32_t>(kHistBins - 1 - 16 * tid - j);
-            F.sel[1] = above;
-            F.sel[2] = c[j];
-            break;
-          }
-          above += c[j];
+        for (int u = 0; u < kB; ++u) {
+          const int32_t s0 = b + 128 * u + 4 * lane;
+          f[u] = s0 < hi ? __ldcg(v4 + (s0 >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
-    }
-    __syncthreads();
-    const uint32_t sel = F.sel[0], abv = F.sel[1], cbin = F.sel[2];
-    const uint32_t n_want = abv + cbin;
-    if (n_want > static_cast<uint32_t>(kFCap)) {       // block-uniform
-      enlist(a, t, which);
-      return;
-    }
-    // ---- pass 2: entries with key >= the bin's lowest key, in row order;
-    // warp w owns a contiguous segment, 128 entries (a float4 per lane) per step
-    const uint32_t t_lo = sel << (32 - kHistBits);
-    const int32_t seg = ((len + kFW - 1) / kFW + 127) & ~127;
-    const int32_t lo = warp * seg, hi = min(len, lo + seg);
-    // eight steps' loads are issued before any is used (one L2 round trip
-    // per 1024 entries of the segment instead of one per 128)
-    constexpr int kB = 8;
-    const auto load8 = [&](int32_t b, float4 (&f)[kB]) {
 #pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        const int32_t s0 = b + 128 * u + 4 * lane;
-        f[u] = s0 < hi ? __ldcg(v4 + (s0 >> 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    };
-    const auto keep_bits = [&](int32_t s0, const float4& f, uint32_t (&k)[4]) {
-      k[0] = order_key(f.x); k[1] = order_key(f.y); k[2] = order_key(f.z); k[3] = order_key(f.w);
-      uint32_t m = 0u;
+        for (int u = 0; u < kB; ++u) {
+          const int32_t s0 = b + 128 * u + 4 * lane;
+          const uint32_t k[4] = {order_key(f[u].x), order_key(f[u].y), order_key(f[u].z),
+                                 order_key(f[u].w)};
+          uint32_t m = 0u;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) m |= (s0 + j < hi && k[j] >= t_lo) ? (1u << j) : 0u;
-      return m;
-    };
-    uint32_t wcount = 0u;
-    for (int32_t b = lo; b < hi; b += 128 * kB) {
-      float4 f[kB];
-      load8(b, f);
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        uint32_t k[4];
-        const uint32_t m = keep_bits(b + 128 * u + 4 * lane, f[u], k);
-        wcount += __popc(m);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wcount += __shfl_xor_sync(0xffffffffu, wcount, o);
-    if (lane == 0) F.wtot[warp] = wcount;
-    __syncthreads();
-    uint32_t at = 0u, total = 0u;
-#pragma unroll
-    for (int w = 0; w < kFW; ++w) {
-      const uint32_t x = F.wtot[w];
-      at += w < warp ? x : 0u;
-      total += x;
-    }
-    __syncthreads();
-    if (total != n_want) {                            // block-uniform
-      enlist(a, t, which);
-      return;
-    }
-    for (int32_t b = lo; b < hi; b += 128 * kB) {
-      float4 f[kB];
-      load8(b, f);
-#pragma unroll
-      for (int u = 0; u < kB; ++u) {
-        uint32_t k[4];
-        const int32_t s0 = b + 128 * u + 4 * lane;
-        const uint32_t m = keep_bits(s0, f[u], k);
-        const uint32_t cnt = __popc(m);
-        uint32_t pre = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, pre, o);
-          if (lane >= o) pre += y;
-        }
-        uint32_t pos = at + pre - cnt;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if ((m >> j) & 1u) {
-            F.ckey[pos] = k[j];
-            F.cid[pos] = s0 + j;
-            ++pos;
-          }
-        }
-        at += __shfl_sync(0xffffffffu, pre, 31);
-      }
-    }
-    __syncthreads();
-    // ---- exact threshold inside bin `sel`: the k-th largest of its keys,
-    // two 10-bit digits below the top 12 bits
-    int32_t k2 = want - static_cast<int32_t>(abv);     // 1 .. cbin
-    uint32_t prefix = sel << (32 - kHistBits), mask = ~0u << (32 - kHistBits);
-    uint32_t thr = 0u;
-    int32_t need_eq = 0;
-    bool settled = false;
-    const int32_t n = static_cast<int32_t>(total);
-    for (int shift = 32 - kHistBits - 10; shift >= 0 && !settled; shift -= 10) {
-      for (int i = tid; i < 1024; i += kFT) F.hist[i] = 0u;
-      __syncthreads();
-      for (int i = tid; i < n; i += kFT) {
-        const uint32_t key = F.ckey[i];
-        if ((key & mask) == prefix) atomicAdd(&F.hist[(key >> shift) & 1023u], 1u);
-      }
-      __syncthreads();
-      // thread i holds digits 1023-4i .. 1020-4i
-      uint32_t d[4], dm = 0u;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        d[j] = F.hist[1023 - 4 * tid - j];
-        dm += d[j];
-      }
-      uint32_t dtot;
-      const uint32_t dincl = fast_scan(dm, dtot, F);
-      {
-        const uint32_t kk = static_cast<uint32_t>(k2);
-        uint32_t above = dincl - dm;
-        if (above < kk && kk <= dincl) {
+          for (int j = 0; j < 4; ++j) m |= (s0 + j < hi && k[j] >= t_p) ? (1u << j) : 0u;
+          const uint32_t cnt = __popc(m);
+          const unsigned b0 = __ballot_sync(0xffffffffu, cnt & 1u);
+          const unsigned b1 = __ballot_sync(0xffffffffu, cnt & 2u);
+          const unsigned b2 = __ballot_sync(0xffffffffu, cnt & 4u);
+          const uint32_t tot = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+          if (tot == 0u) continue;                      // warp-uniform
+          uint32_t base = 0u;
+          if (lane == 0) base = atomicAdd(&F.cnt, tot);
+          base = __shfl_sync(0xffffffffu, base, 0) + __popc(b0 & below) + 2 * __popc(b1 & below) +
+                 4 * __popc(b2 & below);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            if (above + d[j] >= kk) {
-              F.sel[0] = static_cast<uint32_t>(1023 - 4 * tid - j);
-              F.sel[1] = above;
-              F.sel[2] = d[j];
-              break;
+            if ((m >> j) & 1u) {
+              if (base < static_cast<uint32_t>(kFCap)) {
+                F.ckey[base] = k[j];
+                F.cid[base] = static_cast<uint16_t>(s0 + j);
+              }
+              ++base;
             }
-            above += d[j];
           }
         }
       }
+    }
+    __syncthreads();
+    const uint32_t n = F.cnt;
+    if (n > static_cast<uint32_t>(kFCap) || n < static_cast<uint32_t>(want)) {   // block-uniform
+      enlist(a, t, which);
+      return;
+    }
+    // ---- the want-th best key among the candidates: digits of 12, 10, 10 bits
+    uint32_t prefix = 0u, mask = 0u, thr = 0u;
+    int32_t k2 = want, need_eq = 0;
+    bool settled = false;
+#pragma unroll 1
+    for (int round = 0; round < 3 && !settled; ++round) {
+      const int width_b = round == 0 ? kHistBits : 10;
+      const int shift = round == 0 ? 32 - kHistBits : (round == 1 ? 10 : 0);
+      const int nbins = 1 << width_b;
+      for (int i = tid; i < nbins; i += kFT) F.hist[i] = 0u;
       __syncthreads();
-      const uint32_t dsel = F.sel[0];
+      for (uint32_t i = tid; i < n; i += kFT) {
+        const uint32_t key = F.ckey[i];
+        if ((key & mask) == prefix) atomicAdd(&F.hist[(key >> shift) & (nbins - 1)], 1u);
+      }
+      __syncthreads();
+      if (round == 0) fast_pick<kHistBins / kFT>(F.hist, static_cast<uint32_t>(k2), F);
+      else fast_pick<1024 / kFT>(F.hist, static_cast<uint32_t>(k2), F);
+      const uint32_t d = F.sel[0];
       k2 -= static_cast<int32_t>(F.sel[1]);
       const uint32_t in_digit = F.sel[2];
       __syncthreads();
-      prefix |= dsel << shift;
-      mask |= 1023u << shift;
+      prefix |= d << shift;
+      mask |= static_cast<uint32_t>(nbins - 1) << shift;
       if (in_digit == static_cast<uint32_t>(k2)) {
         thr = prefix - 1u;                             // every key of this digit and above
         need_eq = 0;
@@ -1618,28 +1583,51 @@ __global__ void __launch_bounds__(kFT) fast_select_kernel(DevArgs a) {
       thr = prefix;
       need_eq = k2;
     }
-    // ---- ordered output: thread i takes candidates [i*per, (i+1)*per)
-    const int32_t per = (n + kFT - 1) / kFT;
-    const int32_t i0 = min(n, tid * per), i1 = min(n, i0 + per);
-    uint32_t gt = 0u, eq = 0u;
-    for (int32_t i = i0; i < i1; ++i) {
+    // ---- winners into position bitmaps (gt: key > thr, eq: key == thr)
+    uint32_t* gtb = F.hist;
+    uint32_t* eqb = F.hist + kBitWords;
+    const int32_t words = (len + 31) >> 5;
+    for (int i = tid; i < words; i += kFT) {
+      gtb[i] = 0u;
+      eqb[i] = 0u;
+    }
+    __syncthreads();
+    for (uint32_t i = tid; i < n; i += kFT) {
       const uint32_t key = F.ckey[i];
-      gt += key > thr ? 1u : 0u;
-      eq += key == thr ? 1u : 0u;
+      const uint32_t pos = F.cid[i];
+      if (key > thr) atomicOr(&gtb[pos >> 5], 1u << (pos & 31));
+      else if (key == thr) atomicOr(&eqb[pos >> 5], 1u << (pos & 31));
+    }
+    __syncthreads();
+    // ---- ordered scan: thread i owns words [i*per, (i+1)*per)
+    const int32_t per = (words + kFT - 1) / kFT;
+    const int32_t w0 = min(words, tid * per), w1 = min(words, w0 + per);
+    uint32_t cg = 0u, ce = 0u;
+    for (int32_t w = w0; w < w1; ++w) {
+      cg += __popc(gtb[w]);
+      ce += __popc(eqb[w]);
     }
     uint32_t gt_tot, eq_tot;
-    const uint32_t gt_incl = fast_scan(gt, gt_tot, F);
-    const uint32_t eq_incl = fast_scan(eq, eq_tot, F);
+    const uint32_t gt_incl = fast_scan(cg, gt_tot, F);
+    const uint32_t eq_incl = fast_scan(ce, eq_tot, F);
     const uint32_t ne = static_cast<uint32_t>(need_eq);
-    uint32_t eq_seen = eq_incl - eq;
-    uint32_t o = (gt_incl - gt) + min(eq_seen, ne);
-    for (int32_t i = i0; i < i1; ++i) {
-      const uint32_t key = F.ckey[i];
-      const bool take = key > thr || (key == thr && eq_seen < ne);
-      if (key == thr) ++eq_seen;
-      if (take) {
-        if (o < static_cast<uint32_t>(want)) out[o] = F.cid[i];
-        ++o;
+    uint32_t eq_seen = eq_incl - ce;
+    uint32_t o = (gt_incl - cg) + min(eq_seen, ne);
+    for (int32_t w = w0; w < w1; ++w) {
+      const uint32_t g = gtb[w], e = eqb[w];
+      uint32_t bits = g | e;
+      while (bits) {
+        const int bpos = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        bool take = true;
+        if (!((g >> bpos) & 1u)) {
+          take = eq_seen < ne;
+          ++eq_seen;
+        }
+        if (take) {
+          if (o < static_cast<uint32_t>(want)) out[o] = w * 32 + bpos;
+          ++o;
+        }
       }
     }
     written = min(static_cast<int32_t>(gt_tot + min(eq_tot, ne)), want);
