@@ -39,10 +39,16 @@ L2_BYTES = 129 * 1024 * 1024
 ROTATE_SETS = {1: 1, 2: 3, 3: 16, 4: 8, 5: 1}
 SCORE_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_score.cu")
 PREFILL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_prefill.cu")
+ATTN_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_attn.cu")
 # workload -> (committed ncu summary, the kernel source it was taken on)
 PROFILES = {
-    2: ("stream_kernel_decode_b64_ratio1.md", SCORE_SRC, "score_source_sha256"),
+    1: ("stream_kernel_decode_b1_ratio2.md", SCORE_SRC, "stream_source_sha256"),
+    2: ("stream_kernel_decode_b64_ratio1.md", SCORE_SRC, "stream_source_sha256"),
     3: ("prefill_kernel_prefill_t4096_2x2048.md", PREFILL_SRC, "prefill_source_sha256"),
+    4: ("stream_kernel_consumer_b32_ratio2.md", SCORE_SRC, "stream_source_sha256"),
+    # captured on 2 of the 8 1M-context requests and scaled by scored pairs
+    5: ("stream_kernel_longctx_2of8x1M.md", SCORE_SRC, "stream_source_sha256"),
+    "attn": ("attn_kernel_decode_b64_h64_topk2048.md", ATTN_SRC, "attn_source_sha256"),
 }
 
 
@@ -175,8 +181,10 @@ def roofline(idx, sets, args, score_ms_avg):
     alg = sum(score_algorithmic_bytes(c, p) for c, _, p in chosen) / len(chosen)
     achieved = alg / (score_ms_avg / 1e3) / 1e9
     peak, kind = peaks()
+    # the workload-5 summary gives the whole workload's traffic; a cut has none
+    traffic = profiled_traffic(idx) if idx != 5 or args.long_requests >= 8 else None
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(idx), "kernel": "stream_kernel",
+            "frac": achieved / peak, "traffic": traffic, "kernel": "stream_kernel",
             "peak_source": kind, "kernel_ms": score_ms_avg, "algorithmic_bytes": alg}
 
 
@@ -357,7 +365,8 @@ def run_ours(args):
     base_seed = idx - 1
     sets = []
     for s in range(nsets):
-        case = synth.config(idx, seed=base_seed + 1000 * s + 100 * rank)
+        case = synth.config(idx, seed=base_seed + 1000 * s + 100 * rank,
+                            long_requests=args.long_requests)
         kw = synth.upload(case, "cuda")
         call = qli.Call(**kw)
         sets.append((case, call, pairs_of(case)))
@@ -410,9 +419,9 @@ def run_ours(args):
     flush = None
     if nsets * kbytes <= L2_BYTES:
         # the input sets fit in L2 together: every step is timed on its own
-        # (events around it) after a 256 MB write that evicts the previous
+        # (events around it) after a 256 MB read that evicts the previous
         # steps' data, outside the events
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        flush = torch.ones(256 << 20, dtype=torch.uint8, device="cuda")
         step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
 
@@ -420,7 +429,7 @@ def run_ours(args):
         barrier(world)
         if flush is not None:
             for k in range(args.steps):
-                flush.fill_(k & 255)
+                flush.max()              # a read: evicts L2 and leaves no dirty lines behind
                 step_ev[k][0].record(stream)
                 whole[(args.warmup + k) % nsets].replay()
                 step_ev[k][1].record(stream)
@@ -486,14 +495,17 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {
-            "workload": synth.CONFIG_NAMES[idx], "global_batch": case0.B * world,
+            "workload": synth.CONFIG_NAMES[idx] + (
+                "" if idx != 5 or args.long_requests >= 8
+                else " (cut: %d of the 8 1M-context requests)" % args.long_requests),
+            "global_batch": case0.B * world,
             "query_tokens": case0.T, "heads": case0.N, "ratio": case0.ratio,
             "topk": case0.topk, "cand_mode": case0.cand_mode,
             "pairs_per_step": my_pairs / args.steps,
             "l2": ("inputs larger than L2: the steps rotate over %d independent input sets, "
                    "%.1f MB of index K (rows and scales) each, %.0f MB in all (L2 129 MB)"
                    % (nsets, kbytes / 1e6, nsets * kbytes / 1e6)) if flush is None else
-                  ("L2 flushed between steps: a 256 MB write before each step, outside the "
+                  ("L2 flushed between steps: a 256 MB read before each step, outside the "
                    "events that time the step (%.2f MB of index K per step)" % (kbytes / 1e6)),
             "parallelism": "replicas" if world > 1 else "single",
             "launch": "one CUDA graph per input set holding the whole call",
@@ -789,8 +801,9 @@ def run_attn(args):
                              page_stride=case.page_stride, scale=ATTN_SCALE, out=out, lse=lse,
                              err_word=err)
     # one step reads 134 MB of KV rows, about the size of L2: every step is
-    # timed on its own after a 256 MB write that evicts the previous one
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # timed on its own after a 256 MB read that evicts the previous one (a
+    # read leaves no dirty lines whose write-back the step would pay for)
+    flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize()
@@ -804,7 +817,7 @@ def run_attn(args):
     def region():
         barrier(world)
         for k in range(args.steps):
-            flush.fill_(k & 255)
+            flush.max()
             evs[k][0].record(stream)
             g.replay()
             evs[k][1].record(stream)
@@ -877,7 +890,7 @@ def run_attn(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": synth.ATTN_WORKLOAD, "query_tokens": T, "heads": H,
                    "listed_per_token": case.attn_indices.shape[-1],
-                   "l2": "a 256 MB write before each step, outside the events that time it",
+                   "l2": "a 256 MB read before each step, outside the events that time it",
                    "timing": "median of %d repeats of the %d-step region" % (len(times), args.steps),
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
@@ -899,6 +912,9 @@ def main():
                     help="index: the indexer (default); the others time the query quantiser, "
                          "the index-K cache writer or the attention over the indices alone")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = default)")
+    ap.add_argument("--long-requests", type=int, default=8,
+                    help="workload 5 only: 1M-context requests kept (8 = the workload; fewer "
+                         "for profiler captures that must stay small)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-rows", type=int, default=4)

@@ -390,8 +390,11 @@ CONFIG_NAMES = {
 }
 
 
-def config(idx: int, seed: Optional[int] = None) -> Case:
-    """The five workloads the indexer is measured on (seeds 0..4 by default)."""
+def config(idx: int, seed: Optional[int] = None, long_requests: int = 8) -> Case:
+    """The five workloads the indexer is measured on (seeds 0..4 by default).
+    long_requests (workload 5 only) cuts the number of 1M-context requests
+    (8 in the workload) for captures that must stay small; the four short
+    requests stay."""
     s = idx - 1 if seed is None else int(seed)
     if idx == 1:
         return make_case(s, [2048], [1], N=64, ratio=2, topk=512, cand_mode="none",
@@ -411,7 +414,10 @@ def config(idx: int, seed: Optional[int] = None) -> Case:
         raw = []
         for b in range(12):
             raw.append(4096 if b % 3 == 2 else 1 << 20)
-        return make_case(s, raw, [1] * 12, N=64, ratio=2, topk=2048, cand_mode="source",
+        if long_requests < 8:
+            keep_long = [i for i, r in enumerate(raw) if r == 1 << 20][:long_requests]
+            raw = [r for i, r in enumerate(raw) if r != 1 << 20 or i in keep_long]
+        return make_case(s, raw, [1] * len(raw), N=64, ratio=2, topk=2048, cand_mode="source",
                          cand_blocks=2048, name=CONFIG_NAMES[5])
     raise ValueError(idx)
 

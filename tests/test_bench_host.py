@@ -60,9 +60,10 @@ def test_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic(2) is None
 
 
-@pytest.mark.parametrize("idx", [2, 3])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, "attn"])
 def test_committed_summaries_name_their_source_and_traffic(idx):
     import bench
-    name, _, key = bench.PROFILES[idx]
+    name, src, key = bench.PROFILES[idx]
     txt = open(os.path.join(ROOT, "profiles", name)).read()
     assert key + ":" in txt and "traffic_bytes_per_launch:" in txt
+    assert "--clock-control none" in txt and os.path.exists(src)

@@ -305,3 +305,30 @@ def test_parity_workloads_full_size(idx):
     else:
         rows = None
     check(case, rows=rows)
+
+
+def test_prefill_rows_with_heavy_ties_take_the_general_selection():
+    """Prefill-shaped calls (many tokens per request): rows whose scores take
+    a few distinct values put more entries at the threshold than the
+    many-rows-per-SM selection keeps, so they are listed for the general
+    selection; rows of equal scores do too. Both give the oracle's rows
+    (equal scores rank by lower position)."""
+    case = synth.make_case(84, [24000, 9000], [6, 3], N=64, ratio=2, topk=1500,
+                           cand_mode="source", cand_blocks=512, name="prefill-ties")
+    rng = np.random.default_rng(7)
+    base = rng.integers(-127, 128, size=(6, 128), dtype=np.int8)
+    case.k_rows[:] = base[rng.integers(0, 6, size=case.k_rows.shape[0])]
+    case.k_scale[:] = np.float16(0.01).view(np.uint16)
+    assert case.T > 2 * case.B                      # the prefill (group) path
+    check(case)
+    case.k_rows[:] = 5
+    check(case)
+
+
+def test_prefill_rows_longer_than_the_candidate_space_sample_a_threshold():
+    """Prefill rows of 5K-12K positions (more than the 4608 candidates one
+    CTA keeps): a sampled provisional threshold, one pass, exact select."""
+    case = synth.make_case(85, [24000, 10000, 9500], [5, 3, 4], N=64, ratio=2, topk=2048,
+                           cand_mode="source", cand_blocks=1024, name="prefill-sampled")
+    assert case.T > 2 * case.B
+    check(case)
