@@ -5,6 +5,10 @@ definitions (the GPU parity tests check the kernels themselves):
 - keep test: order_key(x) >= t_lo is one unsigned compare on the raw FP32
   bits, (u - lo) <= span, for every threshold that can occur (the start of
   any of the 4096 top-12-bit bins);
+- float keep test (prefill selection): for the same thresholds and every
+  finite score x, order_key(x) >= t_lo exactly when x >= key_floor(t_lo) as
+  an IEEE compare (so -0 and +0 agree), key_floor giving -inf below the key
+  of -FLT_MAX;
 - unit search: a warp probing 32 tile prefixes per round trip finds the same
   (token, tile) as a scalar binary search;
 - look-ahead: 32 consecutive tiles' tokens found from one load of the next
@@ -46,6 +50,30 @@ def test_keep_range_equals_the_key_compare():
         lo, span = keep_range(t_lo)
         fast = ((u - np.uint64(lo)) & np.uint64(M32)) <= np.uint64(span)
         assert np.array_equal(fast, k >= np.uint64(t_lo)), b
+
+
+def key_floor(key):
+    """The smallest score of key >= `key` on a bin boundary: the inverse of
+    order_key, -inf below the key of -FLT_MAX."""
+    if key < 0x00800000:
+        return np.float32(-np.inf)
+    bits = (key & 0x7FFFFFFF) if key & 0x80000000 else (~key) & M32
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+def test_float_compare_equals_the_key_compare():
+    rng = np.random.default_rng(1)
+    u = np.concatenate([rng.integers(0, 1 << 32, 200000, dtype=np.uint64),
+                        np.array([0, 0x80000000, 0x7F7FFFFF, 0xFF7FFFFF, 1, 0x80000001,
+                                  0x00800000, 0x80800000, 0x7F800000, 0xFF800000], dtype=np.uint64)])
+    x = u.astype(np.uint32).view(np.float32)
+    finite = ~np.isnan(x)
+    u, x = u[finite], x[finite]
+    k = order_key(u)
+    for b in range(4096):
+        t_lo = b << 20
+        f_p = key_floor(t_lo)      # NaN above the key of +inf: nothing passes
+        assert np.array_equal(x >= f_p, k >= np.uint64(t_lo)), b
 
 
 def scalar_search(us, T, u):
