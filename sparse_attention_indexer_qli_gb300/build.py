@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "-I", INCLUDE, "-I", CSRC]
 UNITS = ["qli_api.cpp", "qli_plan.cu", "qli_score.cu", "qli_prefill.cu", "qli_select.cu",
-         "qli_static.cu", "qli_quant.cu", "qli_attn.cu"]
+         "qli_static.cu", "qli_quant.cu", "qli_attn.cu", "qli_small.cu"]
 HEADERS = ["qli_internal.h", "qli_ptx.cuh"]
 
 

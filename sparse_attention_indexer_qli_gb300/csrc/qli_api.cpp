@@ -126,6 +126,7 @@ WsLayout workspace_layout(const qli_args& a) {
   const int64_t T = a.T, B = a.B, C = a.cand_blocks;
   const int64_t cap = static_cast<int64_t>(a.bt_stride) * a.rows_per_page;
   L.stream_path = use_stream_path(a) ? 1 : 0;
+  L.small = use_small_path(a) ? 1 : 0;
   L.G = L.stream_path ? 1 : kMaxMmaN / (a.N > 0 ? a.N : 64);
   L.Gmax = L.stream_path ? 0 : static_cast<int32_t>((T + L.G - 1) / L.G + B);
   if (a.cand_mode == QLI_CAND_CONSUMER) {
@@ -140,7 +141,9 @@ WsLayout workspace_layout(const qli_args& a) {
     off = round_up(off + bytes, kAlign);
     return at;
   };
-  L.err = take(16);
+  // err, counter, 8 spare bytes, then (single-launch path) one counter per token
+  L.err_bytes = 16 + (L.small ? 4 * static_cast<size_t>(T) : 0);
+  L.err = take(L.err_bytes);
   L.counter = L.err + 4;
   L.tok_V = take(4 * T);
   L.tok_b = take(4 * T);
@@ -170,7 +173,7 @@ WsLayout workspace_layout(const qli_args& a) {
   L.long_bytes = L.lchunks ? (off - L.lext) : 0;          // zeroed before the passes
   L.lkey = take(L.lchunks ? 4 * rows2 * L.lchunks * kLongChunkCap : 0);
   L.lid = take(L.lchunks ? 4 * rows2 * L.lchunks * kLongChunkCap : 0);
-  L.fhist = take(L.stream_path ? 4 * 4096 * rows2 : 0);
+  L.fhist = take(L.stream_path && !L.small ? 4 * 4096 * rows2 : 0);
   L.flist = take(L.stream_path ? 0 : 4 * rows2);
   L.scores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Lrow));
   L.bscores = take(4 * static_cast<size_t>(T) * static_cast<size_t>(L.Brow));
@@ -227,7 +230,9 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.lkey = reinterpret_cast<uint32_t*>(w + L.lkey);
   d.lid = reinterpret_cast<int32_t*>(w + L.lid);
   d.lchunks = L.lchunks;
-  d.fhist = L.stream_path ? reinterpret_cast<uint32_t*>(w + L.fhist) : nullptr;
+  d.fhist = L.stream_path && !L.small ? reinterpret_cast<uint32_t*>(w + L.fhist) : nullptr;
+  d.small = L.small;
+  d.done = reinterpret_cast<uint32_t*>(w + L.err + 16);
   d.flist = reinterpret_cast<int32_t*>(w + L.flist);
   d.long_zero_bytes = L.long_bytes;
   d.kf16 = reinterpret_cast<__half*>(w + L.kf16);
@@ -263,6 +268,13 @@ qli_status run_stages(const qli_args* a, void* ws, size_t bytes, int32_t stage, 
   if (st != QLI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
+  if (d.small) {
+    // planning zeroes the error word and the per-token counters; the score
+    // stage's kernel also selects, so the select stage queues nothing
+    if (stage == 0 || stage == QLI_STAGE_PLAN) e = launch_small_zero(d, L.err_bytes, s);
+    if (e == cudaSuccess && (stage == 0 || stage == QLI_STAGE_SCORE)) e = launch_small(d, s);
+    return e == cudaSuccess ? QLI_OK : QLI_ERR_CUDA;
+  }
   if (stage == 0 || stage == QLI_STAGE_PLAN) e = launch_plan(d, s);
   if (e == cudaSuccess && (stage == 0 || stage == QLI_STAGE_SCORE)) e = launch_score(d, s);
   if (e == cudaSuccess && (stage == 0 || stage == QLI_STAGE_SELECT)) e = launch_select(d, s);
@@ -302,9 +314,13 @@ qli_status qli_launch_count(const qli_args* a, int32_t stage, int32_t* launches)
   const qli::WsLayout L = qli::workspace_layout(*a);
   const qli::DevArgs d = qli::make_dev_args(*a, nullptr, L);
   int n = 0;
-  if (stage == 0 || stage == QLI_STAGE_PLAN) n += a->T > 0 ? qli::plan_launches(d) : 0;
-  if (stage == 0 || stage == QLI_STAGE_SCORE) n += qli::score_launches(d);
-  if (stage == 0 || stage == QLI_STAGE_SELECT) n += qli::select_launches(d);
+  if (d.small) {
+    n = (stage == 0 || stage == QLI_STAGE_PLAN ? 1 : 0) + (stage == 0 || stage == QLI_STAGE_SCORE ? 1 : 0);
+  } else {
+    if (stage == 0 || stage == QLI_STAGE_PLAN) n += a->T > 0 ? qli::plan_launches(d) : 0;
+    if (stage == 0 || stage == QLI_STAGE_SCORE) n += qli::score_launches(d);
+    if (stage == 0 || stage == QLI_STAGE_SELECT) n += qli::select_launches(d);
+  }
   *launches = n;
   return QLI_OK;
 }

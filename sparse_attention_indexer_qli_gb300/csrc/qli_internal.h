@@ -26,6 +26,8 @@ constexpr int kSmemKeys = 44 * 1024;    // keys one selection CTA holds in share
 constexpr int kLongChunk = 32768;       // row entries per CTA in the long-row passes
 constexpr int kLongChunkCap = 4096;     // candidates kept per chunk
 constexpr int kLongCandCap = 16384;     // candidates kept per long row
+constexpr int kSmallMaxT = 64;          // single-launch path: tokens,
+constexpr int kSmallMaxPositions = 4096;   // and positions a request can hold
 
 // Everything a kernel needs, passed by value (a few hundred bytes).
 struct DevArgs {
@@ -90,6 +92,8 @@ struct DevArgs {
   int64_t cap;         // bt_stride * R: most positions a request can hold
   int32_t stream_path; // 1: one token per tile, persistent streaming kernel
   int32_t num_sms;     // SMs of the device (persistent grids)
+  int32_t small;       // 1: the single-launch path (planning, scoring, selection in one kernel)
+  uint32_t* done;      // single-launch path: [T] CTAs of the token done (zeroed with err)
 };
 
 struct WsLayout {
@@ -102,11 +106,21 @@ struct WsLayout {
   int64_t Lrow, Brow;
   int32_t Gmax, G;
   int32_t stream_path;
+  int32_t small;
+  size_t err_bytes;    // err, counter and (single-launch path) the per-token counters
 };
 
 // The streaming (decode) kernel takes one token per tile; the group kernel
 // shares a tile between up to 256/N tokens of one request (prefill).
 bool use_stream_path(const qli_args& a);
+
+// Small decode batches (INT8, none/source, at most kSmallMaxT tokens and 64
+// requests, at most kSmallMaxPositions positions per request) run planning,
+// scoring and selection in one kernel, after a one-CTA kernel that zeroes the
+// first `bytes` of the workspace (the error word and the per-token counters).
+bool use_small_path(const qli_args& a);
+cudaError_t launch_small_zero(const DevArgs& d, size_t bytes, cudaStream_t s);
+cudaError_t launch_small(const DevArgs& d, cudaStream_t s);
 
 // Raises `func`'s dynamic shared-memory limit to `bytes` once per device
 // (`done` holds one bit per device ordinal below 64; others always set it).

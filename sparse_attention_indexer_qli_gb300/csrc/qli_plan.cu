@@ -12,19 +12,11 @@
 #include <climits>
 
 #include "qli_internal.h"
+#include "qli_meta.cuh"
 #include "qli_ptx.cuh"
 
 namespace qli {
 namespace {
-
-__device__ __forceinline__ int32_t visible_count(int32_t lk, int32_t res, int32_t ratio,
-                                                 int32_t q_len, int32_t i) {
-  const int64_t S = static_cast<int64_t>(lk) * ratio + res;
-  const int64_t seen = S - q_len + i + 1;   // raw tokens at or before the query
-  if (seen <= 0) return 0;
-  const int64_t v = seen / ratio;
-  return static_cast<int32_t>(v < lk ? v : lk);
-}
 
 // Exclusive prefix sum of f(0..n-1) into out[0..n], by one CTA of NT threads.
 template <int NT, class F>
@@ -101,21 +93,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   // compressed length into [0, cap] and the residual into [0, ratio)
   uint32_t e = 0u;
   for (int b = tid; b < a.B; b += blockDim.x) {
-    const int32_t c0 = a.cu[b], c1 = a.cu[b + 1];
-    int32_t lk = a.k_lens[b];
-    int32_t res = a.residual ? a.residual[b] : 0;
-    const int32_t q0 = min(max(c0, 0), a.T);
-    const int32_t q1 = min(max(c1, q0), a.T);
-    if (c0 != q0 || c1 != q1 || (b == 0 && c0 != 0) || (b == a.B - 1 && c1 != a.T))
-      e |= QLI_DEVERR_SEQLENS;
-    if (lk < 0 || lk > a.cap) {
-      e |= QLI_DEVERR_KLEN;
-      lk = lk < 0 ? 0 : static_cast<int32_t>(a.cap);
-    }
-    if (res < 0 || res >= a.ratio) {
-      e |= QLI_DEVERR_RESIDUAL;
-      res = 0;
-    }
+    int32_t q0, q1, lk, res;
+    e |= sanitize_request(a, b, q0, q1, lk, res);
     a.req_q0[b] = q0;
     a.req_q1[b] = q1;
     a.req_lk[b] = lk;
@@ -147,16 +126,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
   // sanitised starts never decrease for valid metadata; a token no request
   // covers keeps V = 0 and request -1)
   for (int t = tid; t < a.T; t += blockDim.x) {
-    int32_t lo = 0, hi = a.B - 1;
-    while (lo < hi) {
-      const int32_t mid = (lo + hi + 1) >> 1;
-      if (q0s[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    int32_t V = 0, owner = -1;
-    if (a.B > 0 && q0s[lo] <= t && t < q1s[lo]) {
-      owner = lo;
-      V = visible_count(lks[lo], ress[lo], a.ratio, q1s[lo] - q0s[lo], t - q0s[lo]);
-    }
+    int32_t owner;
+    const int32_t V = token_owner(a, q0s, q1s, lks, ress, t, owner);
     a.tok_V[t] = V;
     a.tok_b[t] = owner;
     if (tok_small) s_tiles[t] = (V + kTile - 1) / kTile;

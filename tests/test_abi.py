@@ -191,7 +191,16 @@ def test_workspace_size_and_launch_counts(L):
     # at least the FP32 score rows: T * bt_stride * rows_per_page * 4 bytes
     assert n.value >= 4 * 8 * 64 * 4
     cnt = ctypes.c_int32(0)
+    # a small decode batch: two kernels (the plan stage zeroes counters, the
+    # score stage's kernel also selects)
     assert L.qli_launch_count(ctypes.byref(a), 0, ctypes.byref(cnt)) == 0
+    assert cnt.value == 2
+    for stage, want in ((1, 1), (2, 1), (3, 0)):
+        assert L.qli_launch_count(ctypes.byref(a), stage, ctypes.byref(cnt)) == 0
+        assert cnt.value == want
+    # more tokens than two per request: the staged path, three stages or more
+    big = good_args("source", T=5, B=2)
+    assert L.qli_launch_count(ctypes.byref(big), 0, ctypes.byref(cnt)) == 0
     assert cnt.value >= 3
     off, stride = ctypes.c_size_t(0), ctypes.c_int64(0)
     assert L.qli_scores_layout(ctypes.byref(a), ctypes.byref(off), ctypes.byref(stride)) == 0

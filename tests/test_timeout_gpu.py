@@ -38,8 +38,11 @@ def stall_lib():
 
 def test_a_wait_that_runs_out_reports_and_leaves_the_context_usable(stall_lib):
     import torch
-    case = synth.make_case(91, [3000, 1200, 777], [1, 1, 1], N=64, ratio=2, topk=128,
+    # one context past 4096 compressed positions, so that the call takes the
+    # streaming kernel (not the single-launch path for small batches)
+    case = synth.make_case(91, [9000, 1200, 777], [1, 1, 1], N=64, ratio=2, topk=128,
                            name="stall")
+    assert case.bt_stride * case.rows_per_page > 4096
     call = qli.Call(**synth.upload(case, "cuda"))
     ws = call.alloc_workspace()
     stream = torch.cuda.current_stream().cuda_stream
