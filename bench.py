@@ -40,9 +40,11 @@ ROTATE_SETS = {1: 1, 2: 3, 3: 16, 4: 8, 5: 1}
 SCORE_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_score.cu")
 PREFILL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_prefill.cu")
 ATTN_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_attn.cu")
+SMALL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_small.cu")
 # workload -> (committed ncu summary, the kernel source it was taken on)
 PROFILES = {
-    1: ("stream_kernel_decode_b1_ratio2.md", SCORE_SRC, "stream_source_sha256"),
+    # one token: the single-launch path (its kernel also selects)
+    1: ("small_kernel_decode_b1_ratio2.md", SMALL_SRC, "small_source_sha256"),
     2: ("stream_kernel_decode_b64_ratio1.md", SCORE_SRC, "stream_source_sha256"),
     3: ("prefill_kernel_prefill_t4096_2x2048.md", PREFILL_SRC, "prefill_source_sha256"),
     4: ("stream_kernel_consumer_b32_ratio2.md", SCORE_SRC, "stream_source_sha256"),
@@ -183,8 +185,11 @@ def roofline(idx, sets, args, score_ms_avg):
     peak, kind = peaks()
     # the workload-5 summary gives the whole workload's traffic; a cut has none
     traffic = profiled_traffic(idx) if idx != 5 or args.long_requests >= 8 else None
+    # a small batch runs the single-launch kernel, whose score stage also selects
+    small = sets[0][1].launches(3) == 0
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": traffic, "kernel": "stream_kernel",
+            "frac": achieved / peak, "traffic": traffic,
+            "kernel": "small_kernel" if small else "stream_kernel",
             "peak_source": kind, "kernel_ms": score_ms_avg, "algorithmic_bytes": alg}
 
 

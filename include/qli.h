@@ -144,7 +144,11 @@ qli_status qli_workspace_size(const qli_args *a, size_t *bytes);
 qli_status qli_run(const qli_args *a, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Queues one stage (QLI_STAGE_*) of qli_run, for timing. Running PLAN, SCORE
- * and SELECT in that order on one stream equals qli_run. */
+ * and SELECT in that order on one stream equals qli_run. Small decode batches
+ * (INT8, none or source mode, T <= 64, B <= 64, bt_stride*rows_per_page <=
+ * 4096) run planning, scoring and selection in the SCORE stage's one kernel:
+ * their PLAN stage only zeroes the error word and per-token counters, and
+ * their SELECT stage queues nothing. */
 qli_status qli_run_stage(const qli_args *a, void *workspace, size_t workspace_bytes,
                          int32_t stage, void *stream);
 
