@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         const int s = k % kStages;
         const uint32_t ph = (k / kStages) & 1;
         if (lane == 0) {
-          ok = mbar_wait_bounded(&S.empty[s], ph ^ 1);
+          ok = mbar_wait_bounded<true>(&S.empty[s], ph ^ 1);
           if (ok) {
             mbar_arrive_expect_tx(&S.full[s], kABytes);
             const int32_t y = x.b * static_cast<int32_t>(a.kstride) + (x.tile0 + i) * kTile;
@@ -185,11 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         const Unit x = unit_at(a, u);
         const uint32_t nmma = static_cast<uint32_t>(x.cnt * a.N);
         const uint32_t idesc = idesc_f16_m128(nmma);
-        if (!mbar_wait_bounded(&S.bfull, n & 1)) { ok = false; break; }
+        if (!mbar_wait_bounded<true>(&S.bfull, n & 1)) { ok = false; break; }
         for (int i = 0; i < x.ntiles; ++i, ++k) {
           const int s = k % kStages, ds = k & 1;
-          if (!mbar_wait_bounded(&S.full[s], (k / kStages) & 1) ||
-              !mbar_wait_bounded(&S.dempty[ds], ((k >> 1) & 1) ^ 1)) { ok = false; break; }
+          if (!mbar_wait_bounded<true>(&S.full[s], (k / kStages) & 1) ||
+              !mbar_wait_bounded<true>(&S.dempty[ds], ((k >> 1) & 1) ^ 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(&S.a[s][0]);
           const uint32_t d = tmem + ds * 256;
@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       // before overwriting the queries and this parity's weights: every
       // epilogue warp has loaded the previous unit's last tile (so it is done
       // with the unit before that), and the previous unit's MMAs are complete
-      if (k > 0 && !mbar_wait_warp(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
-      if (!mbar_wait_warp(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
+      if (k > 0 && !mbar_wait_warp<true>(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait_warp<true>(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
       const int nrows = x.cnt * a.N;
       {
         // every load first, then the conversions (one global latency, not eight)
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.bfull);
       // every warp's staging is complete (and visible) once bfull flips
-      if (!mbar_wait_warp(&S.bfull, n & 1)) { ok = false; break; }
+      if (!mbar_wait_warp<true>(&S.bfull, n & 1)) { ok = false; break; }
 
       // the (up to two) tokens this warp sums, and the TMEM columns of each
       // 32-column half it loads
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       };
       for (int i = 0; i < x.ntiles; ++i, ++k) {
         const int ds = k & 1;
-        if (!mbar_wait_warp(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait_warp<true>(&S.dfull[ds], (k >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const int32_t pos = (x.tile0 + i) * kTile + row;
         const float ks = ksrow[pos];
