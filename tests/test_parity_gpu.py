@@ -332,3 +332,25 @@ def test_prefill_rows_longer_than_the_candidate_space_sample_a_threshold():
                            cand_mode="source", cand_blocks=1024, name="prefill-sampled")
     assert case.T > 2 * case.B
     check(case)
+
+
+def test_prefill_rows_between_32k_and_the_shared_memory_limit():
+    """Prefill rows of 32K-45K positions: the many-rows-per-SM selection
+    still takes them (position bitmaps of up to 1408 words, 16-bit
+    positions); the candidate rows are longer than C."""
+    case = synth.make_case(86, [90000, 70000], [3, 2], N=32, ratio=2, topk=2048,
+                           cand_mode="source", cand_blocks=2048, name="prefill-44k")
+    assert case.T > 2 * case.B
+    assert 32768 < int(case.k_lens.max()) <= 44 * 1024
+    check(case)
+
+
+def test_prefill_rows_past_the_shared_memory_limit_take_the_long_row_passes():
+    """Prefill rows longer than one CTA's shared memory (45056 keys) are
+    listed by the many-rows-per-SM selection and ranked by the chunked
+    long-row passes and the general selection."""
+    case = synth.make_case(87, [120000, 3000], [3, 2], N=64, ratio=2, topk=2048,
+                           cand_mode="source", cand_blocks=1024, name="prefill-long")
+    assert case.T > 2 * case.B
+    assert int(case.k_lens.max()) > 44 * 1024
+    check(case)
