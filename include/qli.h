@@ -239,17 +239,38 @@ qli_status qli_write_index_k(const uint16_t *k, int64_t n, const int64_t *slot_m
                              int32_t rows_per_page, int64_t k_offset, int64_t scale_offset,
                              uint32_t *err_word, void *stream);
 
-/* Self-check of the quantisers' divisions, which compute x / s and amax / 127
- * from the row's reciprocal with one correction step instead of an IEEE
- * divide (Markstein, IBM J. Res. Dev. 34(1), 1990). Both operands come from
- * finite sets (x a BF16 value, s a positive finite FP16 scale), so one
- * kernel on `stream` tries every pair a row can produce: all s with
- * |x| <= 256 s (a row's amax / s stays below 192 unless s is the 65504 cap)
- * and every finite x for s = 65504. It leaves in the device array counts[2]
- * (8-byte aligned; zeroed by the call): counts[0] = pairs
- * whose code clamp(rint(x / s), -127, 127) differs from the one an IEEE FP32
- * division gives, plus the BF16 values amax >= 0 whose scale FP16(amax / 127)
- * (computed the same way) differs from the IEEE one, counts[1] = pairs with |x| >= 2^-100 whose FP32 quotient
+/* The FP8 variant of the two calls above (quant mode 1, which the guide's
+ * section 编译范围 names for the A5 build; the pages give no formula). The
+ * same per-row scheme with E4M3's largest finite value 448 in place of 127:
+ *     s   = FP16(amax / 448)   FP32 quotient, round to nearest even; capped
+ *                              at 65504
+ *     c_d = E4M3(x_d / s)      FP32 quotient, rounded to nearest even on the
+ *                              E4M3 grid ("fn" encoding: bias 7, no
+ *                              infinities), saturated to +-448
+ * A row whose s rounds to zero gets codes 0 and scale +0. Codes are E4M3 bit
+ * patterns in the bytes the INT8 calls would write, so qli_run with
+ * quant_mode = QLI_QUANT_FP8 reads them. Arguments, layouts, alignment and
+ * errors as for qli_quantize_q and qli_write_index_k. */
+qli_status qli_quantize_q_fp8(const uint16_t *x, int64_t rows, uint8_t *q_out,
+                              uint16_t *scale_out, void *stream);
+qli_status qli_write_index_k_fp8(const uint16_t *k, int64_t n, const int64_t *slot_mapping,
+                                 uint8_t *cache, int64_t num_pages, int64_t page_stride,
+                                 int32_t rows_per_page, int64_t k_offset, int64_t scale_offset,
+                                 uint32_t *err_word, void *stream);
+
+/* Self-check of the quantisers' divisions, which compute x / s, amax / 127
+ * and amax / 448 from the row's reciprocal with one correction step instead
+ * of an IEEE divide (Markstein, IBM J. Res. Dev. 34(1), 1990). Both operands
+ * come from finite sets (x a BF16 value, s a positive finite FP16 scale), so
+ * one kernel on `stream` tries every pair a row can produce: all s with
+ * |x| <= 768 s (a row's amax / s stays below 1.5 x 127 or 1.5 x 448 unless
+ * s is the 65504 cap) and every finite x for s = 65504; codes are compared
+ * for both the INT8 and the E4M3 encoding. It leaves in the device array
+ * counts[2] (8-byte aligned; zeroed by the call): counts[0] = pairs whose
+ * INT8 code clamp(rint(x / s), -127, 127) or E4M3 code differs from the one
+ * an IEEE FP32 division gives, plus the BF16 values amax >= 0 whose scale
+ * FP16(amax / 127) or FP16(amax / 448) (computed the same way) differs from
+ * the IEEE one; counts[1] = pairs with |x| >= 2^-100 whose FP32 quotient
  * differs from the IEEE one (below that the correction's residual can
  * underflow; those quotients round to code 0 either way). Asynchronous. */
 qli_status qli_check_quant_rounding(unsigned long long *counts, void *stream);

@@ -265,15 +265,16 @@ def f32_to_e4m3(x: float) -> int:
 
 
 def write_index_k(k_bf16: np.ndarray, slot: np.ndarray, pages: np.ndarray, rows_per_page: int,
-                  k_offset: int, scale_offset: int) -> int:
-    """Quantises the n rows of k_bf16 ([n, D] uint16 BF16 bits) and writes
-    them into `pages` ([num_pages, page_stride] uint8, modified in place) at
-    slot[i] = page * R + row. Returns the oracle's status (0, or -5 when a
-    slot lies past the pool; valid rows are written either way)."""
+                  k_offset: int, scale_offset: int, fp8: bool = False) -> int:
+    """Quantises the n rows of k_bf16 ([n, D] uint16 BF16 bits; INT8 codes, or
+    E4M3 codes when fp8) and writes them into `pages` ([num_pages,
+    page_stride] uint8, modified in place) at slot[i] = page * R + row.
+    Returns the oracle's status (0, or -5 when a slot lies past the pool;
+    valid rows are written either way)."""
     k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
     sl = np.ascontiguousarray(slot, dtype=np.int64)
     assert pages.flags.c_contiguous and pages.dtype == np.uint8 and pages.ndim == 2
-    f = _quant_fn("oracle_write_index_k", ctypes.c_int,
+    f = _quant_fn("oracle_write_index_k_e4m3" if fp8 else "oracle_write_index_k", ctypes.c_int,
                   [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                    ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                    ctypes.c_int64, ctypes.c_int64])

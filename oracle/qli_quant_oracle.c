@@ -182,11 +182,12 @@ int oracle_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int32_t D, uint8_
 }
 
 /* Index K: n new rows of D = 128 BF16 values, slot[i] = page * R + row.
- * Writes each row's codes and scale into the page pool `cache`. Returns 0,
- * or the first error (every valid row is still written). */
-int oracle_write_index_k(const uint16_t *k, int64_t n, int32_t D, const int64_t *slot,
-                         uint8_t *cache, int64_t num_pages, int64_t page_stride, int32_t R,
-                         int64_t k_offset, int64_t scale_offset) {
+ * Writes each row's codes (INT8, or E4M3 when fp8) and scale into the page
+ * pool `cache`. Returns 0, or the first error (every valid row is still
+ * written). */
+static int write_index_k_rows(const uint16_t *k, int64_t n, int32_t D, const int64_t *slot,
+                              uint8_t *cache, int64_t num_pages, int64_t page_stride, int32_t R,
+                              int64_t k_offset, int64_t scale_offset, int fp8) {
     if (n < 0 || D <= 0 || R <= 0 || num_pages < 0 || (n > 0 && (!k || !slot || !cache)))
         return QORACLE_EINVAL;
     int err = QORACLE_OK;
@@ -200,7 +201,8 @@ int oracle_write_index_k(const uint16_t *k, int64_t n, int32_t D, const int64_t 
             continue;
         }
         uint16_t s;
-        const int e = oracle_quant_row(k + i * D, D, codes, &s);
+        const int e = fp8 ? oracle_quant_row_e4m3(k + i * D, D, (uint8_t *)codes, &s)
+                          : oracle_quant_row(k + i * D, D, codes, &s);
         if (e) {
             if (!err) err = e;
             continue;
@@ -211,4 +213,19 @@ int oracle_write_index_k(const uint16_t *k, int64_t n, int32_t D, const int64_t 
         memcpy(p + scale_offset + row * 2, &s, 2);
     }
     return err;
+}
+
+int oracle_write_index_k(const uint16_t *k, int64_t n, int32_t D, const int64_t *slot,
+                         uint8_t *cache, int64_t num_pages, int64_t page_stride, int32_t R,
+                         int64_t k_offset, int64_t scale_offset) {
+    return write_index_k_rows(k, n, D, slot, cache, num_pages, page_stride, R, k_offset,
+                              scale_offset, 0);
+}
+
+/* The FP8 variant: E4M3 codes (oracle_quant_row_e4m3) in the same places. */
+int oracle_write_index_k_e4m3(const uint16_t *k, int64_t n, int32_t D, const int64_t *slot,
+                              uint8_t *cache, int64_t num_pages, int64_t page_stride, int32_t R,
+                              int64_t k_offset, int64_t scale_offset) {
+    return write_index_k_rows(k, n, D, slot, cache, num_pages, page_stride, R, k_offset,
+                              scale_offset, 1);
 }

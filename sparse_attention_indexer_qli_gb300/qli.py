@@ -72,7 +72,8 @@ class AttnArgs(ctypes.Structure):
 EXPORTS = ["qli_validate", "qli_workspace_size", "qli_run", "qli_run_stage", "qli_launch_count",
            "qli_scores_layout", "qli_read_device_error", "qli_status_string", "qli_abi_version",
            "qli_args_size", "qli_run_static", "qli_read_static_device_error",
-           "qli_quantize_q", "qli_write_index_k", "qli_check_quant_rounding",
+           "qli_quantize_q", "qli_write_index_k", "qli_quantize_q_fp8", "qli_write_index_k_fp8",
+           "qli_check_quant_rounding",
            "qli_sparse_attention", "qli_attn_args_size"]
 
 _lib = None
@@ -105,11 +106,13 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.qli_status_string.restype = ctypes.c_char_p
     L.qli_abi_version.restype = c_int32
     L.qli_args_size.restype = c_int64
-    L.qli_quantize_q.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p]
-    L.qli_quantize_q.restype = c_int32
-    L.qli_write_index_k.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_int64,
+    for name in ("qli_quantize_q", "qli_quantize_q_fp8"):
+        getattr(L, name).argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p]
+        getattr(L, name).restype = c_int32
+    for name in ("qli_write_index_k", "qli_write_index_k_fp8"):
+        getattr(L, name).argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_int64,
                                     c_int32, c_int64, c_int64, c_void_p, c_void_p]
-    L.qli_write_index_k.restype = c_int32
+        getattr(L, name).restype = c_int32
     L.qli_check_quant_rounding.argtypes = [c_void_p, c_void_p]
     L.qli_check_quant_rounding.restype = c_int32
     L.qli_sparse_attention.argtypes = [ctypes.POINTER(AttnArgs), c_void_p]
@@ -273,10 +276,11 @@ def run(*args, workspace=None, stream=None, **kw):
     return c.run(ws, stream)
 
 
-def quantize_q(x, q_out=None, scale_out=None, stream=None):
-    """qli_quantize_q: BF16 rows x [..., 128] (torch.bfloat16 or int16/uint16
-    bit patterns, CUDA, contiguous) -> (codes int8 [..., 128], FP16 scale bits
-    int16 [...]). For the indexer's queries x is [T, N, 128]."""
+def quantize_q(x, q_out=None, scale_out=None, stream=None, quant_mode=QUANT_INT8):
+    """qli_quantize_q (or, with quant_mode=QUANT_FP8, qli_quantize_q_fp8): BF16
+    rows x [..., 128] (torch.bfloat16 or int16/uint16 bit patterns, CUDA,
+    contiguous) -> (codes int8 [..., 128] (E4M3 bit patterns for FP8), FP16
+    scale bits int16 [...]). For the indexer's queries x is [T, N, 128]."""
     import torch
     if not isinstance(x, torch.Tensor) or not x.is_cuda or not x.is_contiguous():
         raise TypeError("x must be a contiguous CUDA tensor")
@@ -288,8 +292,9 @@ def quantize_q(x, q_out=None, scale_out=None, stream=None):
     if scale_out is None:
         scale_out = torch.empty(x.shape[:-1], dtype=torch.int16, device=x.device)
     _require_cuda("q_out", q_out, torch.int8)
-    _check(lib().qli_quantize_q(_ptr(x), rows, _ptr(q_out), _ptr(scale_out), _stream(stream)),
-           "qli_quantize_q")
+    name = "qli_quantize_q_fp8" if quant_mode == QUANT_FP8 else "qli_quantize_q"
+    _check(getattr(lib(), name)(_ptr(x), rows, _ptr(q_out), _ptr(scale_out), _stream(stream)),
+           name)
     return q_out, scale_out
 
 
@@ -305,10 +310,12 @@ def check_quant_rounding(stream=None):
 
 
 def write_index_k(k, slot_mapping, cache, *, rows_per_page: int, page_stride: int,
-                  k_offset: int, scale_offset: int, err_word=None, stream=None):
-    """qli_write_index_k: quantises the rows of k [n, 128] (BF16 patterns,
-    CUDA, contiguous) and writes them into the page pool `cache` (uint8, CUDA)
-    at slot_mapping [n] (int64: page * rows_per_page + row; negative = skip)."""
+                  k_offset: int, scale_offset: int, err_word=None, stream=None,
+                  quant_mode=QUANT_INT8):
+    """qli_write_index_k (or, with quant_mode=QUANT_FP8, qli_write_index_k_fp8):
+    quantises the rows of k [n, 128] (BF16 patterns, CUDA, contiguous) and
+    writes them into the page pool `cache` (uint8, CUDA) at slot_mapping [n]
+    (int64: page * rows_per_page + row; negative = skip)."""
     import torch
     _require_cuda("slot_mapping", slot_mapping, torch.int64)
     _require_cuda("cache", cache, torch.uint8)
@@ -319,9 +326,10 @@ def write_index_k(k, slot_mapping, cache, *, rows_per_page: int, page_stride: in
     if slot_mapping.numel() != k.shape[0]:
         raise ValueError("one slot per row")
     num_pages = cache.numel() // page_stride
-    _check(lib().qli_write_index_k(_ptr(k), k.shape[0], _ptr(slot_mapping), _ptr(cache),
-                                   num_pages, page_stride, rows_per_page, k_offset, scale_offset,
-                                   _ptr(err_word), _stream(stream)), "qli_write_index_k")
+    name = "qli_write_index_k_fp8" if quant_mode == QUANT_FP8 else "qli_write_index_k"
+    _check(getattr(lib(), name)(_ptr(k), k.shape[0], _ptr(slot_mapping), _ptr(cache), num_pages,
+                                page_stride, rows_per_page, k_offset, scale_offset,
+                                _ptr(err_word), _stream(stream)), name)
 
 
 def sparse_attention(q, cu_seqlens_q, cache, block_table, indices, *, rows_per_page: int,

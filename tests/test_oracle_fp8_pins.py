@@ -190,3 +190,37 @@ def test_quantiser_degenerate_rows():
     assert sc[0] == 0x7BFF and np.all(c[0, ::2] == 0x7E) and np.all(c[0, 1::2] == 0xFE)
     with pytest.raises(oracle.OracleError):
         oracle.quantize_rows_e4m3(np.full((1, 128), 0x7F80, np.uint16))
+
+
+@pytest.mark.parametrize("ratio", [1, 2])
+def test_fp8_writer_places_rows_where_the_indexer_reads_them(ratio):
+    # the E4M3 writer fills the same bytes the indexer's page packing puts
+    # the E4M3 codes and scales in (synth's packing, not the writer's code)
+    case = synth.make_case(70 + ratio, [700, 130, 1], [1, 1, 1], N=32, ratio=ratio, topk=16)
+    n = int(case.k_lens.sum())
+    kb = synth.bf16_rows(70 + ratio, (n, 128), sigma=2.0)
+    codes, scales = oracle.quantize_rows_e4m3(kb)
+    case.k_rows = codes.view(np.int8)
+    case.k_scale = scales
+    slots = np.concatenate([synth.slots_of(case, b, np.arange(int(case.k_lens[b])))
+                            for b in range(case.B)])
+    want = case.pack_pages_numpy()
+    pages = want.copy()
+    R = case.rows_per_page
+    rng = np.random.default_rng(4)
+    for m in slots:                              # scribble over every target slot
+        p, r = divmod(int(m), R)
+        pages[p, case.k_offset + r * 128:case.k_offset + (r + 1) * 128] = rng.integers(0, 256, 128)
+        pages[p, case.scale_offset + 2 * r:case.scale_offset + 2 * r + 2] = rng.integers(0, 256, 2)
+    perm = rng.permutation(len(slots))
+    rc = oracle.write_index_k(kb[perm], slots[perm], pages, R, case.k_offset, case.scale_offset,
+                              fp8=True)
+    assert rc == 0
+    assert np.array_equal(pages, want)
+    # and the INT8 writer touches exactly the same bytes
+    other = want.copy()
+    oracle.write_index_k(kb, slots, other, R, case.k_offset, case.scale_offset)
+    int8_codes, int8_scales = oracle.quantize_rows(kb)
+    assert not np.array_equal(other, want)
+    case.k_rows, case.k_scale = int8_codes, int8_scales
+    assert np.array_equal(other, case.pack_pages_numpy())

@@ -157,3 +157,72 @@ def test_division_matches_ieee_on_every_bf16_value_and_fp16_scale():
     # division, exhaustively over every (x, scale) pair a row can produce
     counts = qli.check_quant_rounding()
     assert counts == (0, 0)
+
+
+# ---- FP8 (E4M3) variant ---------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 6, 257, 4099])
+def test_quantize_q_fp8_matches_oracle(n):
+    import torch
+    x = _mixed_rows(400 + n, n)
+    want_c, want_s = oracle.quantize_rows_e4m3(x)
+    c, s = qli.quantize_q(_to_dev(x), quant_mode=qli.QUANT_FP8)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.cpu().numpy().view(np.uint8), want_c)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), want_s)
+
+
+@pytest.mark.parametrize("ratio,raw_lens", [(1, [700, 130, 1]), (2, [5000, 64, 3, 0])])
+def test_write_index_k_fp8_matches_oracle(ratio, raw_lens):
+    import torch
+    case, kb, slots = _writer_setup(180 + ratio + len(raw_lens), ratio, raw_lens)
+    slots = slots.copy()
+    if len(slots) > 4:
+        slots[2] = -1                                       # padding row
+    pages = case.pack_pages_numpy()
+    want = pages.copy()
+    assert oracle.write_index_k(kb, slots, want, case.rows_per_page, case.k_offset,
+                                case.scale_offset, fp8=True) == 0
+    dev = torch.from_numpy(pages).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qli.write_index_k(_to_dev(kb), torch.from_numpy(slots).cuda(), dev,
+                      rows_per_page=case.rows_per_page, page_stride=case.page_stride,
+                      k_offset=case.k_offset, scale_offset=case.scale_offset, err_word=err,
+                      quant_mode=qli.QUANT_FP8)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(dev.cpu().numpy(), want)
+
+
+def test_fp8_quantised_inputs_feed_the_indexer():
+    """BF16 queries and index K quantised to E4M3 on the GPU (bit-equal to the
+    oracle's quantisation), K written into the pages on the GPU, then the
+    indexer in quant mode 1: the FP8 parity rule against the oracle."""
+    import torch
+    from test_fp8_gpu import check as check_fp8
+    case, kb, slots = _writer_setup(97, 2, [9000, 2500])
+    case.quant_mode = qli.QUANT_FP8
+    codes, scales = oracle.quantize_rows_e4m3(kb)
+    case.k_rows, case.k_scale = codes.view(np.int8), scales
+    qb = synth.bf16_rows(98, case.q.shape, sigma=1.0)
+    qc, qs = oracle.quantize_rows_e4m3(qb)
+    case.q, case.q_scale = qc.view(np.int8), qs
+    kw = synth.upload(case, "cuda")
+    cache = kw["cache"]
+    want = cache.cpu().numpy()
+    assert oracle.write_index_k(kb, slots, want, case.rows_per_page, case.k_offset,
+                                case.scale_offset, fp8=True) == 0
+    R = case.rows_per_page
+    for m in slots:                                   # scramble the index-K rows first
+        p, r = divmod(int(m), R)
+        cache[p, case.k_offset + r * D:case.k_offset + (r + 1) * D] = 0x5A
+    qli.write_index_k(_to_dev(kb), torch.from_numpy(slots).cuda(), cache,
+                      rows_per_page=R, page_stride=case.page_stride,
+                      k_offset=case.k_offset, scale_offset=case.scale_offset,
+                      quant_mode=qli.QUANT_FP8)
+    q, s = qli.quantize_q(_to_dev(qb), quant_mode=qli.QUANT_FP8)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache.cpu().numpy(), want)
+    assert np.array_equal(q.cpu().numpy(), case.q)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), case.q_scale)
+    check_fp8(case)
