@@ -162,6 +162,28 @@ def test_consumer_beyond_the_bitmap_takes_the_sorting_path():
     check(case)
 
 
+@pytest.mark.parametrize("geom", ["compact", "scales-first"])
+@pytest.mark.parametrize("ratio", [1, 2])
+def test_stream_path_page_geometries(geom, ratio):
+    """Page geometries other than the pages' own: the FP16 scales right after
+    the index-K rows in a compact page (stride R*130), and the scales placed
+    before the rows. The stream kernel takes k_offset and scale_offset as
+    given and matches the oracle in both, for source and consumer calls."""
+    import dataclasses
+    for mode, C in (("source", 64), ("consumer", 128)):
+        case = synth.make_case(90 + ratio, [9000, 1300, 260], [1, 1, 1], N=64, ratio=ratio,
+                               topk=200, cand_mode=mode, cand_blocks=C,
+                               name=f"geometry-{geom}-r{ratio}-{mode}")
+        R = case.rows_per_page
+        assert case.bt_stride * R > 4096        # not the single-launch path
+        if geom == "compact":
+            stride, ko, so = R * 130, 0, R * 128
+        else:
+            so, ko = 0, 2 * R + 16
+            stride = ko + R * 128 + 16
+        check(dataclasses.replace(case, page_stride=stride, k_offset=ko, scale_offset=so))
+
+
 def test_device_checks_flag_bad_metadata():
     import torch
     case = synth.make_case(8, [500, 300], [1, 1], N=64, ratio=2, topk=16)
