@@ -198,6 +198,7 @@ DevArgs make_dev_args(const qli_args& a, void* ws, const WsLayout& L) {
   d.R = a.rows_per_page;
   d.k_off = a.k_offset;
   d.s_off = a.scale_offset;
+  d.kfused = a.rows_per_page == kTile && a.scale_offset == a.k_offset + kTile * kHeadDim;
   d.num_pages = a.num_pages;
   d.bt = a.block_table;
   d.bt_stride = a.bt_stride;

@@ -94,6 +94,8 @@ struct DevArgs {
   int32_t num_sms;     // SMs of the device (persistent grids)
   int32_t small;       // 1: the single-launch path (planning, scoring, selection in one kernel)
   uint32_t* done;      // single-launch path: [T] CTAs of the token done (zeroed with err)
+  int32_t kfused;      // 1: 128-row pages whose FP16 scales follow the index-K rows
+                       // (s_off == k_off + 128*128): one copy brings both
 };
 
 struct WsLayout {

@@ -128,8 +128,19 @@ constexpr int kMmaWarp0 = 1, kConvWarp0 = 3, kEpiWarp0 = kConvWarp0 + 8,
               kWarpsTotal = kEpiWarp0 + 8;
 constexpr int kThreads = 32 * kWarpsTotal;
 static_assert(kThreads == 608, "stream kernel block size");
-constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per stage
-constexpr int kSBytes = kTile * 2;                   // 256 B of FP16 scales per stage
+constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per tile
+// A K stage (17 KB): the tile's 128 rows of 128 B from 0 (one 128-row page,
+// two 64-row pages, or 16 candidate blocks of 8 rows), their FP16 scales from
+// kScOff, brought by a second copy per page (by the producer's stores for
+// candidate tiles). A 128-row page whose scales follow its rows (kfused) is
+// fetched by one copy of 130 rows instead: the scales arrive in rows 128-129,
+// swizzled like the K rows. (Two 64-row pages cannot both carry their scale
+// row in a 17 KB stage without breaking the 1024-byte alignment that the
+// swizzle needs; stages of 18 KB that held them were slower.)
+constexpr int kStageBytes = 17 * 1024;
+constexpr uint32_t kScOff = kKBytes;
+static_assert(kScOff + kTile * 2 <= kStageBytes && (kKBytes + 2 * kHeadDim) <= kStageBytes &&
+                  kStageBytes % 1024 == 0, "K stage layout");
 constexpr int kBBytes = 64 * kHeadDim * 2;           // 16 KB: up to 64 heads, FP16
 constexpr uint32_t kTmemCols = 512;
 
@@ -144,9 +155,8 @@ constexpr int kSlots = 16;
 static_assert(kSlots >= 2 + kASlots + kDSlots && kSlots % 2 == 0, "wq / ks slot reuse distance");
 
 struct Smem {
-  uint8_t k[kKStages][kKBytes];                      // 1024-aligned (offset 0)
+  uint8_t k[kKStages][kStageBytes];                  // 1024-aligned (offset 0)
   uint8_t b[2][kBBytes];                             // 1024-aligned; one per converter group
-  uint8_t sc[kKStages][kSBytes];
   alignas(16) __half wq[kSlots][64];
   float ks[kSlots][kTile];
   uint64_t full[kKStages], empty[kKStages];
@@ -350,12 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         const int32_t p1 = __shfl_sync(0xffffffffu, pg1, k & 31);
         if (lane == 0) {
           const int npages = p1 >= 0 ? 2 : 1;
-          mbar_arrive_expect_tx(&S.full[s], npages * (a.R * kHeadDim + a.R * 2));
+          const int box_rows = a.kfused ? a.R + 2 : a.R;
+          mbar_arrive_expect_tx(&S.full[s],
+                                npages * (box_rows * kHeadDim + (a.kfused ? 0 : a.R * 2)));
           for (int p = 0; p < npages; ++p) {
             const int32_t page = p == 0 ? p0 : p1;
-            const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
             tma_load_3d_hint(&S.k[s][p * a.R * kHeadDim], &tm_page, 0, 0, page, &S.full[s], kpol);
-            bulk_g2s_hint(&S.sc[s][p * a.R * 2], pg + a.s_off, a.R * 2, &S.full[s], kpol);
+            if (!a.kfused) {
+              const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
+              bulk_g2s_hint(&S.k[s][kScOff + p * a.R * 2], pg + a.s_off, a.R * 2, &S.full[s], kpol);
+            }
           }
         }
       } else {
@@ -365,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
         const int32_t blk = cn_blk, page = cn_page;
         // the block's scales (gathered by the candidate kernel) go to the
         // stage by plain stores, ordered before lane 0's arrival on it
-        if (lane < nblk) *reinterpret_cast<uint4*>(&S.sc[s][lane * kBlock * 2]) = cn_sc;
+        if (lane < nblk) *reinterpret_cast<uint4*>(&S.k[s][kScOff + lane * kBlock * 2]) = cn_sc;
         __syncwarp();
         if (lane == 0) mbar_arrive_expect_tx(&S.full[s], nblk * (kBlock * kHeadDim));
         __syncwarp();
@@ -477,12 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
       // Two halves of 64 K values (32 TMEM columns) each.
       // The whole row and its scale go to registers first, so the K stage
       // returns to the producer before any conversion work.
+      // a fused page's scale bytes b = 2*row sit in box row 128 + b/128,
+      // whose swizzle phase is b/128 (128 is a multiple of 8)
+      uint32_t s_at = kScOff + 2 * row;
+      if (!consumer && a.kfused) {
+        const uint32_t b = 2u * row;
+        s_at = kKBytes + (b >> 7) * 128u + ((((b >> 4) & 7u) ^ ((b >> 7) & 7u)) << 4) + (b & 15u);
+      }
       const uint8_t* src = &S.k[sk][row * kHeadDim];
       uint4 raw[8];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         raw[ch] = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
-      S.ks[slot][row] = __half2float(*reinterpret_cast<const __half*>(&S.sc[sk][row * 2]));
+      S.ks[slot][row] = __half2float(*reinterpret_cast<const __half*>(&S.k[sk][s_at]));
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&S.empty[sk]);
@@ -621,7 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
 }  // namespace stream
 
 // Tensor map over the index-K rows of the page pool: x = the 128 bytes of a
-// row, y = row within the page (R rows, 128 B apart), z = page (page_stride
+// row, y = row within the page (`rows` rows, 128 B apart: R, or 130 when a
+// 128-row page's 256 bytes of scales follow its rows), z = page (page_stride
 // apart); the box is 128 B x box_rows x 1 page, 128-byte swizzle.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -641,10 +663,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool encode_k_map(const DevArgs& d, int box_rows, CUtensorMap* m) {
+bool encode_k_map(const DevArgs& d, int rows, int box_rows, CUtensorMap* m) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(d.R),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(d.num_pages)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
                                  static_cast<cuuint64_t>(d.page_stride)};
@@ -664,7 +686,10 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
   if (d.stream_path) {
     CUtensorMap tm_page, tm_blk;
-    if (!encode_k_map(d, d.R, &tm_page) || !encode_k_map(d, kBlock, &tm_blk))
+    // with the scales right after a 128-row page's rows, its box runs on
+    // over them (two more rows)
+    const int page_rows = d.kfused ? d.R + 2 : d.R;
+    if (!encode_k_map(d, page_rows, page_rows, &tm_page) || !encode_k_map(d, d.R, kBlock, &tm_blk))
       return cudaErrorInvalidValue;
     // one instance per code type: INT8 (quant mode 2) or E4M3 (quant mode 1)
     auto* kern = d.fp8 ? stream::stream_kernel<true> : stream::stream_kernel<false>;
