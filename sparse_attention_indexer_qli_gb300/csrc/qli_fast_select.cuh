@@ -93,10 +93,12 @@ __device__ __forceinline__ Row row_of(const DevArgs& a, int t, int which, int32_
 // candidates (digits of 12, 10 and 10 bits) finds the want-th best key; the
 // winners are marked in position bitmaps, and one ordered scan of the bitmaps
 // writes them in ascending order (equal keys at the threshold by lower
-// position). Histograms hold two 16-bit counts per word. A row this path
-// cannot finish (longer than kFMaxLen entries, a sample that misjudged: fewer
-// than `want` or more than kFCap candidates) is appended to a list for the
-// general selection (select_list_kernel), which ranks it exactly.
+// position). Histograms hold two 16-bit counts per word. Where the sample
+// misjudged the row (the pass kept fewer than `want` or more than kFCap
+// entries) the sample rank is scaled by what the pass kept and the pass runs
+// once more. A row this path cannot finish (longer than kFMaxLen entries, or
+// misjudged twice) is appended to a list for the general selection
+// (select_list_kernel), which ranks it exactly.
 constexpr int kFT = 256;
 constexpr int kFW = kFT / 32;
 constexpr int kFPerSM = 4;                         // resident CTAs per SM
@@ -264,28 +266,6 @@ __device__ __forceinline__ void fast_row(const DevArgs& a, int t, int which, int
     }
     if (tid == 0) F.cnt = 0u;
     __syncthreads();
-    // ---- provisional threshold (keep everything when the row fits)
-    uint32_t t_p = 0u;
-    if (sampled) {
-      const float fv[4] = {sf.x, sf.y, sf.z, sf.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (s0 + j < len) hist16_add(F.shist, hist_bin(order_key(fv[j])));
-      __syncthreads();
-      // a rank 10% past the want-th best's expected sample rank, plus 24
-      const uint32_t rank = static_cast<uint32_t>(
-          (static_cast<int64_t>(want) * kSample * 11) / (10 * static_cast<int64_t>(len))) + 24u;
-      if (rank >= static_cast<uint32_t>(kSample) - 64u) {   // block-uniform
-            enlist(a, t, which);
-        return;
-      }
-      fast_pick<kHistBins>(F.shist, rank, F);
-      t_p = F.sel[0] << (32 - kHistBits);
-      // the sample's histogram becomes the 10-bit digits' (read after the
-      // barrier that ends the pass)
-      reinterpret_cast<uint4*>(F.shist)[tid] = z4;
-      reinterpret_cast<uint4*>(F.shist)[tid + kFT] = z4;
-    }
     const float kNaN = __uint_as_float(0x7fffffffu);
     if (!sampled) {
       // ---- a row that fits keeps every entry in place: slot = position;
@@ -303,58 +283,93 @@ __device__ __forceinline__ void fast_row(const DevArgs& a, int t, int which, int
       }
       if (tid == 0) F.cnt = static_cast<uint32_t>(len);
     } else {
-      // ---- one pass over the row: the position of every entry with key >=
-      // t_p, found by a float compare against the smallest score of that
-      // key (NaN, which passes no compare, pads past the end); warp w owns a
-      // contiguous segment (whole 128-entry rows, its last step possibly
-      // partial), lane l entries 4l..4l+3 of each 128
-      const float f_p = key_floor(t_p);
+      // ---- provisional threshold from the sample
+      const float fv[4] = {sf.x, sf.y, sf.z, sf.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (s0 + j < len) hist16_add(F.shist, hist_bin(order_key(fv[j])));
+      __syncthreads();
+      // a rank 10% past the want-th best's expected sample rank, plus 24
+      uint32_t rank = static_cast<uint32_t>(
+          (static_cast<int64_t>(want) * kSample * 11) / (10 * static_cast<int64_t>(len))) + 24u;
+      constexpr uint32_t kRankMax = static_cast<uint32_t>(kSample) - 64u;
+      if (rank >= kRankMax) {   // block-uniform
+        enlist(a, t, which);
+        return;
+      }
       const int32_t seg = ((len + kFW - 1) / kFW + 127) & ~127;
       const int32_t lo = warp * seg, hi = min(len, lo + seg);
-      for (int32_t b = lo; b < hi; b += kFStep) {
-        float v[4 * kFB];
+      for (int attempt = 0;; ++attempt) {
+        fast_pick<kHistBins>(F.shist, rank, F);
+        // ---- one pass over the row: the position of every entry with a key
+        // at or above the picked bin's, found by a float compare against the
+        // smallest score of that key (NaN, which passes no compare, pads past
+        // the end); warp w owns a contiguous segment (whole 128-entry rows,
+        // its last step possibly partial), lane l entries 4l..4l+3 of each 128
+        const float f_p = key_floor(F.sel[0] << (32 - kHistBits));
+        for (int32_t b = lo; b < hi; b += kFStep) {
+          float v[4 * kFB];
 #pragma unroll
-        for (int u = 0; u < kFB; ++u) {
-          const int32_t e0 = b + 128 * u + 4 * lane;
-          const float4 f = e0 < hi ? __ldcg(v4 + (e0 >> 2)) : make_float4(kNaN, kNaN, kNaN, kNaN);
-          v[4 * u] = f.x;
-          v[4 * u + 1] = f.y;
-          v[4 * u + 2] = f.z;
-          v[4 * u + 3] = f.w;
-        }
-        if (b + kFStep > hi) {                          // warp-uniform: a segment's ragged end
+          for (int u = 0; u < kFB; ++u) {
+            const int32_t e0 = b + 128 * u + 4 * lane;
+            const float4 f = e0 < hi ? __ldcg(v4 + (e0 >> 2)) : make_float4(kNaN, kNaN, kNaN, kNaN);
+            v[4 * u] = f.x;
+            v[4 * u + 1] = f.y;
+            v[4 * u + 2] = f.z;
+            v[4 * u + 3] = f.w;
+          }
+          if (b + kFStep > hi) {                          // warp-uniform: a segment's ragged end
 #pragma unroll
-          for (int e = 0; e < 4 * kFB; ++e)
-            if (b + 128 * (e >> 2) + 4 * lane + (e & 3) >= hi) v[e] = kNaN;
-        }
-        uint32_t m = 0u;
+            for (int e = 0; e < 4 * kFB; ++e)
+              if (b + 128 * (e >> 2) + 4 * lane + (e & 3) >= hi) v[e] = kNaN;
+          }
+          uint32_t m = 0u;
 #pragma unroll
-        for (int e = 0; e < 4 * kFB; ++e) m |= v[e] >= f_p ? (1u << e) : 0u;
-        const uint32_t c = __popc(m);
-        uint32_t incl = c;
+          for (int e = 0; e < 4 * kFB; ++e) m |= v[e] >= f_p ? (1u << e) : 0u;
+          const uint32_t c = __popc(m);
+          uint32_t incl = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+          if (tot == 0u) continue;                        // warp-uniform
+          uint32_t base = 0u;
+          if (lane == 31) base = atomicAdd(&F.cnt, tot);
+          base = __shfl_sync(0xffffffffu, base, 31);
+          // a row whose candidates overflow the room is listed, so a step
+          // whose slots do not all fit writes none of them (warp-uniform)
+          if (base + tot > static_cast<uint32_t>(kFCap)) continue;
+          // positions only, one per kept entry; the scores are read again below
+          uint32_t w = base + incl - c;
+          const uint32_t lane_pos = static_cast<uint32_t>(b + 4 * lane);
+          while (m) {
+            const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
+            m &= m - 1u;
+            F.cpos[w++] = static_cast<uint16_t>(lane_pos + 128u * (e >> 2) + (e & 3u));
+          }
         }
-        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-        if (tot == 0u) continue;                        // warp-uniform
-        uint32_t base = 0u;
-        if (lane == 31) base = atomicAdd(&F.cnt, tot);
-        base = __shfl_sync(0xffffffffu, base, 31);
-        // a row whose candidates overflow the room is listed, so a step
-        // whose slots do not all fit writes none of them (warp-uniform)
-        if (base + tot > static_cast<uint32_t>(kFCap)) continue;
-        // positions only, one per kept entry; the scores are read again below
-        uint32_t w = base + incl - c;
-        const uint32_t lane_pos = static_cast<uint32_t>(b + 4 * lane);
-        while (m) {
-          const uint32_t e = static_cast<uint32_t>(__ffs(m) - 1);
-          m &= m - 1u;
-          F.cpos[w++] = static_cast<uint16_t>(lane_pos + 128u * (e >> 2) + (e & 3u));
-        }
+        __syncthreads();
+        // a threshold that kept fewer than `want` or more than kFCap entries
+        // (the sample misjudged the row) is moved once: the rank is scaled by
+        // what it kept, aiming at the middle of [want, kFCap]
+        const uint32_t got = F.cnt;
+        const bool fits = got >= static_cast<uint32_t>(want) && got <= static_cast<uint32_t>(kFCap);
+        if (attempt > 0 || fits) break;                 // block-uniform
+        const uint32_t aim = (static_cast<uint32_t>(want) + kFCap) / 2u;
+        uint32_t r2 = got == 0u ? 2u * rank + 32u
+                                : static_cast<uint32_t>(static_cast<uint64_t>(rank) * aim / got);
+        r2 = min(max(r2, 1u), kRankMax);
+        if (r2 == rank) break;
+        rank = r2;
+        __syncthreads();                                // every thread has read F.cnt
+        if (tid == 0) F.cnt = 0u;                       // (fast_pick's barrier orders it)
       }
-      __syncthreads();
+      // the sample's histogram becomes the 10-bit digits' (added to after
+      // the barrier that follows the gather below)
+      reinterpret_cast<uint4*>(F.shist)[tid] = z4;
+      reinterpret_cast<uint4*>(F.shist)[tid + kFT] = z4;
       // ---- the kept scores again (from L2), as keys, and their first digit;
       // a row that overflowed the room (and so left slots unwritten) is
       // listed below instead

@@ -356,6 +356,73 @@ def test_prefill_rows_longer_than_the_candidate_space_sample_a_threshold():
     check(case)
 
 
+def _sample_runs(n):
+    """Entries of a row of n the many-rows-per-SM selection samples: 16
+    evenly spread runs of 64 (each start rounded down to a multiple of 4)."""
+    tid = np.arange(256)
+    s0 = (((n * (tid >> 4)) // 16) & ~3) + 4 * (tid & 15)
+    idx = (s0[:, None] + np.arange(4)[None, :]).reshape(-1)
+    return idx[idx < n]
+
+
+def _threshold_attempts(sc, want, cap=4608, sample=1024):
+    """What the sampled pass keeps, attempt by attempt: the threshold is the
+    floor of the 12-bit key bin holding the sample's rank-th best (rank 10%
+    past the want-th best's expected sample rank, plus 24); a count outside
+    [want, cap] scales the rank once by (want + cap) / 2 over the count."""
+    def keys(f):
+        u = np.asarray(f, dtype=np.float32).view(np.uint32).copy()
+        u[(u << np.uint32(1)) == 0] = 0
+        return np.where(u >> np.uint32(31) == 1, ~u, u | np.uint32(0x80000000)).astype(np.uint32)
+    n = sc.size
+    hist = np.bincount(keys(sc[_sample_runs(n)]) >> np.uint32(20), minlength=4096)
+    k = keys(sc)
+    rank = (want * sample * 11) // (10 * n) + 24
+    got = []
+    for attempt in range(2):
+        b = 4095 - int(np.argmax(np.cumsum(hist[::-1]) >= rank))
+        got.append(int(np.count_nonzero(k >= np.uint32(b << 20))))
+        if want <= got[-1] <= cap:
+            break
+        rank = min(max(rank * ((want + cap) // 2) // got[-1] if got[-1] else 2 * rank + 32, 1),
+                   sample - 64)
+    return got
+
+
+def test_prefill_rows_whose_sample_misjudges_the_threshold():
+    """K scales raised by half at the entries the selection samples make the
+    sample overrate its row: the first pass keeps fewer than TopK entries.
+    The pass then runs once more with the rank scaled by what it kept; where
+    that still misses, the row goes to the general selection. The input is
+    checked to hold both kinds of row, and every row must equal the
+    oracle's."""
+    case = synth.make_case(85, [24000, 10000, 9500], [5, 3, 4], N=64, ratio=2, topk=2048,
+                           cand_mode="source", cand_blocks=1024, name="prefill-misjudged")
+    assert case.T > 2 * case.B
+    prep = oracle.prepare(case)
+    vis = oracle.run(prep, rows=np.arange(case.T), want_scores=False)["visible"]
+    owner = np.searchsorted(case.cu_seqlens_q, np.arange(case.T), side="right") - 1
+    for b in range(case.B):
+        L = int(case.k_lens[b])
+        ks = case.k_scale[case.k_row_start[b]:case.k_row_start[b] + L].view(np.float16)
+        hit = np.zeros(L, bool)
+        for t in np.flatnonzero(owner == b):
+            idx = _sample_runs(int(vis[t]))
+            hit[idx[idx < L]] = True
+        ks[hit] = (ks[hit].astype(np.float32) * 1.5).astype(np.float16)
+    prep = oracle.prepare(case)
+    ora = oracle.run(prep, rows=np.arange(case.T), want_scores=True,
+                     score_stride=int(case.k_lens.max()))
+    kinds = set()
+    for t in range(case.T):
+        V = int(ora["visible"][t])
+        if V > 4608:
+            got = _threshold_attempts(ora["scores"][t][:V], case.topk)
+            kinds.add((len(got), case.topk <= got[-1] <= 4608))
+    assert (2, True) in kinds and (2, False) in kinds, kinds
+    check(case)
+
+
 def test_prefill_rows_between_32k_and_the_shared_memory_limit():
     """Prefill rows of 32K-45K positions: the many-rows-per-SM selection
     still takes them (position bitmaps of up to 1408 words, 16-bit
