@@ -221,14 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     int k = 0, n = 0;
     for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
       const Unit x = unit_at(a, u);
-      // before overwriting the queries and this parity's weights: every
-      // epilogue warp has loaded the previous unit's last tile (so it is done
-      // with the unit before that), and the previous unit's MMAs are complete
-      if (k > 0 && !mbar_wait_warp<true>(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
-      if (!mbar_wait_warp<true>(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
       const int nrows = x.cnt * a.N;
       {
-        // every load first, then the conversions (one global latency, not eight)
+        // the unit's queries and weights are loaded first (one global
+        // latency, overlapping the previous unit's last tiles), then stored
+        // once the buffers are free
         constexpr int kPer = kMaxMmaN * 16 / 512;
         uint2 v[kPer];
 #pragma unroll
@@ -240,6 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             v[i] = *reinterpret_cast<const uint2*>(a.q + static_cast<int64_t>(x.t0 + gi) * a.q_st +
                                                    static_cast<int64_t>(h) * a.q_sh + ch * 8);
         }
+        uint16_t wb = 0, qb = 0;
+        if (etid < nrows) {
+          const int64_t o = static_cast<int64_t>(x.t0) * a.N + etid;   // tokens are consecutive
+          wb = a.w[o];
+          qb = a.qs[o];
+        }
+        // before overwriting the queries and this parity's weights: every
+        // epilogue warp has loaded the previous unit's last tile (so it is
+        // done with the unit before that), and the previous unit's MMAs are
+        // complete
+        if (k > 0 && !mbar_wait_warp<true>(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait_warp<true>(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
+        if (etid < nrows) S.wq[n & 1][etid] = __hmul(__ushort_as_half(wb), __ushort_as_half(qb));
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
           const int idx = etid + 512 * i;
@@ -248,10 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) =
                 a.fp8 ? e4m3x8_to_f16x8(v[i], true) : widen8(v[i], true);
         }
-      }
-      for (int nn = etid; nn < nrows; nn += 512) {
-        const int64_t o = static_cast<int64_t>(x.t0) * a.N + nn;   // tokens are consecutive
-        S.wq[n & 1][nn] = __hmul(__ushort_as_half(a.w[o]), __ushort_as_half(a.qs[o]));
       }
       fence_proxy_async_smem();
       __syncwarp();
