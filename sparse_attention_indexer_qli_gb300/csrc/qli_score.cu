@@ -88,6 +88,11 @@ __device__ __forceinline__ uint4 i8x8_to_f16x8_div1024(uint2 v) {
 //               block in consumer mode); for dense tiles lane j resolves the
 //               page IDs of tile k0+j once per 32 tiles, so no block-table
 //               load sits between two copies
+//   warp 19     consumer mode only: a second producer, warp 0 taking the
+//               even tiles and warp 19 the odd ones. A candidate tile is 16
+//               copies and each holds its issuing thread for hundreds of
+//               cycles, so one issuer would cap the tile rate; dense tiles
+//               (one or two copies) run faster with a single producer
 //   warps 1-2   MMA, one issuing thread per tile parity: 8 x tcgen05.mma
 //               (A from TMEM, B = the token's queries from shared memory),
 //               committed to the A slot's and the accumulator's barriers.
@@ -103,11 +108,12 @@ __device__ __forceinline__ uint4 i8x8_to_f16x8_div1024(uint2 v) {
 //               golden chain per position (a 64-long dependent FP32 add chain,
 //               so two tiles are summed at once), score store, block max
 // Each tile parity p runs converter group p -> MMA warp p -> epilogue group
-// p, and owns A slots p, p + 2 and accumulator slots p, p + 2: the two
-// parities are independent in-order pipelines (sharing only the K ring), so
-// every barrier's previous phase belongs to the same parity and has already
-// been consumed. (With an odd slot count, one parity's epilogue could meet a
-// slot still a phase behind, waiting on the other parity's MMA issuer.)
+// p, and owns A slots p, p + 2 and accumulator slots p, p + 2 (in consumer
+// mode also producer p and K stages p, p + 2, ...): the two parities are
+// independent in-order pipelines, so every barrier's previous phase belongs
+// to the same parity and has already been consumed. (With an odd slot
+// count, one parity's epilogue could meet a slot still a phase behind,
+// waiting on the other parity's MMA issuer.)
 namespace stream {
 
 constexpr int kKStages = 8;                          // shared-memory K ring
@@ -122,12 +128,13 @@ static_assert(kASlots % 2 == 0 && kDSlots % 2 == 0, "each tile parity owns its s
 constexpr uint32_t kSlotCols = 64;
 constexpr uint32_t kDCol0 = kASlots * kSlotCols;
 static_assert(kDCol0 + kDSlots * kSlotCols == 512, "TMEM column budget");
-// warp roles: 0 producer, 1 MMA, then two groups of four converter warps,
-// then two groups of four epilogue warps
-constexpr int kMmaWarp0 = 1, kConvWarp0 = 3, kEpiWarp0 = kConvWarp0 + 8,
-              kWarpsTotal = kEpiWarp0 + 8;
-constexpr int kThreads = 32 * kWarpsTotal;
-static_assert(kThreads == 608, "stream kernel block size");
+// warp roles: 0 producer, 1-2 MMA, then two groups of four converter warps,
+// then two groups of four epilogue warps, then the second producer
+constexpr int kProdWarp0 = 0, kMmaWarp0 = 1, kConvWarp0 = 3, kEpiWarp0 = kConvWarp0 + 8,
+              kProdWarp1 = kEpiWarp0 + 8;
+// block size: the dense instance has no second producer
+constexpr int threads_for(bool cand) { return 32 * (kProdWarp1 + (cand ? 1 : 0)); }
+static_assert(threads_for(false) == 608 && threads_for(true) == 640, "stream kernel block size");
 constexpr int kKBytes = kTile * kHeadDim;            // 16 KB of INT8 rows per tile
 // A K stage (17 KB): the tile's 128 rows of 128 B from 0 (one 128-row page,
 // two 64-row pages, or 16 candidate blocks of 8 rows), their FP16 scales from
@@ -228,11 +235,12 @@ __device__ __forceinline__ void cvt_row16(const uint4 v, uint32_t* out8) {
 // tm_page: box of R rows x 128 B (a whole page's index K); tm_blk: box of
 // 8 rows x 128 B (one candidate block). Both use the 128-byte swizzle, so
 // row r's 16-byte chunk c lands at r*128 + ((c ^ (r & 7)) * 16).
-// 19 warps: the four SM sub-partitions hold 5, 5, 5 and 4 of them in 16K
-// registers each, which caps a thread at 96 registers (allocated in steps of
-// 8): a larger per-thread budget would make the launch fail
-template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(
+// 19 warps (20 with the second producer): the four SM sub-partitions hold
+// at most 5 of them each in 16K registers, which caps a thread at 96
+// registers (allocated in steps of 8): a larger per-thread budget would make
+// the launch fail
+template <bool kFp8, bool kCand>
+__global__ void __launch_bounds__(threads_for(kCand), 1) stream_kernel(
     const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_blk,
     DevArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -278,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     return;
   }
   const int32_t nk = u1 - u0;
-  const bool consumer = a.mode == QLI_CAND_CONSUMER;
+  const bool consumer = a.mode == QLI_CAND_CONSUMER;   // == kCand
   bool ok = true;
 
-  if (warp == 0) {
-    // ---------------- producer
+  if (!kCand && warp == kProdWarp0) {
+    // ---------------- producer (dense tiles)
     // index K is read once: its lines leave L2 first, ahead of the score
     // rows and histograms the selection reads next
     const uint64_t kpol = l2_policy_evict_first();
@@ -396,6 +404,62 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(
     // never leave a copy in flight: wait for the last stages issued
     if (lane == 0) {
       for (int k = max(0, issued - kKStages); k < issued; ++k)
+        (void)mbar_wait_drain(&S.full[k % kKStages], (k / kKStages) & 1);
+    }
+    if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
+  } else if (kCand && (warp == kProdWarp0 || warp == kProdWarp1)) {
+    // ---------------- producers of candidate tiles: warp kProdWarp0 takes
+    // the even tiles, kProdWarp1 the odd ones; a tile's candidate count,
+    // this lane's block, its page and scales are loaded while the
+    // producer's previous tile is issued
+    const int pp = warp == kProdWarp0 ? 0 : 1;
+    const uint64_t kpol = l2_policy_evict_first();
+    Cursor c;
+    c.init(a, u0 + pp);
+    int last = -1;
+    int32_t cn_nc = 0, cn_blk = 0, cn_page = 0;
+    uint4 cn_sc = make_uint4(0u, 0u, 0u, 0u);
+    const auto fetch = [&](const Cursor& at) {
+      const int32_t t = at.t;
+      const int64_t i = static_cast<int64_t>(t) * a.C + at.tile * (kTile / kBlock) + lane;
+      cn_nc = a.cand_cnt[t];
+      if (at.tile * (kTile / kBlock) + lane < a.C) {
+        cn_blk = a.cand_list[i];
+        cn_page = a.cand_page[i];
+        cn_sc = a.cand_sc[i];
+      }
+    };
+    if (pp < nk) fetch(c);
+    for (int k = pp; k < nk && ok; k += 2) {
+      const int s = k % kKStages;
+      const uint32_t ph = (k / kKStages) & 1;
+      if (lane == 0) ok = mbar_wait_bounded(&S.empty[s], ph ^ 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // pages were looked up (and range-checked) by the candidate kernel
+      const int32_t first = c.tile * (kTile / kBlock);
+      const int32_t nblk = min(kTile / kBlock, cn_nc - first);
+      const int32_t blk = cn_blk, page = cn_page;
+      // the block's scales (gathered by the candidate kernel) go to the
+      // stage by plain stores, ordered before lane 0's arrival on it
+      if (lane < nblk) *reinterpret_cast<uint4*>(&S.k[s][kScOff + lane * kBlock * 2]) = cn_sc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&S.full[s], nblk * (kBlock * kHeadDim));
+      __syncwarp();
+      if (lane < nblk) {
+        const int32_t row = (blk * kBlock) % a.R;
+        tma_load_3d_hint(&S.k[s][lane * kBlock * kHeadDim], &tm_blk, 0, row, page, &S.full[s],
+                         kpol);
+      }
+      c.next(a, u0 + k + 1);
+      c.next(a, u0 + k + 2);
+      if (k + 2 < nk) fetch(c);
+      __syncwarp();
+      last = k;
+    }
+    // never leave a copy in flight: wait for this producer's last stages
+    if (lane == 0) {
+      for (int k = max(pp, last - kKStages + 2); k <= last; k += 2)
         (void)mbar_wait_drain(&S.full[k % kKStages], (k / kKStages) & 1);
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
@@ -680,7 +744,7 @@ bool encode_k_map(const DevArgs& d, int rows, int box_rows, CUtensorMap* m) {
 
 }  // namespace
 
-std::atomic<uint64_t> g_smem_stream_kernel[2] = {{0}, {0}};
+std::atomic<uint64_t> g_smem_stream_kernel[4] = {{0}, {0}, {0}, {0}};
 
 cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0) return cudaSuccess;
@@ -692,12 +756,19 @@ cudaError_t launch_score(const DevArgs& d, cudaStream_t s) {
     if (!encode_k_map(d, page_rows, page_rows, &tm_page) || !encode_k_map(d, d.R, kBlock, &tm_blk))
       return cudaErrorInvalidValue;
     // one instance per code type: INT8 (quant mode 2) or E4M3 (quant mode 1)
-    auto* kern = d.fp8 ? stream::stream_kernel<true> : stream::stream_kernel<false>;
+    // one instance per code type (INT8, quant mode 2, or E4M3, quant mode 1)
+    // and per tile kind (dense or candidate blocks)
+    const bool cand = d.mode == QLI_CAND_CONSUMER;
+    void (*const kinds[4])(CUtensorMap, CUtensorMap, DevArgs) = {
+        stream::stream_kernel<false, false>, stream::stream_kernel<false, true>,
+        stream::stream_kernel<true, false>, stream::stream_kernel<true, true>};
+    const int which = (d.fp8 ? 2 : 0) + (cand ? 1 : 0);
+    auto* kern = kinds[which];
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), stream::kSmemBytes,
-                                      g_smem_stream_kernel[d.fp8 ? 1 : 0]);
+                                      g_smem_stream_kernel[which]);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(d.num_sms), dim3(stream::kThreads), stream::kSmemBytes, s, tm_page,
-                   tm_blk, d);
+    e = launch_pdl(kern, dim3(d.num_sms), dim3(stream::threads_for(cand)), stream::kSmemBytes, s,
+                   tm_page, tm_blk, d);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   return launch_prefill(d, s);

@@ -1,8 +1,9 @@
 """A model of the stream kernel's barrier protocol, explored over random
 interleavings on the CPU.
 
-The kernel's roles (one TMA producer; two converter groups, two MMA
-issuers and two epilogue groups, one of each per tile parity) hand tiles to
+The kernel's roles (one TMA producer, or for candidate tiles one per tile
+parity; two converter groups, two MMA issuers and two epilogue groups, one
+of each per tile parity) hand tiles to
 each other through mbarriers waited on by phase parity. A parity wait cannot
 tell phase n from phase n-2: if a waiter can ever reach a barrier two phases
 early, it passes on a stale phase. The model tracks every barrier's count of
@@ -66,7 +67,7 @@ class Barrier:
             raise Stale("%s: waited for phase %d, barrier has completed %d" % (what, phase, self.done))
 
 
-def run(c, nk, seed, token_every):
+def run(c, nk, seed, token_every, producers=1):
     S, A, D, SL = c["S"], c["A"], c["D"], c["SL"]
     rng = random.Random(seed)
     full = [Barrier(1) for _ in range(S)]
@@ -85,8 +86,8 @@ def run(c, nk, seed, token_every):
     token_change = {k for k in range(nk) if k < 2 or (token_every and k % token_every == 0)}
 
     # role programs: lists of steps; each step = (ready(), act())
-    def producer():
-        for k in range(nk):
+    def producer(p):
+        for k in range(p, nk, producers):
             s = k % S
             if k >= S:
                 yield ("wait", empty[s], k // S - 1, "empty")
@@ -149,7 +150,8 @@ def run(c, nk, seed, token_every):
 
     inflight = []                   # copies in flight: they land in any order
     mmas = []                       # MMAs in flight: the tensor core finishes them in issue order
-    roles = [producer(), converter(0), converter(1), mma(0), mma(1), epilogue(0), epilogue(1)]
+    roles = [producer(p) for p in range(producers)]
+    roles += [converter(0), converter(1), mma(0), mma(1), epilogue(0), epilogue(1)]
 
     def advance(r):
         try:
@@ -190,12 +192,15 @@ def run(c, nk, seed, token_every):
                                                          for p in pending])
 
 
-def test_kernel_slot_counts_never_meet_a_stale_phase():
+@pytest.mark.parametrize("producers", [1, 2])
+def test_kernel_slot_counts_never_meet_a_stale_phase(producers):
+    # one producer for dense tiles; for candidate tiles two, each issuing
+    # the tiles of one parity into the stages of that parity
     c = kernel_constants()
-    assert c["A"] % 2 == 0 and c["D"] % 2 == 0
+    assert c["A"] % 2 == 0 and c["D"] % 2 == 0 and c["S"] % 2 == 0
     for seed in range(400):
         for nk in (1, 2, 7, 33):
-            run(c, nk, seed, token_every=1 + seed % 9)
+            run(c, nk, seed, token_every=1 + seed % 9, producers=producers)
 
 
 def test_the_model_catches_odd_slot_counts():
