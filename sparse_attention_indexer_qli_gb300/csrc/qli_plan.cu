@@ -192,10 +192,9 @@ __device__ void consumer_units(const DevArgs& a) {
 // page 0 instead. The score kernel then needs one round trip per tile and
 // one copy per block.
 template <int NT>
-__device__ void cand_pages(const DevArgs& a, int t, int32_t n) {
+__device__ void cand_pages(const DevArgs& a, int t, int32_t n, const int32_t* list) {
   __syncthreads();                       // the CTA's list writes are visible
   const int32_t b = a.tok_b[t];
-  const int32_t* list = a.cand_list + static_cast<int64_t>(t) * a.C;
   int32_t* pages = a.cand_page + static_cast<int64_t>(t) * a.C;
   const int64_t bt_row = static_cast<int64_t>(b < 0 ? 0 : b) * a.bt_stride;
   bool bad = false;
@@ -223,6 +222,8 @@ __global__ void __launch_bounds__(kPrepThreads) cand_prep_kernel(DevArgs a, int3
   __shared__ int32_t keys[kMaxCand];
   __shared__ int32_t warp_sum[kPrepThreads / 32];
   const int t = blockIdx.x, tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();                            // V(t) and the zeroed counter
   const int32_t V = a.tok_V[t];
   const int32_t nb = (V + kBlock - 1) / kBlock;
   const int32_t* row = a.cand_in + static_cast<int64_t>(t) * a.C;
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kPrepThreads) cand_prep_kernel(DevArgs a, int3
   for (int k = lo; k < lo + per && k < pow2; ++k)
     if (keys[k] != INT_MAX && (k == 0 || keys[k] != keys[k - 1])) out[pos++] = keys[k];
   if (tid == 0) a.cand_cnt[t] = total;
-  cand_pages<kPrepThreads>(a, t, total);
+  cand_pages<kPrepThreads>(a, t, total, a.cand_list + static_cast<int64_t>(t) * a.C);
 
   consumer_units<kPrepThreads>(a);
 }
@@ -290,7 +291,12 @@ constexpr int kBitmapWords = 16384;                  // 64 KB: 524288 blocks
 __global__ void __launch_bounds__(kBitmapThreads) cand_bitmap_kernel(DevArgs a, int32_t words) {
   extern __shared__ uint32_t bm[];
   __shared__ int32_t warp_sum[kBitmapThreads / 32];
+  __shared__ int32_t s_list[kMaxCand];    // the list again, for the page lookups
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the score kernel may start its set-up now; V(t) and the zeroed counter
+  // come from the planning kernel
+  pdl_trigger();
+  pdl_wait();
   const int32_t V = a.tok_V[t];
   const int32_t nb = (V + kBlock - 1) / kBlock;
   const int32_t nw = min((nb + 31) >> 5, words);
@@ -324,12 +330,14 @@ __global__ void __launch_bounds__(kBitmapThreads) cand_bitmap_kernel(DevArgs a, 
   for (int32_t w = w0; w < w1; ++w) {
     uint32_t bits = bm[w];
     while (bits) {
-      out[pos++] = (w << 5) + (__ffs(bits) - 1);
+      const int32_t id = (w << 5) + (__ffs(bits) - 1);
+      out[pos] = id;
+      s_list[pos++] = id;
       bits &= bits - 1u;
     }
   }
   if (tid == 0) a.cand_cnt[t] = total;
-  cand_pages<kBitmapThreads>(a, t, total);
+  cand_pages<kBitmapThreads>(a, t, total, s_list);
   consumer_units<kBitmapThreads>(a);
 }
 
@@ -354,12 +362,16 @@ cudaError_t launch_plan(const DevArgs& d, cudaStream_t s) {
                               g_smem_cand_bitmap);
         if (e != cudaSuccess) return e;
       }
-      cand_bitmap_kernel<<<d.T, kBitmapThreads, 4 * w, s>>>(d, w);
+      e = launch_pdl(cand_bitmap_kernel, dim3(static_cast<unsigned>(d.T)), dim3(kBitmapThreads),
+                     static_cast<size_t>(4 * w), s, d, w);
+      if (e != cudaSuccess) return e;
     } else {
       int32_t pow2 = 1;
       while (pow2 < d.C) pow2 <<= 1;
       if (pow2 < kPrepThreads) pow2 = kPrepThreads;
-      cand_prep_kernel<<<d.T, kPrepThreads, 0, s>>>(d, pow2);
+      e = launch_pdl(cand_prep_kernel, dim3(static_cast<unsigned>(d.T)), dim3(kPrepThreads), 0, s,
+                     d, pow2);
+      if (e != cudaSuccess) return e;
     }
     e = cudaGetLastError();
   }
