@@ -7,8 +7,9 @@
 //    (a few MB per request: L2-resident while the main kernel runs);
 //  * prefill_kernel is persistent, one CTA per SM. A unit is one token group
 //    (up to 4 tokens of one request, MMA N = tokens*64 <= 256) and a range of
-//    up to 64 position tiles. The group's queries stay in shared memory
-//    (FP16 * 2^-10, 128-byte swizzle) for the whole unit; K tiles stream in
+//    up to 64 position tiles; a CTA takes a contiguous range of units, and a
+//    group's queries stay in shared memory (FP16 * 2^-10, 128-byte swizzle)
+//    across all of its units in the range; K tiles stream in
 //    by TMA (128-byte swizzle) through a 4-stage ring; the 128 x N FP32
 //    accumulator is double-buffered across all 512 TMEM columns.
 // Warp roles: warp 0 producer, warp 1 MMA issuer, warps 2-17 epilogue (four
@@ -98,9 +99,25 @@ __global__ void __launch_bounds__(kConvThreads) kconv_kernel(DevArgs a) {
 }
 
 // ---- unit walk -----------------------------------------------------------
+// A CTA takes a contiguous range of the unit list, so its consecutive units
+// mostly belong to one token group: the group's queries are staged once for
+// all of them, and the next unit is found from the current one.
 struct Unit {
-  int32_t g, t0, cnt, b, tile0, ntiles;
+  int32_t g, t0, cnt, b, tile0, ntiles, tiles;
 };
+
+__device__ __forceinline__ Unit unit_of_group(const DevArgs& a, int32_t g, int32_t u) {
+  Unit x;
+  x.g = g;
+  x.t0 = a.grp_t0[g];
+  x.cnt = a.grp_cnt[g];
+  x.b = a.tok_b[x.t0];
+  const int32_t vmax = a.tok_V[x.t0 + x.cnt - 1];
+  x.tiles = (vmax + kTile - 1) / kTile;
+  x.tile0 = (u - a.unit_start[g]) * kUnitTiles;
+  x.ntiles = min(kUnitTiles, x.tiles - x.tile0);
+  return x;
+}
 
 __device__ __forceinline__ Unit unit_at(const DevArgs& a, int32_t u) {
   int32_t lo = 0, hi = a.Gmax - 1;
@@ -108,16 +125,26 @@ __device__ __forceinline__ Unit unit_at(const DevArgs& a, int32_t u) {
     const int32_t mid = (lo + hi + 1) >> 1;
     if (a.unit_start[mid] <= u) lo = mid; else hi = mid - 1;
   }
-  Unit x;
-  x.g = lo;
-  x.t0 = a.grp_t0[lo];
-  x.cnt = a.grp_cnt[lo];
-  x.b = a.tok_b[x.t0];
-  const int32_t vmax = a.tok_V[x.t0 + x.cnt - 1];
-  const int32_t tiles = (vmax + kTile - 1) / kTile;
-  x.tile0 = (u - a.unit_start[lo]) * kUnitTiles;
-  x.ntiles = min(kUnitTiles, tiles - x.tile0);
-  return x;
+  return unit_of_group(a, lo, u);
+}
+
+// Unit u, the one after x: the same group's next tiles while u is below the
+// next group's first unit, else the next group that has units.
+__device__ __forceinline__ Unit unit_after(const DevArgs& a, const Unit& x, int32_t u) {
+  int32_t g = x.g;
+  if (a.unit_start[g + 1] > u) {
+    Unit y = x;
+    y.tile0 = x.tile0 + kUnitTiles;
+    y.ntiles = min(kUnitTiles, x.tiles - y.tile0);
+    return y;
+  }
+  do { ++g; } while (a.unit_start[g + 1] <= u);
+  return unit_of_group(a, g, u);
+}
+
+// Whether unit u (of group g) is its group's last one in the range ending at ue.
+__device__ __forceinline__ bool group_ends(const DevArgs& a, int32_t g, int32_t u, int32_t ue) {
+  return u + 1 >= ue || a.unit_start[g + 1] <= u + 1;
 }
 
 // 18 warps: the four SM sub-partitions hold 5, 5, 4 and 4 of them in 16K
@@ -129,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t U = a.unit_start[a.Gmax];
-  if (static_cast<int32_t>(blockIdx.x) >= U) return;
+  const int32_t ub = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
+  const int32_t ue = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
+  if (ub >= ue) return;
 
   if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
   if (tid == 32) {
@@ -154,8 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   if (warp == 0) {
     // ---------------- producer: FP16 K tiles by TMA
     int k = 0;
-    for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x) {
-      const Unit x = unit_at(a, u);
+    Unit x{};
+    for (int32_t u = ub; u < ue && ok; ++u) {
+      x = u == ub ? unit_at(a, u) : unit_after(a, x, u);
       for (int i = 0; i < x.ntiles && ok; ++i, ++k) {
         const int s = k % kStages;
         const uint32_t ph = (k / kStages) & 1;
@@ -179,13 +209,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      int k = 0, n = 0;
+      int k = 0, n = -1;             // n: groups staged so far
       const uint32_t b0 = smem_u32(&S.b[0]);
-      for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
-        const Unit x = unit_at(a, u);
+      Unit x{};
+      for (int32_t u = ub; u < ue && ok; ++u) {
+        const bool first = u == ub;
+        x = first ? unit_at(a, u) : unit_after(a, x, u);
         const uint32_t nmma = static_cast<uint32_t>(x.cnt * a.N);
         const uint32_t idesc = idesc_f16_m128(nmma);
-        if (!mbar_wait_bounded<true>(&S.bfull, n & 1)) { ok = false; break; }
+        if (first || x.tile0 == 0) {   // a new group: its queries are staged by the epilogue
+          ++n;
+          if (!mbar_wait_bounded<true>(&S.bfull, n & 1)) { ok = false; break; }
+        }
         for (int i = 0; i < x.ntiles; ++i, ++k) {
           const int s = k % kStages, ds = k & 1;
           if (!mbar_wait_bounded<true>(&S.full[s], (k / kStages) & 1) ||
@@ -202,7 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           mma_commit(&S.empty[s]);
           mma_commit(&S.dfull[ds]);
         }
-        mma_commit(&S.bempty);   // the unit's queries are no longer read
+        // after the group's last unit in this range its queries are no
+        // longer read
+        if (group_ends(a, x.g, u, ue)) mma_commit(&S.bempty);
       }
       if (k > 0) (void)mbar_wait_drain(&S.dfull[(k - 1) & 1], ((k - 1) >> 1) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
@@ -218,12 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const int row = 32 * quarter + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
     const int etid = tid - 64;              // 0..511
-    int k = 0, n = 0;
-    for (int32_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++n) {
-      const Unit x = unit_at(a, u);
+    int k = 0, n = -1;               // n: groups staged so far
+    Unit x{};
+    for (int32_t u = ub; u < ue && ok; ++u) {
+      const bool first = u == ub;
+      x = first ? unit_at(a, u) : unit_after(a, x, u);
       const int nrows = x.cnt * a.N;
-      {
-        // the unit's queries and weights are loaded first (one global
+      if (first || x.tile0 == 0) {
+        ++n;
+        // a new group: its queries and weights are loaded first (one global
         // latency, overlapping the previous unit's last tiles), then stored
         // once the buffers are free
         constexpr int kPer = kMaxMmaN * 16 / 512;
@@ -244,10 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           qb = a.qs[o];
         }
         // before overwriting the queries and this parity's weights: every
-        // epilogue warp has loaded the previous unit's last tile (so it is
-        // done with the unit before that), and the previous unit's MMAs are
-        // complete
-        if (k > 0 && !mbar_wait_warp<true>(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) { ok = false; break; }
+        // epilogue warp has loaded this warp's last tile (the previous
+        // group's), so it is done with the group before that, and the
+        // previous group's MMAs are complete
+        if (k > 0 && !mbar_wait_warp<true>(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
         if (!mbar_wait_warp<true>(&S.bempty, (n & 1) ^ 1)) { ok = false; break; }
         if (etid < nrows) S.wq[n & 1][etid] = __hmul(__ushort_as_half(wb), __ushort_as_half(qb));
 #pragma unroll
@@ -258,12 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
             *reinterpret_cast<uint4*>(&S.b[sw128(nrows, nn, ch)]) =
                 a.fp8 ? e4m3x8_to_f16x8(v[i], true) : widen8(v[i], true);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.bfull);
+        // every warp's staging is complete (and visible) once bfull flips
+        if (!mbar_wait_warp<true>(&S.bfull, n & 1)) { ok = false; break; }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.bfull);
-      // every warp's staging is complete (and visible) once bfull flips
-      if (!mbar_wait_warp<true>(&S.bfull, n & 1)) { ok = false; break; }
 
       // the (up to two) tokens this warp sums, and the TMEM columns of each
       // 32-column half it loads
