@@ -21,7 +21,6 @@ constexpr int kBlock = 8;          // positions per candidate block
 constexpr int kMaxMmaN = 256;      // token-heads per tile (MMA N)
 constexpr int kMaxTopK = 2048;
 constexpr int kMaxCand = 2048;
-constexpr int kPrefillUnitTiles = 64;   // position tiles per prefill work unit
 constexpr int kSmemKeys = 44 * 1024;    // keys one selection CTA holds in shared memory
 constexpr int kLongChunk = 32768;       // row entries per CTA in the long-row passes
 constexpr int kLongChunkCap = 4096;     // candidates kept per chunk
@@ -66,7 +65,8 @@ struct DevArgs {
   int32_t* cand_cnt;   // [T] consumer: how many
   int32_t* cand_page;  // [T, C] consumer: the page holding each listed block (checked)
   uint4* cand_sc;      // [T, C] consumer: each listed block's eight FP16 K scales
-  int32_t* unit_start; // [T+1] stream path: first score tile of token t
+  int32_t* unit_start; // [T+1] stream path: first score tile of token t; group
+                       // path: [Gmax+1] first position tile of group g
   uint32_t* counter;   // consumer: CTAs done in the candidate kernel; group path: rows
                        // listed in flist (reset by plan)
   int32_t* flist;      // group path: [2T] rows (2t + which) left to the general selection

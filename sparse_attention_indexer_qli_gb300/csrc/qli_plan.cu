@@ -154,15 +154,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(DevArgs a) {
       }
     }
     __syncthreads();
-    // group g owns ceil(tiles/64) units of up to 64 tiles, where its last
-    // (most advanced) token sees ceil(V/128) tiles
+    // group g owns ceil(V/128) position tiles, V of its last (most
+    // advanced) token: unit_start is the tile prefix over the groups
     cta_scan_store<1024>(
         a.Gmax,
         [&](int32_t g) {
           const int32_t c = a.grp_cnt[g];
           if (c == 0) return 0;
-          const int32_t tiles = (a.tok_V[a.grp_t0[g] + c - 1] + kTile - 1) / kTile;
-          return (tiles + kPrefillUnitTiles - 1) / kPrefillUnitTiles;
+          return (a.tok_V[a.grp_t0[g] + c - 1] + kTile - 1) / kTile;
         },
         a.unit_start);
   }

@@ -7,9 +7,10 @@
 //    (a few MB per request: L2-resident while the main kernel runs);
 //  * prefill_kernel is persistent, one CTA per SM. A unit is one token group
 //    (up to 4 tokens of one request, MMA N = tokens*64 <= 256) and a range of
-//    up to 64 position tiles; a CTA takes a contiguous range of units, and a
-//    group's queries stay in shared memory (FP16 * 2^-10, 128-byte swizzle)
-//    across all of its units in the range; K tiles stream in
+//    its position tiles: the tiles of all groups are split evenly into one
+//    contiguous range per CTA, and a group's queries stay in shared memory
+//    (FP16 * 2^-10, 128-byte swizzle) across its part of the range; K tiles
+//    stream in
 //    by TMA (128-byte swizzle) through a 4-stage ring; the 128 x N FP32
 //    accumulator is double-buffered across all 512 TMEM columns.
 // Warp roles: warp 0 producer, warp 1 MMA issuer, warps 2-17 epilogue (four
@@ -29,7 +30,6 @@
 namespace qli {
 namespace {
 
-constexpr int kUnitTiles = kPrefillUnitTiles;
 constexpr int kStages = 4;
 constexpr int kThreads = 576;
 constexpr int kABytes = kTile * kHeadDim * 2;     // 32 KB FP16 tile (two 16 KB K halves)
@@ -98,53 +98,46 @@ __global__ void __launch_bounds__(kConvThreads) kconv_kernel(DevArgs a) {
         __half2float(*reinterpret_cast<const __half*>(pg + a.s_off + r * 2));
 }
 
-// ---- unit walk -----------------------------------------------------------
-// A CTA takes a contiguous range of the unit list, so its consecutive units
-// mostly belong to one token group: the group's queries are staged once for
-// all of them, and the next unit is found from the current one.
-struct Unit {
-  int32_t g, t0, cnt, b, tile0, ntiles, tiles;
+// ---- work walk -----------------------------------------------------------
+// The position tiles of all token groups, group after group, are split into
+// one contiguous range per CTA (equal within one tile). A CTA walks its range
+// as segments, one per group: the group's queries are staged once for the
+// segment, whose tiles then stream through.
+struct Seg {
+  int32_t g, t0, cnt, b, tile0, ntiles, end;   // end: the group's end in the tile list
 };
 
-__device__ __forceinline__ Unit unit_of_group(const DevArgs& a, int32_t g, int32_t u) {
-  Unit x;
+// Group g's part of the range [tb, te).
+__device__ __forceinline__ Seg seg_of_group(const DevArgs& a, int32_t g, int32_t tb, int32_t te) {
+  Seg x;
   x.g = g;
   x.t0 = a.grp_t0[g];
   x.cnt = a.grp_cnt[g];
   x.b = a.tok_b[x.t0];
-  const int32_t vmax = a.tok_V[x.t0 + x.cnt - 1];
-  x.tiles = (vmax + kTile - 1) / kTile;
-  x.tile0 = (u - a.unit_start[g]) * kUnitTiles;
-  x.ntiles = min(kUnitTiles, x.tiles - x.tile0);
+  const int32_t s0 = a.unit_start[g];
+  x.end = a.unit_start[g + 1];
+  const int32_t lo = max(tb, s0);
+  x.tile0 = lo - s0;
+  x.ntiles = min(te, x.end) - lo;
   return x;
 }
 
-__device__ __forceinline__ Unit unit_at(const DevArgs& a, int32_t u) {
+// The first segment: the group holding tile tb (the last group starting at
+// or before it; groups without tiles start where the next one does).
+__device__ __forceinline__ Seg seg_first(const DevArgs& a, int32_t tb, int32_t te) {
   int32_t lo = 0, hi = a.Gmax - 1;
   while (lo < hi) {
     const int32_t mid = (lo + hi + 1) >> 1;
-    if (a.unit_start[mid] <= u) lo = mid; else hi = mid - 1;
+    if (a.unit_start[mid] <= tb) lo = mid; else hi = mid - 1;
   }
-  return unit_of_group(a, lo, u);
+  return seg_of_group(a, lo, tb, te);
 }
 
-// Unit u, the one after x: the same group's next tiles while u is below the
-// next group's first unit, else the next group that has units.
-__device__ __forceinline__ Unit unit_after(const DevArgs& a, const Unit& x, int32_t u) {
-  int32_t g = x.g;
-  if (a.unit_start[g + 1] > u) {
-    Unit y = x;
-    y.tile0 = x.tile0 + kUnitTiles;
-    y.ntiles = min(kUnitTiles, x.tiles - y.tile0);
-    return y;
-  }
-  do { ++g; } while (a.unit_start[g + 1] <= u);
-  return unit_of_group(a, g, u);
-}
-
-// Whether unit u (of group g) is its group's last one in the range ending at ue.
-__device__ __forceinline__ bool group_ends(const DevArgs& a, int32_t g, int32_t u, int32_t ue) {
-  return u + 1 >= ue || a.unit_start[g + 1] <= u + 1;
+// The segment after x, when x.end < te: the next group with tiles.
+__device__ __forceinline__ Seg seg_next(const DevArgs& a, const Seg& x, int32_t te) {
+  int32_t g = x.g + 1;
+  while (a.unit_start[g + 1] <= x.end) ++g;
+  return seg_of_group(a, g, x.end, te);
 }
 
 // 18 warps: the four SM sub-partitions hold 5, 5, 4 and 4 of them in 16K
@@ -155,10 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   Smem& S = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int32_t U = a.unit_start[a.Gmax];
-  const int32_t ub = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
-  const int32_t ue = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
-  if (ub >= ue) return;
+  const int32_t U = a.unit_start[a.Gmax];   // position tiles of all groups
+  const int32_t tb = static_cast<int32_t>(static_cast<int64_t>(U) * blockIdx.x / gridDim.x);
+  const int32_t te = static_cast<int32_t>(static_cast<int64_t>(U) * (blockIdx.x + 1) / gridDim.x);
+  if (tb >= te) return;
 
   if (warp == 0) tmem_alloc(&S.tmem_base, kTmemCols);
   if (tid == 32) {
@@ -183,9 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   if (warp == 0) {
     // ---------------- producer: FP16 K tiles by TMA
     int k = 0;
-    Unit x{};
-    for (int32_t u = ub; u < ue && ok; ++u) {
-      x = u == ub ? unit_at(a, u) : unit_after(a, x, u);
+    for (Seg x = seg_first(a, tb, te); ok; x = seg_next(a, x, te)) {
       for (int i = 0; i < x.ntiles && ok; ++i, ++k) {
         const int s = k % kStages;
         const uint32_t ph = (k / kStages) & 1;
@@ -200,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      if (x.end >= te) break;
     }
     if (lane == 0) {
       for (int j = max(0, k - kStages); j < k; ++j)
@@ -209,18 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      int k = 0, n = -1;             // n: groups staged so far
+      int k = 0, n = 0;              // n: segments (groups) so far
       const uint32_t b0 = smem_u32(&S.b[0]);
-      Unit x{};
-      for (int32_t u = ub; u < ue && ok; ++u) {
-        const bool first = u == ub;
-        x = first ? unit_at(a, u) : unit_after(a, x, u);
+      for (Seg x = seg_first(a, tb, te); ok; x = seg_next(a, x, te), ++n) {
         const uint32_t nmma = static_cast<uint32_t>(x.cnt * a.N);
         const uint32_t idesc = idesc_f16_m128(nmma);
-        if (first || x.tile0 == 0) {   // a new group: its queries are staged by the epilogue
-          ++n;
-          if (!mbar_wait_bounded<true>(&S.bfull, n & 1)) { ok = false; break; }
-        }
+        // the group's queries, staged by the epilogue warps
+        if (!mbar_wait_bounded<true>(&S.bfull, n & 1)) { ok = false; break; }
         for (int i = 0; i < x.ntiles; ++i, ++k) {
           const int s = k % kStages, ds = k & 1;
           if (!mbar_wait_bounded<true>(&S.full[s], (k / kStages) & 1) ||
@@ -237,9 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           mma_commit(&S.empty[s]);
           mma_commit(&S.dfull[ds]);
         }
-        // after the group's last unit in this range its queries are no
-        // longer read
-        if (group_ends(a, x.g, u, ue)) mma_commit(&S.bempty);
+        mma_commit(&S.bempty);   // the group's queries are no longer read
+        if (x.end >= te) break;
       }
       if (k > 0) (void)mbar_wait_drain(&S.dfull[(k - 1) & 1], ((k - 1) >> 1) & 1);
       if (!ok) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
@@ -255,16 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
     const int row = 32 * quarter + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
     const int etid = tid - 64;              // 0..511
-    int k = 0, n = -1;               // n: groups staged so far
-    Unit x{};
-    for (int32_t u = ub; u < ue && ok; ++u) {
-      const bool first = u == ub;
-      x = first ? unit_at(a, u) : unit_after(a, x, u);
+    int k = 0, n = 0;                // n: segments (groups) so far
+    for (Seg x = seg_first(a, tb, te); ok; x = seg_next(a, x, te), ++n) {
       const int nrows = x.cnt * a.N;
-      if (first || x.tile0 == 0) {
-        ++n;
-        // a new group: its queries and weights are loaded first (one global
-        // latency, overlapping the previous unit's last tiles), then stored
+      {
+        // the group's queries and weights are loaded first (one global
+        // latency, overlapping the previous group's last tiles), then stored
         // once the buffers are free
         constexpr int kPer = kMaxMmaN * 16 / 512;
         uint2 v[kPer];
@@ -285,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
         }
         // before overwriting the queries and this parity's weights: every
         // epilogue warp has loaded this warp's last tile (the previous
-        // group's), so it is done with the group before that, and the
-        // previous group's MMAs are complete
+        // segment's), so it is done with the segment before that, and the
+        // previous segment's MMAs are complete
         if (k > 0 && !mbar_wait_warp<true>(&S.dempty[(k - 1) & 1], ((k - 1) >> 1) & 1)) {
           ok = false;
           break;
@@ -385,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(
           if (has1) emit(chain(0.0f, r, w1), ks, pos, V1, srow1, brow1);
         }
       }
+      if (x.end >= te) break;
     }
     if (!ok && lane == 0) atomicOr(a.err, QLI_DEVERR_TIMEOUT);
   }
