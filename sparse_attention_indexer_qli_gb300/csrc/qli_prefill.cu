@@ -68,34 +68,62 @@ __device__ __forceinline__ uint4 widen8(uint2 v, bool div1024) {
   return r;
 }
 
-// ---- K widening: one thread per 8 INT8 values, 16 threads per row ---------
+// ---- K widening: a CTA per 128-row tile of a request, 8 threads per row
+// (16 INT8 values each) and 4 rows per thread; every load of the tile is in
+// flight before the first conversion, so the kernel takes one pass of three
+// round trips (length, block table, rows) instead of waves of them
 constexpr int kConvThreads = 256;
+constexpr int kConvRows = kTile;                        // rows per CTA
+constexpr int kConvRPT = kConvRows / (kConvThreads / 8);  // rows per thread
 
 __global__ void __launch_bounds__(kConvThreads) kconv_kernel(DevArgs a) {
   const int b = blockIdx.y;
   const int lk = a.req_lk[b];
-  const int row = blockIdx.x * (kConvThreads / 16) + threadIdx.x / 16;
-  const int ch = threadIdx.x % 16;
+  const int row0 = blockIdx.x * kConvRows;
   const int padded = (lk + kTile - 1) / kTile * kTile;
-  if (row >= padded) return;
-  uint4* dst = reinterpret_cast<uint4*>(a.kf16 + (static_cast<int64_t>(b) * a.kstride + row) * kHeadDim) + ch;
-  if (row >= lk) {   // zero tail of the last tile
-    *dst = make_uint4(0, 0, 0, 0);
-    if (ch == 0) a.ks32[static_cast<int64_t>(b) * a.kstride + row] = 0.0f;
-    return;
+  if (row0 >= padded) return;
+  const int ch = threadIdx.x & 7;                       // 16-byte piece of the row
+  const int rsub = threadIdx.x >> 3;                    // 0..31
+  const int64_t base = static_cast<int64_t>(b) * a.kstride;
+  int32_t page[kConvRPT];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kConvRPT; ++i) {
+    const int row = row0 + rsub + 32 * i;
+    page[i] = row < lk ? a.bt[static_cast<int64_t>(b) * a.bt_stride + row / a.R] : 0;
   }
-  int32_t page = a.bt[static_cast<int64_t>(b) * a.bt_stride + row / a.R];
-  if (page < 0 || page >= a.num_pages) {
-    if (ch == 0) atomicOr(a.err, QLI_DEVERR_PAGE);
-    page = 0;
+  uint4 v[kConvRPT];
+  uint16_t sc[kConvRPT];
+#pragma unroll
+  for (int i = 0; i < kConvRPT; ++i) {
+    const int row = row0 + rsub + 32 * i;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    sc[i] = 0;
+    if (row < lk) {
+      if (page[i] < 0 || page[i] >= a.num_pages) {
+        bad = true;
+        page[i] = 0;
+      }
+      const uint8_t* pg = a.cache + static_cast<int64_t>(page[i]) * a.page_stride;
+      const int r = row % a.R;
+      v[i] = __ldg(reinterpret_cast<const uint4*>(pg + a.k_off + r * kHeadDim) + ch);
+      if (ch == 0) sc[i] = __ldg(reinterpret_cast<const uint16_t*>(pg + a.s_off) + r);
+    }
   }
-  const uint8_t* pg = a.cache + static_cast<int64_t>(page) * a.page_stride;
-  const int r = row % a.R;
-  const uint2 v = __ldg(reinterpret_cast<const uint2*>(pg + a.k_off + r * kHeadDim) + ch);
-  *dst = a.fp8 ? e4m3x8_to_f16x8(v, false) : widen8(v, false);
-  if (ch == 0)
-    a.ks32[static_cast<int64_t>(b) * a.kstride + row] =
-        __half2float(*reinterpret_cast<const __half*>(pg + a.s_off + r * 2));
+  if (bad && ch == 0) atomicOr(a.err, QLI_DEVERR_PAGE);
+#pragma unroll
+  for (int i = 0; i < kConvRPT; ++i) {
+    const int row = row0 + rsub + 32 * i;
+    if (row >= padded) continue;
+    // rows past the request's length are the zero tail of the last tile
+    uint4* dst = reinterpret_cast<uint4*>(a.kf16 + (base + row) * kHeadDim) + 2 * ch;
+    const uint2 lo = make_uint2(v[i].x, v[i].y), hi = make_uint2(v[i].z, v[i].w);
+    const bool live = row < lk;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    dst[0] = live ? (a.fp8 ? e4m3x8_to_f16x8(lo, false) : widen8(lo, false)) : z;
+    dst[1] = live ? (a.fp8 ? e4m3x8_to_f16x8(hi, false) : widen8(hi, false)) : z;
+    if (ch == 0) a.ks32[base + row] = live ? __half2float(__ushort_as_half(sc[i])) : 0.0f;
+  }
 }
 
 // ---- work walk -----------------------------------------------------------
@@ -414,15 +442,15 @@ std::atomic<uint64_t> g_smem_prefill_kernel{0};
 
 cudaError_t launch_prefill(const DevArgs& d, cudaStream_t s) {
   if (d.T == 0 || d.B == 0) return cudaSuccess;
-  const int rows_per_cta = kConvThreads / 16;
-  dim3 cgrid(static_cast<unsigned>((d.kstride + rows_per_cta - 1) / rows_per_cta),
+  dim3 cgrid(static_cast<unsigned>((d.kstride + kConvRows - 1) / kConvRows),
              static_cast<unsigned>(d.B));
   kconv_kernel<<<cgrid, kConvThreads, 0, s>>>(d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap tm;
   if (!encode_kf16_map(d, &tm)) return cudaErrorInvalidValue;
-  e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes, g_smem_prefill_kernel);
+  e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_kernel), kSmemBytes,
+                        g_smem_prefill_kernel);
   if (e != cudaSuccess) return e;
   prefill_kernel<<<d.num_sms, kThreads, kSmemBytes, s>>>(tm, d);
   return cudaGetLastError();
