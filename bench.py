@@ -41,6 +41,7 @@ SCORE_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "ql
 PREFILL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_prefill.cu")
 ATTN_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_attn.cu")
 SMALL_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_small.cu")
+QUANT_SRC = os.path.join(ROOT, "sparse_attention_indexer_qli_gb300", "csrc", "qli_quant.cu")
 # workload -> (committed ncu summary, the kernel source it was taken on)
 PROFILES = {
     # one token: the single-launch path (its kernel also selects)
@@ -51,6 +52,8 @@ PROFILES = {
     # captured on 2 of the 8 1M-context requests and scaled by scored pairs
     5: ("stream_kernel_longctx_2of8x1M.md", SCORE_SRC, "stream_source_sha256"),
     "attn": ("attn_kernel_decode_b64_h64_topk2048.md", ATTN_SRC, "attn_source_sha256"),
+    "quantize_q": ("quant_kernel_queries_t4096_n64.md", QUANT_SRC, "quant_source_sha256"),
+    "write_index_k": ("quant_kernel_index_k_2x32768.md", QUANT_SRC, "quant_source_sha256"),
 }
 
 
@@ -745,7 +748,7 @@ def run_op(args):
     achieved = op_bytes(op, rows) / (per_ms / 1e3) / 1e9
     peak, kind = peaks()
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": None, "kernel": "quant_kernel",
+            "frac": achieved / peak, "traffic": profiled_traffic(op), "kernel": "quant_kernel",
             "peak_source": kind, "kernel_ms": per_ms, "algorithmic_bytes": op_bytes(op, rows)}
 
     # e2e: inputs from pinned host memory, outputs (codes and scales) back
