@@ -60,7 +60,7 @@ def test_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic(2) is None
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, "attn"])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, "attn", "quantize_q", "write_index_k"])
 def test_committed_summaries_name_their_source_and_traffic(idx):
     import bench
     name, src, key = bench.PROFILES[idx]
