@@ -443,3 +443,40 @@ def test_prefill_rows_past_the_shared_memory_limit_take_the_long_row_passes():
     assert case.T > 2 * case.B
     assert int(case.k_lens.max()) > 44 * 1024
     check(case)
+
+
+def _fuzz_cases(n=40, seed=20261203):
+    """A seeded sweep of small batches beyond the hand-picked ones: ratio 1
+    or 2, 32 or 64 heads, every candidate mode, one to four requests of
+    contexts from empty to 9000 raw tokens (some shorter than their query
+    run), decode-shaped (one query per request) or prefill-shaped (up to 24),
+    TopK from 1 to 2048 and 64 to 1024 candidate blocks, consumer lists valid
+    or messy. Together they take the small-batch, stream and group paths."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 5))
+        ratio = int(rng.integers(1, 3))
+        N = int(rng.choice([32, 64]))
+        mode = str(rng.choice(["none", "source", "consumer"]))
+        raw = rng.integers(0, 9001, size=B)
+        tiny = rng.random(B) < 0.2
+        raw[tiny] = rng.integers(0, 40, size=int(tiny.sum()))
+        ql = np.ones(B, dtype=np.int64) if rng.random() < 0.5 else rng.integers(1, 25, size=B)
+        topk = int(rng.choice([1, 7, 64, 300, 1024, 2048]))
+        C = int(rng.integers(1, 17)) * 64 if mode != "none" else 0
+        policy = "messy" if mode == "consumer" and rng.random() < 0.5 else "valid"
+        out.append(("fuzz%02d-%s-r%d-n%d" % (i, mode, ratio, N), int(rng.integers(0, 1 << 30)),
+                    raw.tolist(), ql.tolist(), N, ratio, topk, mode, C, policy))
+    return out
+
+
+FUZZ = _fuzz_cases()
+
+
+@pytest.mark.parametrize("p", FUZZ, ids=[p[0] for p in FUZZ])
+def test_parity_seeded_sweep(p):
+    name, seed, raw, ql, N, ratio, topk, mode, C, policy = p
+    case = synth.make_case(seed, raw, ql, N=N, ratio=ratio, topk=topk, cand_mode=mode,
+                           cand_blocks=C, cand_policy=policy, name=name)
+    check(case)
