@@ -151,3 +151,35 @@ def test_attention_full_size_workload_sampled():
     2048 listed positions each); the oracle checks eight sampled tokens."""
     case = synth.attention_workload(seed=21)
     check(case, tokens=[0, 7, 15, 22, 31, 40, 51, 63])
+
+
+def _fuzz_cases(n=16, seed=20261205):
+    """A seeded sweep of small attention calls: ratio (page geometry), 32 to
+    128 heads, one to three requests up to 6000 raw tokens with one to four
+    tokens each, 1 to 2048 listed entries, list lengths drawn below that
+    (some rows listing nothing), and a softmax scale from 1/sqrt(512) up."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 4))
+        ratio = int(rng.integers(1, 3))
+        H = int(rng.choice([32, 64, 96, 128]))
+        raw = rng.integers(1, 6001, size=B)
+        ql = rng.integers(1, 5, size=B)
+        K = int(rng.choice([1, 40, 129, 512, 2048]))
+        lo = int(rng.integers(0, K + 1))
+        scale = float(SCALE * rng.choice([1.0, 1.0, 4.0, 16.0]))
+        out.append(("attnfuzz%02d-r%d-h%d-k%d" % (i, ratio, H, K), int(rng.integers(0, 1 << 30)),
+                    raw.tolist(), ql.tolist(), ratio, H, K, (lo, K), scale))
+    return out
+
+
+FUZZ = _fuzz_cases()
+
+
+@pytest.mark.parametrize("p", FUZZ, ids=[p[0] for p in FUZZ])
+def test_attention_parity_seeded_sweep(p):
+    name, seed, raw, ql, ratio, H, K, count, scale = p
+    case = synth.make_case(seed, raw, ql, N=64, ratio=ratio, topk=16, name=name)
+    synth.add_attention(case, H=H, topk=K, count=count)
+    check(case, scale=scale)

@@ -149,3 +149,34 @@ def test_fp8_and_int8_bytes_give_different_scores():
     b.run(ws)
     torch.cuda.synchronize()
     assert not torch.equal(s8, b.scores(ws)[0, :1500])
+
+
+def _fuzz_cases(n=16, seed=20261204):
+    """A seeded sweep of small E4M3 batches: ratio, head count, candidate
+    mode, one to three requests up to 6000 raw tokens, decode- or
+    prefill-shaped, TopK and candidate counts drawn at random."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        B = int(rng.integers(1, 4))
+        ratio = int(rng.integers(1, 3))
+        N = int(rng.choice([32, 64]))
+        mode = str(rng.choice(["none", "source", "consumer"]))
+        raw = rng.integers(0, 6001, size=B)
+        ql = np.ones(B, dtype=np.int64) if rng.random() < 0.5 else rng.integers(1, 17, size=B)
+        topk = int(rng.choice([1, 33, 256, 2048]))
+        C = int(rng.integers(1, 9)) * 64 if mode != "none" else 0
+        out.append(("fp8fuzz%02d-%s-r%d-n%d" % (i, mode, ratio, N), int(rng.integers(0, 1 << 30)),
+                    raw.tolist(), ql.tolist(), N, ratio, topk, mode, C))
+    return out
+
+
+FUZZ = _fuzz_cases()
+
+
+@pytest.mark.parametrize("p", FUZZ, ids=[p[0] for p in FUZZ])
+def test_fp8_parity_seeded_sweep(p):
+    name, seed, raw, ql, N, ratio, topk, mode, C = p
+    case = synth.make_case(seed, raw, ql, N=N, ratio=ratio, topk=topk, cand_mode=mode,
+                           cand_blocks=C, name=name)
+    check(synth.to_fp8(case))
