@@ -146,11 +146,10 @@ def test_attention_after_the_indexer():
         assert np.all(np.abs(o_g[t] - o_r[t]) <= ATOL_REL_KV * kvmax + RTOL * np.abs(o_r[t]))
 
 
-def test_attention_full_size_workload_sampled():
+def test_attention_full_size_workload():
     """The bench workload (64 decode tokens of the ratio-1 batch, 64 heads,
-    2048 listed positions each); the oracle checks eight sampled tokens."""
-    case = synth.attention_workload(seed=21)
-    check(case, tokens=[0, 7, 15, 22, 31, 40, 51, 63])
+    2048 listed positions each), every token checked against the oracle."""
+    check(synth.attention_workload(seed=21))
 
 
 def _fuzz_cases(n=16, seed=20261205):
